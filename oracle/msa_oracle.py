@@ -1,0 +1,374 @@
+"""CPU oracle for MInference-style dynamic sparse prefill attention (fp64, numpy).
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path imports this module:
+only the tests, the package smoke check and the CPU-baseline leg of the
+benchmark may call it.  It shares no code with the CUDA path.
+
+Every function restates one step of the method in plain numpy, in float64,
+from bf16 inputs converted exactly.  Sources, by page title and section:
+
+* [MInf-1]  MInference 1.0 overview (developer.volcengine.com article),
+            section 1 "Problem Formulation": A(M) = Softmax(Q K^T / sqrt(d) - c (1 - M)) V
+            with a binary dynamic mask M, a scale of sqrt(d) and a constant c that
+            drives masked entries to ~0 after the softmax.
+* [MInf-2.2] same page, section 2.2 "Sparsity Indices Approximation and Dynamic
+            Sparse Attention Calculation": the vertical-slash head (estimate A-hat
+            from a matmul of the last queries with all keys, pick the vertical
+            and slash index sets, convert them to a sparse format, run
+            block-sparse attention) and the block-sparse head (mean-pool Q and
+            K, block-level weights, top-k block index, sparse attention).
+* [MInf-API] same page, the "using only the kernel" listing: the entry points
+            vertical_slash_sparse_attention(q,k,v,vertical_topk,slash),
+            block_sparse_attention(q,k,v,topk) and
+            streaming_forward(q,k,v,init_num,local_window_num).
+* [KV-1.5x] "How KV sparsity achieves 1.5x acceleration for vLLM" (Novita AI
+            blog), section "Key Techniques / 2. Attention modification": the
+            token score is a sum of softmax probabilities over a window of the
+            last queries, computed from the row max and the row sum l.
+
+Readings where the pages are silent or garbled (each one is listed in the
+design notes with its reason):
+
+* masked entries are excluded exactly (c -> infinity); a row with no allowed
+  key outputs zeros;
+* the estimate uses the last ``last_q`` (default 64) query rows with a causal
+  softmax over every key j <= i;
+* the vertical score of key j is the column sum of A-hat, the slash score of
+  offset o = i - j is the sum of A-hat along that diagonal, o in [0, N);
+* top-k orders by score descending, ties to the lower index, and returns the
+  chosen indices in ascending order; k is clamped to the number of candidates;
+* the sparse format expands every selected diagonal to the 64x64 key tiles it
+  crosses and keeps vertical columns that no active tile of the row block
+  already covers;
+* the block-sparse head keeps the diagonal block plus the top-(topk-1) earlier
+  blocks by pooled score; streaming keeps blocks [0, init_num) and the
+  ``local_window_num`` blocks ending at the query's own block;
+* query head h reads KV head h // (Hq / Hkv).
+
+Parity pins for every function live in tests/test_oracle_*.py.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+BLOCK = 64
+
+
+# ----------------------------------------------------------------------------- helpers
+def as_f64(x) -> np.ndarray:
+    """bf16/fp32 torch tensor or array -> float64 numpy array (exact widening)."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            return x.detach().to("cpu", torch.float64).numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.asarray(x, dtype=np.float64)
+
+
+def default_scale(d: int) -> float:
+    """1 / sqrt(d) [MInf-1]."""
+    return 1.0 / np.sqrt(d)
+
+
+# ----------------------------------------------------------------------------- attention given a mask
+def attend_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, rows, allowed_keys, scale: float):
+    """Masked softmax attention for selected query rows [MInf-1].
+
+    q, k, v: [N, d] float64 for one query head and its KV head.
+    rows: iterable of query indices i.
+    allowed_keys(i) -> 1-D integer array (or boolean mask over [0, N)) of the keys
+    the mask M admits for row i; keys j > i are removed here (causal).
+    Returns out [len(rows), d] and the per-row key counts |J_i|.
+
+    A masked entry gets weight exactly 0 (c -> infinity); a row with no admitted
+    key outputs zeros.
+    """
+    rows = list(rows)
+    d = q.shape[1]
+    out = np.zeros((len(rows), d), dtype=np.float64)
+    counts = np.zeros(len(rows), dtype=np.int64)
+    for r, i in enumerate(rows):
+        J = np.asarray(allowed_keys(i))
+        if J.dtype == bool:
+            J = np.nonzero(J)[0]
+        J = J[J <= i]
+        counts[r] = J.size
+        if J.size == 0:
+            continue
+        z = (k[J] @ q[i]) * scale
+        p = np.exp(z - z.max())
+        p /= p.sum()
+        out[r] = p @ v[J]
+    return out, counts
+
+
+def attend_blocks(q, k, v, block_mask, scale: float):
+    """Masked softmax attention for all rows, mask given per 64-row block.
+
+    block_mask(m) -> boolean [N] over keys admitted for every row of row block m
+    (the causal cut j <= i is applied per row here).  Same arithmetic as
+    attend_rows, evaluated 64 rows at a time.
+    """
+    N, d = q.shape
+    out = np.zeros((N, d), dtype=np.float64)
+    counts = np.zeros(N, dtype=np.int64)
+    for m in range((N + BLOCK - 1) // BLOCK):
+        r0, r1 = m * BLOCK, min(N, (m + 1) * BLOCK)
+        allow = np.asarray(block_mask(m), dtype=bool)[:r1]
+        idx = np.arange(r1)
+        M = np.broadcast_to(allow, (r1 - r0, r1)) & (idx[None, :] <= np.arange(r0, r1)[:, None])
+        counts[r0:r1] = M.sum(1)
+        z = (q[r0:r1] @ k[:r1].T) * scale
+        z = np.where(M, z, -np.inf)
+        zmax = z.max(1, keepdims=True)
+        zmax = np.where(np.isfinite(zmax), zmax, 0.0)
+        p = np.exp(z - zmax)
+        den = p.sum(1, keepdims=True)
+        res = p @ v[:r1]
+        out[r0:r1] = np.divide(res, den, out=np.zeros_like(res), where=den > 0)
+    return out, counts
+
+
+def dense_causal(q, k, v, scale: float):
+    """Dense causal attention: the all-ones mask [MInf-1]."""
+    N = q.shape[0]
+    return attend_blocks(q, k, v, lambda m: np.ones(N, dtype=bool), scale)[0]
+
+
+# ----------------------------------------------------------------------------- vertical-slash head
+def estimate_vs(q, k, last_q: int, scale: float):
+    """Estimated attention of the last queries and its line scores [MInf-2.2], [KV-1.5x].
+
+    A-hat[r, j] = softmax over j <= i of scale * q_i . k_j, for the rows
+    i = N - L + r, L = min(last_q, N).  Returns (v_score [N], s_score [N], A_hat [L, N]):
+    v_score[j] = sum over rows of A-hat[r, j]            (vertical line j)
+    s_score[o] = sum over rows of A-hat[r, i - o], i-o>=0 (slash line, offset o)
+    """
+    N = q.shape[0]
+    L = min(last_q, N)
+    rows = np.arange(N - L, N)
+    z = (q[rows] @ k.T) * scale
+    keys = np.arange(N)
+    causal = keys[None, :] <= rows[:, None]
+    z = np.where(causal, z, -np.inf)
+    m = z.max(1, keepdims=True)
+    e = np.exp(z - m)
+    ell = e.sum(1, keepdims=True)
+    A = e / ell
+    v_score = A.sum(0)
+    s_score = np.zeros(N, dtype=np.float64)
+    for r, i in enumerate(rows):
+        # keys j = i, i-1, ..., 0 lie on offsets o = 0, 1, ..., i
+        s_score[: i + 1] += A[r, i::-1]
+    return v_score, s_score, A
+
+
+def topk_indices(scores, k: int) -> np.ndarray:
+    """Top-k by score descending, ties to the lower index; returned ascending."""
+    scores = np.asarray(scores, dtype=np.float64)
+    k = int(min(max(k, 0), scores.size))
+    order = np.argsort(-scores, kind="stable")
+    return np.sort(order[:k]).astype(np.int64)
+
+
+def vs_active_tiles(slash_idx, N: int) -> np.ndarray:
+    """64x64 tiles crossed by the selected diagonals [MInf-2.2] (sparse format, tile part).
+
+    Tile (m, n), n <= m, is active iff some selected offset o has a row
+    i in [64m, 64m+63] with i - o inside key tile n, i.e. iff the key range
+    [64m - o, 64m + 63 - o] (cut at 0) meets [64n, 64n + 63].
+    Returns a boolean [NB, NB] matrix (row block m, key block n).
+    """
+    NB = (N + BLOCK - 1) // BLOCK
+    S = np.asarray(slash_idx, dtype=np.int64)
+    active = np.zeros((NB, NB), dtype=bool)
+    for m in range(NB):
+        first_row = m * BLOCK
+        last_row = min(N, (m + 1) * BLOCK) - 1
+        lo = first_row - S
+        hi = last_row - S
+        keep = hi >= 0
+        lo = np.maximum(lo[keep], 0)
+        hi = hi[keep]
+        for n_lo, n_hi in zip(lo // BLOCK, hi // BLOCK):
+            active[m, n_lo:n_hi + 1] = True
+    return active
+
+
+def vs_columns(vertical_idx, active: np.ndarray, N: int):
+    """Column part of the sparse format [MInf-2.2]: per row block m, the selected
+    vertical keys j <= last row of m whose key tile is not active for m; ascending."""
+    V = np.asarray(vertical_idx, dtype=np.int64)
+    NB = active.shape[0]
+    cols = []
+    for m in range(NB):
+        last_row = min(N, (m + 1) * BLOCK) - 1
+        c = V[V <= last_row]
+        c = c[~active[m, c // BLOCK]]
+        cols.append(c)
+    return cols
+
+
+def vs_block_mask(active, cols, N):
+    """Keys admitted for row block m: active tiles plus the block's columns."""
+    def mask(m):
+        allow = np.repeat(active[m], BLOCK)[:N].copy()
+        allow[cols[m]] = True
+        return allow
+    return mask
+
+
+def vertical_slash_indices(q, k, vertical_topk: int, slash: int, last_q: int = 64,
+                           scale: float | None = None):
+    """Index construction of one vertical-slash head [MInf-2.2]."""
+    N, d = q.shape
+    scale = default_scale(d) if scale is None else scale
+    v_score, s_score, _ = estimate_vs(q, k, last_q, scale)
+    V = topk_indices(v_score, vertical_topk)
+    S = topk_indices(s_score, slash)
+    active = vs_active_tiles(S, N)
+    cols = vs_columns(V, active, N)
+    return {"v_score": v_score, "s_score": s_score, "vertical": V, "slash": S,
+            "active": active, "columns": cols}
+
+
+def vertical_slash_head(q, k, v, vertical_topk: int, slash: int, last_q: int = 64,
+                        scale: float | None = None):
+    """One vertical-slash head end to end: indices, then block-sparse attention."""
+    N, d = q.shape
+    scale = default_scale(d) if scale is None else scale
+    idx = vertical_slash_indices(q, k, vertical_topk, slash, last_q, scale)
+    out, counts = attend_blocks(q, k, v, vs_block_mask(idx["active"], idx["columns"], N), scale)
+    idx["nnz"] = int(counts.sum())
+    return out, idx
+
+
+# ----------------------------------------------------------------------------- block-sparse head
+def mean_pool(x, N: int):
+    """Mean over each 64-row block [MInf-2.2] (block-sparse head, step 1)."""
+    NB = (N + BLOCK - 1) // BLOCK
+    return np.stack([x[m * BLOCK:min(N, (m + 1) * BLOCK)].mean(0) for m in range(NB)])
+
+
+def block_scores(q, k, scale: float):
+    """Pooled block logits scale * Qhat_m . Khat_n (before the row softmax) [MInf-2.2]."""
+    N = q.shape[0]
+    return (mean_pool(q, N) @ mean_pool(k, N).T) * scale
+
+
+def block_sparse_blocks(q, k, topk: int, scale: float | None = None):
+    """Selected key blocks per row block [MInf-2.2]: the diagonal block plus the
+    top-(topk-1) earlier blocks by pooled score (ties to the lower block);
+    min(topk, m+1) blocks, ascending."""
+    N, d = q.shape
+    scale = default_scale(d) if scale is None else scale
+    S = block_scores(q, k, scale)
+    NB = S.shape[0]
+    sel = []
+    for m in range(NB):
+        earlier = topk_indices(S[m, :m], max(topk - 1, 0)) if m > 0 else np.zeros(0, np.int64)
+        sel.append(np.sort(np.concatenate([earlier, [m]]).astype(np.int64)))
+    return sel, S
+
+
+def block_mask_from_blocks(sel, N):
+    def mask(m):
+        allow = np.zeros(((N + BLOCK - 1) // BLOCK) * BLOCK, dtype=bool)
+        for n in sel[m]:
+            allow[n * BLOCK:(n + 1) * BLOCK] = True
+        return allow[:N]
+    return mask
+
+
+def block_sparse_head(q, k, v, topk: int, scale: float | None = None):
+    N, d = q.shape
+    scale = default_scale(d) if scale is None else scale
+    sel, S = block_sparse_blocks(q, k, topk, scale)
+    out, counts = attend_blocks(q, k, v, block_mask_from_blocks(sel, N), scale)
+    return out, {"blocks": sel, "block_scores": S, "nnz": int(counts.sum())}
+
+
+# ----------------------------------------------------------------------------- streaming head
+def streaming_blocks(m: int, init_num: int, local_window_num: int) -> np.ndarray:
+    """Key blocks of row block m for the streaming / A-shape head [MInf-API]:
+    the sink blocks [0, init_num) and the local window [m - local + 1, m], cut at
+    [0, m], without repeats, ascending."""
+    sink = set(range(0, min(init_num, m + 1)))
+    local = set(range(max(0, m - local_window_num + 1), m + 1))
+    return np.array(sorted(sink | local), dtype=np.int64)
+
+
+def streaming_head(q, k, v, init_num: int, local_window_num: int, scale: float | None = None):
+    N, d = q.shape
+    scale = default_scale(d) if scale is None else scale
+    NB = (N + BLOCK - 1) // BLOCK
+    sel = [streaming_blocks(m, init_num, local_window_num) for m in range(NB)]
+    out, counts = attend_blocks(q, k, v, block_mask_from_blocks(sel, N), scale)
+    return out, {"blocks": sel, "nnz": int(counts.sum())}
+
+
+# ----------------------------------------------------------------------------- multi-head entry points
+def _kv_head(h: int, n_q: int, n_kv: int) -> int:
+    return h // (n_q // n_kv)
+
+
+def vertical_slash_sparse_attention(q, k, v, vertical_topk, slash, last_q=64, heads=None,
+                                    scale=None):
+    """[MInf-API] vertical_slash_sparse_attention on q [B,Hq,N,d], k/v [B,Hkv,N,d].
+
+    Returns out [B, len(heads), N, d] float64 and the per-(b, h) index records.
+    """
+    q, k, v = as_f64(q), as_f64(k), as_f64(v)
+    B, Hq, N, d = q.shape
+    heads = list(range(Hq)) if heads is None else list(heads)
+    out = np.zeros((B, len(heads), N, d))
+    recs = {}
+    for b in range(B):
+        for t, h in enumerate(heads):
+            g = _kv_head(h, Hq, k.shape[1])
+            out[b, t], recs[(b, h)] = vertical_slash_head(q[b, h], k[b, g], v[b, g],
+                                                          vertical_topk, slash, last_q, scale)
+    return out, recs
+
+
+def block_sparse_attention(q, k, v, topk, heads=None, scale=None):
+    """[MInf-API] block_sparse_attention on q [B,Hq,N,d], k/v [B,Hkv,N,d]."""
+    q, k, v = as_f64(q), as_f64(k), as_f64(v)
+    B, Hq, N, d = q.shape
+    heads = list(range(Hq)) if heads is None else list(heads)
+    out = np.zeros((B, len(heads), N, d))
+    recs = {}
+    for b in range(B):
+        for t, h in enumerate(heads):
+            g = _kv_head(h, Hq, k.shape[1])
+            out[b, t], recs[(b, h)] = block_sparse_head(q[b, h], k[b, g], v[b, g], topk, scale)
+    return out, recs
+
+
+def streaming_forward(q, k, v, init_num, local_window_num, heads=None, scale=None):
+    """[MInf-API] streaming_forward on q [B,Hq,N,d], k/v [B,Hkv,N,d]."""
+    q, k, v = as_f64(q), as_f64(k), as_f64(v)
+    B, Hq, N, d = q.shape
+    heads = list(range(Hq)) if heads is None else list(heads)
+    out = np.zeros((B, len(heads), N, d))
+    recs = {}
+    for b in range(B):
+        for t, h in enumerate(heads):
+            g = _kv_head(h, Hq, k.shape[1])
+            out[b, t], recs[(b, h)] = streaming_head(q[b, h], k[b, g], v[b, g], init_num,
+                                                     local_window_num, scale)
+    return out, recs
+
+
+# ----------------------------------------------------------------------------- counting
+def nnz_from_blocks(sel, N: int) -> int:
+    """Number of (i, j) pairs, j <= i, admitted by whole 64-key blocks per row block."""
+    total = 0
+    for m, blocks in enumerate(sel):
+        r0, r1 = m * BLOCK, min(N, (m + 1) * BLOCK)
+        for n in blocks:
+            k0, k1 = n * BLOCK, min(N, (n + 1) * BLOCK)
+            for i in range(r0, r1):
+                total += max(0, min(k1, i + 1) - k0)
+    return total
