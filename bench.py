@@ -1,0 +1,475 @@
+"""Benchmark: one step = the whole sparse-prefill hot path over one attention layer.
+
+Default workload ``mixed_128k``: batch 1, 32 query heads / 8 KV heads, d = 128,
+N = 131072 tokens, bf16, causal; a seeded split of the heads into 20
+vertical-slash heads (vertical_topk 1000, slash 6096, last_q 64), 8
+block-sparse heads (top-100 blocks) and 4 streaming heads (1 sink block, 64
+local blocks).  One step calls msa_vertical_slash, msa_block_sparse and
+msa_streaming on their head subsets of the same q/k/v/out tensors.
+
+Metric: effective TFLOP/s = 4 * d * (admitted causal (query, key) pairs of the
+method's own mask, counted exactly from the index sets) / step time, inputs
+resident in HBM; `e2e` repeats it with the inputs in pinned host memory and
+the host<->device copies inside the timed region.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 launch under torchrun: every rank runs its own copy of the workload
+(weak scaling, no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from dynamic_sparse_attention_slash_gb300 import inputs  # noqa: E402
+
+D = 128
+METRIC = "sparse prefill attention effective TFLOP/s at 128K tokens"
+UNIT = "TFLOP/s"
+
+
+# ----------------------------------------------------------------------------- exact pair counts
+def vs_pairs(tile_dist_words, vertical, N: int) -> int:
+    """Admitted (i, j) pairs, j <= i, of one vertical-slash head: active 64x64
+    tiles (the diagonal one triangular) plus the uncovered vertical columns."""
+    NB = N // 64
+    words = np.asarray(tile_dist_words, dtype=np.int64) & 0xFFFFFFFF
+    t = np.arange(NB)
+    bits = ((words[t >> 5] >> (t & 31)) & 1).astype(np.int64)
+    cum = np.cumsum(bits)  # cum[m] = #{t in D, t <= m}
+    diag = int(bits[0])
+    total = int(((cum - diag) * 4096).sum()) + diag * 2080 * NB
+    V = np.asarray(vertical, dtype=np.int64)
+    mj = V // 64
+    # row blocks m > mj whose distance m - mj is not in D contribute 64 rows
+    upto = NB - 1 - mj
+    in_d = np.where(upto >= 1, cum[np.maximum(upto, 0)] - diag, 0)
+    total += int((64 * (upto - in_d)).sum())
+    if not diag:  # the key's own row block: rows j..64*mj+63
+        total += int((64 * (mj + 1) - V).sum())
+    return total
+
+
+def bs_pairs(block_count) -> int:
+    c = np.asarray(block_count, dtype=np.int64)
+    return int(((c - 1) * 4096 + 2080).sum())
+
+
+def st_pairs(N: int, init_num: int, local: int) -> int:
+    total = 0
+    for m in range(N // 64):
+        blocks = set(range(min(init_num, m + 1))) | set(range(max(0, m - local + 1), m + 1))
+        total += 2080 + 4096 * (len(blocks) - 1)
+    return total
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, val in zip(names, r[4:8]) if val == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, local, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value of x over the ranks (timing: the slowest rank sets the time)."""
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- CPU oracle leg
+def oracle_sample(w, q, k, v, heads, rows_per_head: int, seed: int = 0):
+    """Times the oracle on a bounded sample of the workload: for one head of each
+    type, the full index construction plus attention for `rows_per_head` seeded
+    query rows.  Returns (effective FLOPs of the sampled rows, seconds, label)."""
+    from oracle import msa_oracle as O
+    N = w.seq_len
+    G = w.n_q_heads // w.n_kv_heads
+    rng = np.random.default_rng(seed)
+    scale = 1 / np.sqrt(D)
+    flops = 0
+    t0 = time.perf_counter()
+    for kind in ("vs", "bs", "st"):
+        if not heads[kind]:
+            continue
+        h = heads[kind][0]
+        qn = q[0, h].to(torch.float64).numpy()
+        kn = k[0, h // G].to(torch.float64).numpy()
+        vn = v[0, h // G].to(torch.float64).numpy()
+        rows = np.sort(rng.choice(N, size=rows_per_head, replace=False))
+        if kind == "vs":
+            idx = O.vertical_slash_indices(qn, kn, w.vertical_topk, w.slash, w.last_q, scale)
+            mask = O.vs_block_mask(idx["active"], idx["columns"], N)
+        elif kind == "bs":
+            sel, _ = O.block_sparse_blocks(qn, kn, w.block_topk, scale)
+            mask = O.block_mask_from_blocks(sel, N)
+        else:
+            sel = [O.streaming_blocks(m, w.init_num, w.local_window_num) for m in range(N // 64)]
+            mask = O.block_mask_from_blocks(sel, N)
+        _, counts = O.attend_rows(qn, kn, vn, rows, lambda i: mask(i // 64), scale)
+        flops += 4 * D * int(counts.sum())
+    secs = time.perf_counter() - t0
+    label = (f"one head of each type of {w.name}: full index construction + attention for "
+             f"{rows_per_head} seeded query rows per head")
+    return flops, secs, label
+
+
+def cpu_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the CPU oracle as it stands, timed on the host cores."""
+    if rank != 0:
+        return
+    w = inputs.WORKLOADS[args.workload]
+    q, k, v = inputs.make_qkv(w.batch, w.n_q_heads, w.n_kv_heads, w.seq_len, w.seed,
+                              vs_planting=w.vs_planting, bs_planting=w.bs_planting, device="cpu")
+    heads = inputs.head_assignment(w)
+    for _ in range(args.warmup and 1):
+        oracle_sample(w, q, k, v, heads, 8, seed=99)
+    tot_f, tot_s = 0, 0.0
+    label = ""
+    for s in range(args.steps):
+        f, secs, label = oracle_sample(w, q, k, v, heads, args.ref_rows, seed=s)
+        tot_f += f
+        tot_s += secs
+    value = tot_f / tot_s / 1e12
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "seq_len": w.seq_len, "batch": w.batch,
+                       "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(),
+                             "kind": "oracle", "sample": label},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mixed_128k", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-rows", type=int, default=48, help="oracle rows per head (cpu_baseline)")
+    ap.add_argument("--ref-rows", type=int, default=24, help="oracle rows per head (reference arm)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-dense", action="store_true")
+    args = ap.parse_args()
+    rank, local, world = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    from dynamic_sparse_attention_slash_gb300 import msa
+    import json as _json
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = inputs.WORKLOADS[args.workload]
+    q, k, v = inputs.make_qkv(w.batch, w.n_q_heads, w.n_kv_heads, w.seq_len, w.seed,
+                              vs_planting=w.vs_planting, bs_planting=w.bs_planting, device=dev)
+    heads = inputs.head_assignment(w)
+    N, B = w.seq_len, w.batch
+    out = torch.zeros_like(q)
+    stream = torch.cuda.current_stream(dev)
+
+    ws = {}
+    if heads["vs"]:
+        ws["vs"] = torch.empty(msa.workspace_bytes(msa.MSA_KIND_VERTICAL_SLASH, q, k,
+                                                   w.vertical_topk, w.slash, len(heads["vs"])),
+                               dtype=torch.uint8, device=dev)
+    if heads["bs"]:
+        ws["bs"] = torch.empty(msa.workspace_bytes(msa.MSA_KIND_BLOCK_SPARSE, q, k, w.block_topk,
+                                                   0, len(heads["bs"])), dtype=torch.uint8, device=dev)
+    if heads["st"]:
+        ws["st"] = torch.empty(256, dtype=torch.uint8, device=dev)
+
+    def new_events():
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * msa.MSA_STAGE_COUNT)]
+        for e in evs:
+            e.record(stream)
+        return evs
+
+    def step(events=None, export=None, qq=q, kk=k, vv=v, oo=out):
+        ev = events or {}
+        if heads["vs"]:
+            msa.msa_vertical_slash(qq, kk, vv, w.vertical_topk, w.slash, oo, last_q=w.last_q,
+                                   heads=heads["vs"], workspace=ws["vs"], stage_events=ev.get("vs"),
+                                   export=(export or {}).get("vs"))
+        if heads["bs"]:
+            msa.msa_block_sparse(qq, kk, vv, w.block_topk, oo, heads=heads["bs"], workspace=ws["bs"],
+                                 stage_events=ev.get("bs"), export=(export or {}).get("bs"))
+        if heads["st"]:
+            msa.msa_streaming(qq, kk, vv, w.init_num, w.local_window_num, oo, heads=heads["st"],
+                              workspace=ws["st"], stage_events=ev.get("st"))
+
+    # exact work of one step, from the GPU's own index sets
+    U_vs, U_bs = B * len(heads["vs"]), B * len(heads["bs"])
+    export = {}
+    if U_vs:
+        export["vs"] = {"vertical": torch.empty(U_vs, min(w.vertical_topk, N), dtype=torch.int32, device=dev),
+                        "tile_dist": torch.empty(U_vs, (N // 64 + 32) // 32, dtype=torch.int32, device=dev)}
+    if U_bs:
+        export["bs"] = {"block_count": torch.empty(U_bs, N // 64, dtype=torch.int32, device=dev)}
+    step(export=export)
+    torch.cuda.synchronize()
+    pairs = {"vs": 0, "bs": 0, "st": 0}
+    if U_vs:
+        td, vt = export["vs"]["tile_dist"].cpu().numpy(), export["vs"]["vertical"].cpu().numpy()
+        pairs["vs"] = sum(vs_pairs(td[u], vt[u], N) for u in range(U_vs))
+    if U_bs:
+        pairs["bs"] = bs_pairs(export["bs"]["block_count"].cpu().numpy())
+    if heads["st"]:
+        pairs["st"] = B * len(heads["st"]) * st_pairs(N, w.init_num, w.local_window_num)
+    flops = {kk_: 4 * D * vv_ for kk_, vv_ in pairs.items()}
+    step_flops = sum(flops.values())
+    dense_pairs = B * w.n_q_heads * N * (N + 1) // 2
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = {kind: msa.device_status(buf) for kind, buf in ws.items()}
+
+    # ---- timed region (device-resident inputs)
+    ev_sets = [{kind: new_events() for kind in ("vs", "bs", "st") if heads[kind]} for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    l0 = msa.kernel_launches()
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    t_start.record(stream)
+    for s in range(args.steps):
+        step(events=ev_sets[s])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clock_info = clocks.stop()
+    launches = msa.kernel_launches() - l0
+    ms_total = t_start.elapsed_time(t_end)
+    ms_total = max_over_ranks(ms_total, world)
+    ms_step = ms_total / args.steps
+    total_flops = sum_over_ranks(step_flops * args.steps, world)
+    value = total_flops / (ms_total * 1e-3) / 1e12
+
+    stage_ms = {}
+    names = ["estimate", "topk", "index", "prefill"]
+    for kind in ("vs", "bs", "st"):
+        if not heads[kind]:
+            continue
+        for si, nm in enumerate(names):
+            if kind != "vs" and nm in ("estimate", "topk"):
+                continue
+            if kind == "st" and nm == "index":
+                continue
+            vals = [ev[kind][2 * si].elapsed_time(ev[kind][2 * si + 1]) for ev in ev_sets]
+            stage_ms[f"{kind}_{nm}"] = sum(vals) / len(vals)
+
+    # ---- roofline of the dominant kernel (vertical-slash sparse prefill)
+    peaks = {}
+    try:
+        peaks = _json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        peak, peak_src = float(peaks["bf16_tflops_sustained"]), "measured (sustained)"
+    except (OSError, KeyError, ValueError):
+        peak, peak_src = 1700.0, "fallback (sustained)"
+    dom = "vs" if heads["vs"] else ("bs" if heads["bs"] else "st")
+    dom_ms = stage_ms[f"{dom}_prefill"]
+    achieved = flops[dom] / (dom_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None, "kernel": "sparse_prefill_kernel",
+                "peak_source": peak_src,
+                "frac_of_burst": achieved / float(peaks.get("bf16_tflops", 1900.0))}
+
+    # ---- end to end: pinned host inputs, copies inside the timed region
+    e2e = None
+    if args.e2e_steps > 0:
+        qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+        oh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        qd, kd, vd, od = (torch.empty_like(t) for t in (q, k, v, out))
+        od.zero_()
+        barrier(world)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            step(qq=qd, kk=kd, vv=vd, oo=od)
+            oh.copy_(od, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+        e_val = sum_over_ranks(step_flops * args.e2e_steps, world) / (e_ms * 1e-3) / 1e12
+        h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+        e2e = {"value": e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": oh.numel() * oh.element_size(),
+               "ms_per_step": e_ms / args.e2e_steps}
+        del qh, kh, vh, oh, qd, kd, vd, od
+
+    # ---- dense causal attention on the same GPU (context)
+    dense = None
+    if not args.no_dense and rank == 0:
+        dout = torch.empty_like(q)
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        msa.msa_streaming(q, k, v, 0, N // 64, dout)
+        d0.record(stream)
+        msa.msa_streaming(q, k, v, 0, N // 64, dout)
+        d1.record(stream)
+        torch.cuda.synchronize()
+        ours_ms = d0.elapsed_time(d1)
+        sdpa_ms, backend = None, None
+        try:
+            G = w.n_q_heads // w.n_kv_heads
+            kr, vr = k.repeat_interleave(G, dim=1), v.repeat_interleave(G, dim=1)
+            torch.nn.functional.scaled_dot_product_attention(q, kr, vr, is_causal=True)
+            d0.record(stream)
+            torch.nn.functional.scaled_dot_product_attention(q, kr, vr, is_causal=True)
+            d1.record(stream)
+            torch.cuda.synchronize()
+            sdpa_ms = d0.elapsed_time(d1)
+            backend = "torch SDPA (default backend selection)"
+            del kr, vr
+        except RuntimeError as exc:  # pragma: no cover
+            backend = f"unavailable: {exc}"[:120]
+        dense = {"flops": 4 * D * dense_pairs, "ours_ms": ours_ms,
+                 "ours_tflops": 4 * D * dense_pairs / (ours_ms * 1e-3) / 1e12,
+                 "sdpa_ms": sdpa_ms, "sdpa_backend": backend,
+                 "sdpa_tflops": (4 * D * dense_pairs / (sdpa_ms * 1e-3) / 1e12) if sdpa_ms else None}
+        del dout
+
+    # ---- CPU oracle on the host cores (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        qc, kc, vc = q.cpu(), k.cpu(), v.cpu()
+        f, secs, label = oracle_sample(w, qc, kc, vc, heads, args.cpu_rows)
+        cpu = {"value": f / secs / 1e12, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+               "sample": label, "seconds": secs}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "seq_len": N, "batch": B, "q_heads": w.n_q_heads,
+                       "kv_heads": w.n_kv_heads, "head_dim": D,
+                       "heads": {kk_: len(vv_) for kk_, vv_ in heads.items()},
+                       "vertical_topk": w.vertical_topk, "slash": w.slash, "last_q": w.last_q,
+                       "block_topk": w.block_topk, "init_num": w.init_num,
+                       "local_window_num": w.local_window_num,
+                       "l2": "inputs larger than L2 (q 1 GiB, k and v 256 MiB each)"},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clock_info,
+            "stage_ms": stage_ms,
+            "effective_tflop": {kk_: vv_ / 1e12 for kk_, vv_ in flops.items()},
+            "density_vs_dense_causal": sum(pairs.values()) / dense_pairs,
+            "dense_causal": dense,
+            "device_status": status,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

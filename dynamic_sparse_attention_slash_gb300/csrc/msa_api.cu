@@ -1,0 +1,466 @@
+// Host side of the C ABI declared in include/msa.h: argument validation,
+// workspace layout, TMA descriptor construction and kernel launches.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/msa.h"
+#include "msa_internal.h"
+
+namespace msa {
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// ------------------------------------------------------------------ validation
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int check_tensor(const msa_tensor* t) {
+  if (!t || !t->data) return MSA_ERR_INVALID;
+  if (t->B <= 0 || t->H <= 0 || t->N <= 0 || t->D <= 0) return MSA_ERR_INVALID;
+  if (t->D != kHeadDim) return MSA_ERR_UNSUPPORTED;
+  if (t->N % kBlock != 0) return MSA_ERR_UNSUPPORTED;
+  if (t->N > (int64_t{1} << 21)) return MSA_ERR_UNSUPPORTED;
+  if (!aligned(t->data, 16)) return MSA_ERR_INVALID;
+  if (t->sn < t->D || t->sn % 8 || t->sh % 8 || t->sb % 8 || t->sh < 0 || t->sb < 0)
+    return MSA_ERR_INVALID;
+  if (t->H > 1 && t->sh < t->sn) return MSA_ERR_INVALID;
+  return MSA_OK;
+}
+
+struct Call {
+  Geometry g;
+  UnitMap u;
+  cudaStream_t st;
+  int last_q;
+  float scale;
+  const msa_opts* opts;
+};
+
+int prepare(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v, const msa_tensor* out,
+            const msa_opts* opts, Call& c) {
+  int s;
+  if ((s = check_tensor(q)) || (s = check_tensor(k)) || (s = check_tensor(v)) ||
+      (s = check_tensor(out)))
+    return s;
+  if (k->B != q->B || v->B != q->B || out->B != q->B) return MSA_ERR_INVALID;
+  if (k->N != q->N || v->N != q->N || out->N != q->N) return MSA_ERR_INVALID;
+  if (v->H != k->H || out->H != q->H) return MSA_ERR_INVALID;
+  if (q->H % k->H != 0) return MSA_ERR_INVALID;
+  if (opts && opts->flags != 0) return MSA_ERR_INVALID;
+  c.opts = opts;
+  c.st = opts ? static_cast<cudaStream_t>(opts->stream) : nullptr;
+  c.last_q = (opts && opts->last_q) ? static_cast<int>(opts->last_q) : kLastQMax;
+  if (opts && (opts->last_q < 0 || opts->last_q > kLastQMax)) return MSA_ERR_INVALID;
+  c.scale = (opts && opts->scale != 0.f) ? opts->scale : 1.0f / std::sqrt(static_cast<float>(q->D));
+  if (!std::isfinite(c.scale)) return MSA_ERR_INVALID;
+  // head selection
+  std::memset(&c.u, 0, sizeof(c.u));
+  if (opts && opts->heads) {
+    if (opts->n_heads <= 0 || opts->n_heads > MSA_MAX_HEADS) return MSA_ERR_INVALID;
+    static_assert(MSA_MAX_HEADS <= static_cast<int>(sizeof(c.u.heads) / sizeof(c.u.heads[0])),
+                  "head list capacity");
+    bool seen[MSA_MAX_HEADS] = {};
+    for (int i = 0; i < opts->n_heads; ++i) {
+      const int32_t h = opts->heads[i];
+      if (h < 0 || h >= q->H || h >= MSA_MAX_HEADS || seen[h]) return MSA_ERR_INVALID;
+      seen[h] = true;
+      c.u.heads[i] = h;
+    }
+    c.u.n_heads = opts->n_heads;
+  } else {
+    if (q->H > MSA_MAX_HEADS) return MSA_ERR_UNSUPPORTED;
+    for (int i = 0; i < q->H; ++i) c.u.heads[i] = i;
+    c.u.n_heads = static_cast<int>(q->H);
+  }
+  const int64_t units = q->B * c.u.n_heads;
+  if (units > kMaxUnits) return MSA_ERR_UNSUPPORTED;
+  Geometry& g = c.g;
+  g.B = static_cast<int>(q->B);
+  g.Hq = static_cast<int>(q->H);
+  g.Hkv = static_cast<int>(k->H);
+  g.G = g.Hq / g.Hkv;
+  g.N = static_cast<int>(q->N);
+  g.NB = g.N / kBlock;
+  g.NQ = (g.N + kTileM - 1) / kTileM;
+  g.n_units = static_cast<int>(units);
+  g.scale = c.scale;
+  return MSA_OK;
+}
+
+// ------------------------------------------------------------------ workspace
+struct Carver {
+  size_t off = 0;
+  template <typename T>
+  size_t take(size_t count) {
+    off = (off + 255) & ~size_t{255};
+    const size_t at = off;
+    off += count * sizeof(T);
+    return at;
+  }
+};
+
+constexpr size_t kStatusBytes = 256;
+
+struct VSLayout {
+  int kv, ks, kv_pad, n_split, dist_words, chunk_words;
+  size_t partial, v_score, s_score, vertical, slash, tile_dist, qdelta, qdelta_count, col_chunks,
+      kc, vc, total;
+};
+
+int vs_split(int units, int NB) {
+  int s = (608 + units - 1) / units;
+  if (s > 64) s = 64;
+  if (s > NB) s = NB;
+  return s < 1 ? 1 : s;
+}
+
+VSLayout vs_layout(const Geometry& g, int64_t vertical_topk, int64_t slash) {
+  VSLayout L;
+  L.kv = static_cast<int>(vertical_topk < g.N ? vertical_topk : g.N);
+  L.ks = static_cast<int>(slash < g.N ? slash : g.N);
+  L.kv_pad = (L.kv + 127) / 128 * 128;
+  L.n_split = vs_split(g.n_units, g.NB);
+  L.dist_words = (g.NB + 32) / 32;
+  L.chunk_words = ((L.kv + 127) / 128 + 31) / 32;
+  const size_t U = static_cast<size_t>(g.n_units);
+  Carver c;
+  c.off = kStatusBytes;
+  L.partial = c.take<float>(U * L.n_split * 128);
+  L.v_score = c.take<float>(U * g.N);
+  L.s_score = c.take<float>(U * g.N);
+  L.vertical = c.take<int32_t>(U * L.kv);
+  L.slash = c.take<int32_t>(U * L.ks);
+  L.tile_dist = c.take<uint32_t>(U * L.dist_words);
+  L.qdelta = c.take<int32_t>(U * g.NQ);
+  L.qdelta_count = c.take<int32_t>(U);
+  L.col_chunks = c.take<uint32_t>(U * g.NQ * L.chunk_words);
+  L.kc = c.take<__nv_bfloat16>(U * L.kv_pad * kHeadDim);
+  L.vc = c.take<__nv_bfloat16>(U * L.kv_pad * kHeadDim);
+  L.total = (c.off + 255) & ~size_t{255};
+  return L;
+}
+
+struct BSLayout {
+  int kb, tile_cap;
+  size_t qpool, kpool, block_count, block_ids, tiles, tile_count, total;
+};
+
+BSLayout bs_layout(const Geometry& g, int64_t topk) {
+  BSLayout L;
+  L.kb = static_cast<int>(topk < g.NB ? topk : g.NB);
+  L.tile_cap = 2 * L.kb;
+  const size_t U = static_cast<size_t>(g.n_units);
+  Carver c;
+  c.off = kStatusBytes;
+  L.qpool = c.take<float>(U * g.NB * kHeadDim);
+  L.kpool = c.take<float>(static_cast<size_t>(g.B) * g.Hkv * g.NB * kHeadDim);
+  L.block_count = c.take<int32_t>(U * g.NB);
+  L.block_ids = c.take<int32_t>(U * g.NB * L.kb);
+  L.tiles = c.take<int32_t>(U * g.NQ * L.tile_cap);
+  L.tile_count = c.take<int32_t>(U * g.NQ);
+  L.total = (c.off + 255) & ~size_t{255};
+  return L;
+}
+
+int check_workspace(const msa_opts* opts, size_t need) {
+  if (!opts || !opts->workspace) return MSA_ERR_WORKSPACE;
+  if (!aligned(opts->workspace, 256)) return MSA_ERR_WORKSPACE;
+  if (opts->workspace_bytes < need) return MSA_ERR_WORKSPACE;
+  return MSA_OK;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+// ------------------------------------------------------------------ TMA maps
+int make_map_4d(CUtensorMap* m, const msa_tensor* t) {
+  auto fn = encode_fn();
+  if (!fn) return MSA_ERR_CUDA;
+  const int64_t sh = t->H > 1 ? t->sh : t->N * t->sn;
+  const int64_t sb = t->B > 1 ? t->sb : t->H * sh;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(t->D), static_cast<cuuint64_t>(t->N),
+                        static_cast<cuuint64_t>(t->H), static_cast<cuuint64_t>(t->B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(t->sn * 2), static_cast<cuuint64_t>(sh * 2),
+                           static_cast<cuuint64_t>(sb * 2)};
+  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t->data, dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MSA_OK : MSA_ERR_INVALID;
+}
+
+int make_map_rows(CUtensorMap* m, void* base, int64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return MSA_ERR_CUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim * 2)};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t es[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MSA_OK : MSA_ERR_INVALID;
+}
+
+TensorView view(const msa_tensor* t) {
+  return TensorView{static_cast<const __nv_bfloat16*>(t->data), t->sb, t->sh, t->sn};
+}
+
+// ------------------------------------------------------------------ stage events
+struct StageTimer {
+  void* const* ev;
+  cudaStream_t st;
+  void begin(int s) const {
+    if (ev) cudaEventRecord(static_cast<cudaEvent_t>(ev[2 * s]), st);
+  }
+  void end(int s) const {
+    if (ev) cudaEventRecord(static_cast<cudaEvent_t>(ev[2 * s + 1]), st);
+  }
+};
+
+int finish(cudaError_t e, int launches) {
+  g_launches.fetch_add(static_cast<uint64_t>(launches));
+  return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+PrefillParams base_prefill(const Call& c, msa_tensor* out, uint32_t* status) {
+  PrefillParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.g = c.g;
+  p.scale_log2 = c.scale * 1.4426950408889634f;
+  p.out = static_cast<__nv_bfloat16*>(out->data);
+  p.out_sb = out->sb;
+  p.out_sh = out->sh;
+  p.out_sn = out->sn;
+  p.status = status;
+  p.units = c.u;
+  return p;
+}
+
+}  // namespace
+}  // namespace msa
+
+using namespace msa;
+
+extern "C" {
+
+size_t msa_workspace_bytes(int kind, const msa_tensor* q, const msa_tensor* k, int64_t p0,
+                           int64_t p1, int32_t n_heads) {
+  if (check_tensor(q) != MSA_OK || check_tensor(k) != MSA_OK) return 0;
+  Geometry g;
+  g.B = static_cast<int>(q->B);
+  g.Hq = static_cast<int>(q->H);
+  g.Hkv = static_cast<int>(k->H);
+  g.G = g.Hkv > 0 ? g.Hq / g.Hkv : 1;
+  g.N = static_cast<int>(q->N);
+  g.NB = g.N / kBlock;
+  g.NQ = (g.N + kTileM - 1) / kTileM;
+  g.n_units = static_cast<int>(q->B * (n_heads > 0 ? n_heads : q->H));
+  if (kind == MSA_KIND_VERTICAL_SLASH) {
+    if (p0 <= 0 || p1 <= 0) return 0;
+    return vs_layout(g, p0, p1).total;
+  }
+  if (kind == MSA_KIND_BLOCK_SPARSE) {
+    if (p0 <= 0) return 0;
+    return bs_layout(g, p0).total;
+  }
+  if (kind == MSA_KIND_STREAMING) return kStatusBytes;
+  return 0;
+}
+
+int msa_vertical_slash(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v,
+                       int64_t vertical_topk, int64_t slash, msa_tensor* out,
+                       const msa_opts* opts) {
+  Call c;
+  int s = prepare(q, k, v, out, opts, c);
+  if (s) return s;
+  if (vertical_topk <= 0 || slash <= 0) return MSA_ERR_INVALID;
+  const VSLayout L = vs_layout(c.g, vertical_topk, slash);
+  if ((s = check_workspace(opts, L.total))) return s;
+  void* ws = opts->workspace;
+  CUtensorMap mq, mk, mv, mkc, mvc;
+  if ((s = make_map_4d(&mq, q)) || (s = make_map_4d(&mk, k)) || (s = make_map_4d(&mv, v)) ||
+      (s = make_map_rows(&mkc, at<void>(ws, L.kc), static_cast<int64_t>(c.g.n_units) * L.kv_pad)) ||
+      (s = make_map_rows(&mvc, at<void>(ws, L.vc), static_cast<int64_t>(c.g.n_units) * L.kv_pad)))
+    return s;
+  const StageTimer tm{opts->stage_events, c.st};
+  int launches = 0;
+  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), c.st);
+  if (e != cudaSuccess) return finish(e, launches);
+  tm.begin(MSA_STAGE_ESTIMATE);
+  e = launch_vs_estimate(c.g, c.u, view(q), view(k), c.last_q, at<float>(ws, L.partial), L.n_split,
+                         nullptr, at<float>(ws, L.v_score), at<float>(ws, L.s_score), c.st,
+                         &launches);
+  tm.end(MSA_STAGE_ESTIMATE);
+  if (e != cudaSuccess) return finish(e, launches);
+  tm.begin(MSA_STAGE_TOPK);
+  e = launch_topk(at<float>(ws, L.v_score), c.g.N, c.g.N, c.g.n_units, L.kv,
+                  at<int32_t>(ws, L.vertical), L.kv, c.st, &launches);
+  if (e == cudaSuccess)
+    e = launch_topk(at<float>(ws, L.s_score), c.g.N, c.g.N, c.g.n_units, L.ks,
+                    at<int32_t>(ws, L.slash), L.ks, c.st, &launches);
+  tm.end(MSA_STAGE_TOPK);
+  if (e != cudaSuccess) return finish(e, launches);
+  tm.begin(MSA_STAGE_INDEX);
+  e = launch_vs_index(c.g, c.u, view(k), view(v), at<int32_t>(ws, L.slash), L.ks,
+                      at<int32_t>(ws, L.vertical), L.kv, at<uint32_t>(ws, L.tile_dist),
+                      L.dist_words, at<int32_t>(ws, L.qdelta), at<int32_t>(ws, L.qdelta_count),
+                      at<uint32_t>(ws, L.col_chunks), L.chunk_words, at<__nv_bfloat16>(ws, L.kc),
+                      at<__nv_bfloat16>(ws, L.vc), L.kv_pad, c.st, &launches);
+  tm.end(MSA_STAGE_INDEX);
+  if (e != cudaSuccess) return finish(e, launches);
+  PrefillParams p = base_prefill(c, out, at<uint32_t>(ws, 0));
+  p.kind = kPrefillVS;
+  p.tile_dist = at<uint32_t>(ws, L.tile_dist);
+  p.dist_words = L.dist_words;
+  p.qdelta = at<int32_t>(ws, L.qdelta);
+  p.qdelta_count = at<int32_t>(ws, L.qdelta_count);
+  p.col_chunks = at<uint32_t>(ws, L.col_chunks);
+  p.chunk_words = L.chunk_words;
+  p.vertical = at<int32_t>(ws, L.vertical);
+  p.kv = L.kv;
+  p.kv_pad = L.kv_pad;
+  tm.begin(MSA_STAGE_PREFILL);
+  e = launch_prefill(p, mq, mk, mv, mkc, mvc, c.st, &launches);
+  tm.end(MSA_STAGE_PREFILL);
+  if (e != cudaSuccess) return finish(e, launches);
+  if (const msa_index_export* x = opts->export_idx) {
+    const size_t U = static_cast<size_t>(c.g.n_units);
+    auto cp = [&](void* dst, size_t off, size_t bytes) {
+      if (dst && e == cudaSuccess)
+        e = cudaMemcpyAsync(dst, at<void>(ws, off), bytes, cudaMemcpyDeviceToDevice, c.st);
+    };
+    cp(x->v_score, L.v_score, U * c.g.N * sizeof(float));
+    cp(x->s_score, L.s_score, U * c.g.N * sizeof(float));
+    cp(x->vertical, L.vertical, U * L.kv * sizeof(int32_t));
+    cp(x->slash, L.slash, U * L.ks * sizeof(int32_t));
+    cp(x->tile_dist, L.tile_dist, U * L.dist_words * sizeof(uint32_t));
+  }
+  return finish(e, launches);
+}
+
+int msa_block_sparse(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v, int64_t topk,
+                     msa_tensor* out, const msa_opts* opts) {
+  Call c;
+  int s = prepare(q, k, v, out, opts, c);
+  if (s) return s;
+  if (topk <= 0) return MSA_ERR_INVALID;
+  const BSLayout L = bs_layout(c.g, topk);
+  if ((s = check_workspace(opts, L.total))) return s;
+  void* ws = opts->workspace;
+  CUtensorMap mq, mk, mv, mdummy;
+  std::memset(&mdummy, 0, sizeof(mdummy));
+  if ((s = make_map_4d(&mq, q)) || (s = make_map_4d(&mk, k)) || (s = make_map_4d(&mv, v)))
+    return s;
+  const StageTimer tm{opts->stage_events, c.st};
+  int launches = 0;
+  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), c.st);
+  if (e != cudaSuccess) return finish(e, launches);
+  tm.begin(MSA_STAGE_INDEX);
+  e = launch_bs_index(c.g, c.u, view(q), view(k), static_cast<int>(L.kb < topk ? L.kb : topk),
+                      at<float>(ws, L.qpool), at<float>(ws, L.kpool), at<int32_t>(ws, L.block_count),
+                      at<int32_t>(ws, L.block_ids), at<int32_t>(ws, L.tiles),
+                      at<int32_t>(ws, L.tile_count), L.tile_cap, c.st, &launches);
+  tm.end(MSA_STAGE_INDEX);
+  if (e != cudaSuccess) return finish(e, launches);
+  PrefillParams p = base_prefill(c, out, at<uint32_t>(ws, 0));
+  p.kind = kPrefillBS;
+  p.bs_tiles = at<int32_t>(ws, L.tiles);
+  p.bs_tile_count = at<int32_t>(ws, L.tile_count);
+  p.bs_tile_cap = L.tile_cap;
+  tm.begin(MSA_STAGE_PREFILL);
+  e = launch_prefill(p, mq, mk, mv, mdummy, mdummy, c.st, &launches);
+  tm.end(MSA_STAGE_PREFILL);
+  if (e != cudaSuccess) return finish(e, launches);
+  if (const msa_index_export* x = opts->export_idx) {
+    const size_t U = static_cast<size_t>(c.g.n_units);
+    if (x->block_count)
+      e = cudaMemcpyAsync(x->block_count, at<void>(ws, L.block_count), U * c.g.NB * sizeof(int32_t),
+                          cudaMemcpyDeviceToDevice, c.st);
+    if (x->block_ids && e == cudaSuccess)
+      e = cudaMemcpyAsync(x->block_ids, at<void>(ws, L.block_ids),
+                          U * c.g.NB * L.kb * sizeof(int32_t), cudaMemcpyDeviceToDevice, c.st);
+  }
+  return finish(e, launches);
+}
+
+int msa_streaming(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v, int64_t init_num,
+                  int64_t local_window_num, msa_tensor* out, const msa_opts* opts) {
+  Call c;
+  int s = prepare(q, k, v, out, opts, c);
+  if (s) return s;
+  if (init_num < 0 || local_window_num < 1) return MSA_ERR_INVALID;
+  uint32_t* status = nullptr;
+  if (opts && opts->workspace) {
+    if ((s = check_workspace(opts, kStatusBytes))) return s;
+    status = static_cast<uint32_t*>(opts->workspace);
+  }
+  CUtensorMap mq, mk, mv, mdummy;
+  std::memset(&mdummy, 0, sizeof(mdummy));
+  if ((s = make_map_4d(&mq, q)) || (s = make_map_4d(&mk, k)) || (s = make_map_4d(&mv, v)))
+    return s;
+  const StageTimer tm{opts ? opts->stage_events : nullptr, c.st};
+  int launches = 0;
+  cudaError_t e = cudaSuccess;
+  if (status) {  // without a workspace the kernel has nowhere to report a timeout
+    e = cudaMemsetAsync(status, 0, sizeof(uint32_t), c.st);
+    if (e != cudaSuccess) return finish(e, launches);
+  }
+  PrefillParams p = base_prefill(c, out, status);
+  p.kind = kPrefillST;
+  const int64_t nb = c.g.NB;
+  p.init_num = static_cast<int>(init_num < nb ? init_num : nb);
+  p.local_num = static_cast<int>(local_window_num < nb ? local_window_num : nb);
+  tm.begin(MSA_STAGE_PREFILL);
+  e = launch_prefill(p, mq, mk, mv, mdummy, mdummy, c.st, &launches);
+  tm.end(MSA_STAGE_PREFILL);
+  return finish(e, launches);
+}
+
+int msa_device_status(void* workspace, void* stream) {
+  if (!workspace) return MSA_ERR_INVALID;
+  uint32_t h = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MSA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MSA_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), st) != cudaSuccess) return MSA_ERR_CUDA;
+  return (h & kStatusTimeout) ? MSA_ERR_TIMEOUT : MSA_OK;
+}
+
+const char* msa_status_string(int status) {
+  switch (status) {
+    case MSA_OK: return "ok";
+    case MSA_ERR_INVALID: return "invalid argument";
+    case MSA_ERR_UNSUPPORTED: return "unsupported shape or parameter";
+    case MSA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MSA_ERR_CUDA: return "CUDA error";
+    case MSA_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+uint64_t msa_kernel_launches(void) { return g_launches.load(); }
+
+}  // extern "C"

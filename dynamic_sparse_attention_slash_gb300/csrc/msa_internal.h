@@ -1,0 +1,88 @@
+// Internal interfaces between the host-side C ABI (msa_api.cu) and the kernels.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace msa {
+
+constexpr int kHeadDim = 128;
+constexpr int kBlock = 64;     // token block of the sparse formats
+constexpr int kTileM = 128;    // query rows per attention CTA (two row blocks)
+constexpr int kTileN = 128;    // keys per attention tile (two key blocks)
+constexpr int kLastQMax = 64;  // estimate rows handled by one estimate CTA
+constexpr int kMaxUnits = 65535;
+
+// Device status word bits (first word of every workspace).
+constexpr uint32_t kStatusTimeout = 1u;
+
+// A selected (batch, query head) pair and the KV head it reads.
+struct UnitMap {
+  int n_heads;   // selected query heads per batch entry
+  int heads[1024];
+};
+
+struct TensorView {
+  const __nv_bfloat16* data;
+  int64_t sb, sh, sn;
+};
+
+// Per-call geometry shared by the kernels.
+struct Geometry {
+  int B, Hq, Hkv, G, N, NB, NQ;  // NB = N/64 row blocks, NQ = ceil(N/128) query tiles
+  int n_units;
+  float scale;
+};
+
+// ---------------------------------------------------------------- prefill
+enum PrefillKind : int { kPrefillVS = 0, kPrefillBS = 1, kPrefillST = 2 };
+
+struct PrefillParams {
+  Geometry g;
+  int kind;
+  float scale_log2;  // scale * log2(e)
+  __nv_bfloat16* out;
+  int64_t out_sb, out_sh, out_sn;
+  // vertical-slash plan (per unit strides)
+  const uint32_t* tile_dist;  // [units][dist_words] bit t: tile distance t active
+  int dist_words;
+  const int32_t* qdelta;       // [units][NQ+1] ascending active 128-tile distances
+  const int32_t* qdelta_count; // [units]
+  const uint32_t* col_chunks;  // [units][NQ][chunk_words] bit c: column chunk c needed
+  int chunk_words;
+  const int32_t* vertical;     // [units][kv] ascending chosen key columns
+  int kv;                      // number of chosen columns
+  int kv_pad;                  // rows per unit in the gathered K/V buffers (multiple of 128)
+  // block-sparse plan
+  const int32_t* bs_tiles;       // [units][NQ][bs_tile_cap] (q << 4) | quadrant mask
+  const int32_t* bs_tile_count;  // [units][NQ]
+  int bs_tile_cap;
+  // streaming plan
+  int init_num, local_num;
+  uint32_t* status;
+  UnitMap units;
+};
+
+// ---------------------------------------------------------------- launches
+cudaError_t launch_vs_estimate(const Geometry& g, const UnitMap& u, TensorView q, TensorView k,
+                               int last_q, float* partial, int n_split, float* row_stats,
+                               float* v_score, float* s_score, cudaStream_t st, int* n_launch);
+cudaError_t launch_topk(const float* scores, int64_t n, int64_t row_stride, int rows, int k,
+                        int32_t* out_idx, int64_t out_stride, cudaStream_t st, int* n_launch);
+cudaError_t launch_vs_index(const Geometry& g, const UnitMap& u, TensorView k, TensorView v,
+                            const int32_t* slash, int ks, const int32_t* vertical, int kv,
+                            uint32_t* tile_dist, int dist_words, int32_t* qdelta,
+                            int32_t* qdelta_count, uint32_t* col_chunks, int chunk_words,
+                            __nv_bfloat16* kc, __nv_bfloat16* vc, int kv_pad, cudaStream_t st,
+                            int* n_launch);
+cudaError_t launch_bs_index(const Geometry& g, const UnitMap& u, TensorView q, TensorView k,
+                            int topk, float* qpool, float* kpool, int32_t* block_count,
+                            int32_t* block_ids, int32_t* tiles, int32_t* tile_count,
+                            int tile_cap, cudaStream_t st, int* n_launch);
+cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                           const CUtensorMap& mv, const CUtensorMap& mkc, const CUtensorMap& mvc,
+                           cudaStream_t st, int* n_launch);
+
+}  // namespace msa

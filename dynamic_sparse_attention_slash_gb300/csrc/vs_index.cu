@@ -1,0 +1,168 @@
+// Vertical-slash sparse format (MInference 1.0 overview, section 2.2,
+// "Vertical-Slash Head": convert the chosen vertical and slash lines to a
+// sparse format for block-sparse computation).
+//
+// The format is kept compact instead of listing tiles per row block:
+//  * tile_dist: bit t is set iff some chosen offset o has floor(o/64) == t, or
+//    floor(o/64) + 1 == t with o % 64 != 0.  For row block m, key tile n <= m is
+//    active iff bit m - n is set: the diagonal at offset o = 64a + b (b > 0)
+//    through rows [64m, 64m+63] lands on keys [64(m-a) - b, 64(m-a) + 63 - b],
+//    which meets tiles m-a and m-a-1 (only m-a when b == 0).  The set is the
+//    same for every row block.
+//  * qdelta: ascending distances D between 128-row query tiles and 128-key
+//    tiles that hold at least one active 64x64 quadrant (quadrant distances
+//    2D-1, 2D, 2D+1).
+//  * col_chunks: per 128-row query tile p, bit c is set iff some chosen key in
+//    positions [128c, 128c+128) of the ascending vertical list is needed as a
+//    column by row block 2p or 2p+1, i.e. lies at or before the block's last
+//    row and outside the block's active tiles.
+//  * kc / vc: the K and V rows of the chosen vertical keys, gathered into a
+//    contiguous per-unit buffer so column chunks load like ordinary tiles.
+#include "block_scan.cuh"
+#include "msa_internal.h"
+
+namespace msa {
+namespace {
+
+constexpr int kTilesThreads = 512;
+
+__global__ void __launch_bounds__(kTilesThreads) vs_tile_dist_kernel(
+    const int32_t* __restrict__ slash, int ks, int NB, int NQ, uint32_t* __restrict__ tile_dist,
+    int dist_words, int32_t* __restrict__ qdelta, int32_t* __restrict__ qdelta_count) {
+  extern __shared__ uint32_t bits[];
+  __shared__ int warp_sums[kTilesThreads / 32 + 1];
+  const int unit = blockIdx.x, tid = threadIdx.x;
+  for (int w = tid; w < dist_words; w += kTilesThreads) bits[w] = 0u;
+  __syncthreads();
+  const int32_t* S = slash + static_cast<int64_t>(unit) * ks;
+  for (int s = tid; s < ks; s += kTilesThreads) {
+    const int o = S[s];
+    const int t = o >> 6;
+    atomicOr(&bits[t >> 5], 1u << (t & 31));
+    if (o & 63) atomicOr(&bits[(t + 1) >> 5], 1u << ((t + 1) & 31));
+  }
+  __syncthreads();
+  uint32_t* dst = tile_dist + static_cast<int64_t>(unit) * dist_words;
+  for (int w = tid; w < dist_words; w += kTilesThreads) dst[w] = bits[w];
+  auto bit = [&](int t) -> bool { return (bits[t >> 5] >> (t & 31)) & 1u; };
+  int32_t* qd = qdelta + static_cast<int64_t>(unit) * NQ;
+  int written = 0;
+  for (int base = 0; base < NQ; base += kTilesThreads) {
+    const int d = base + tid;
+    bool act = false;
+    if (d < NQ) act = bit(2 * d) || bit(2 * d + 1) || (d > 0 && bit(2 * d - 1));
+    int total;
+    const int pos = block_exclusive_scan<kTilesThreads>(act ? 1 : 0, warp_sums, &total);
+    if (act) qd[written + pos] = d;
+    written += total;
+  }
+  if (tid == 0) qdelta_count[unit] = written;
+}
+
+// One warp per (unit, query tile p, 32-chunk word).
+__global__ void vs_col_chunks_kernel(const int32_t* __restrict__ vertical, int kv, int NB, int NQ,
+                                     const uint32_t* __restrict__ tile_dist, int dist_words,
+                                     uint32_t* __restrict__ col_chunks, int chunk_words,
+                                     int n_units) {
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t per_unit = static_cast<int64_t>(NQ) * chunk_words;
+  if (gw >= per_unit * n_units) return;
+  const int unit = static_cast<int>(gw / per_unit);
+  const int rem = static_cast<int>(gw % per_unit);
+  const int p = rem / chunk_words, w = rem % chunk_words;
+  const int n_chunks = (kv + 127) / 128;
+  const int c = 32 * w + lane;
+  const int32_t* V = vertical + static_cast<int64_t>(unit) * kv;
+  const uint32_t* dist = tile_dist + static_cast<int64_t>(unit) * dist_words;
+  bool need = false;
+  if (c < n_chunks) {
+    const int s_end = min(128 * c + 128, kv);
+    const int last_row = min(64 * (2 * p + 1) + 63, 64 * NB - 1);
+    for (int s = 128 * c; s < s_end && !need; ++s) {
+      const int j = V[s];
+      if (j > last_row) break;  // ascending: later keys are after the tile too
+      for (int a = 0; a < 2; ++a) {
+        const int m = 2 * p + a;
+        if (m >= NB || j > 64 * m + 63) continue;
+        const int t = m - (j >> 6);
+        if (!((dist[t >> 5] >> (t & 31)) & 1u)) need = true;
+      }
+    }
+  }
+  const uint32_t word = __ballot_sync(0xffffffffu, need);
+  if (lane == 0) col_chunks[(static_cast<int64_t>(unit) * NQ + p) * chunk_words + w] = word;
+}
+
+struct GatherArgs {
+  UnitMap u;
+  int G, kv, kv_pad;
+  const __nv_bfloat16* k;
+  int64_t k_sb, k_sh, k_sn;
+  const __nv_bfloat16* v;
+  int64_t v_sb, v_sh, v_sn;
+  const int32_t* vertical;
+  __nv_bfloat16* kc;
+  __nv_bfloat16* vc;
+};
+
+// One warp per gathered row; rows past kv are zero.
+__global__ void vs_gather_kernel(const __grid_constant__ GatherArgs a) {
+  const int unit = blockIdx.y;
+  const int s = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (s >= a.kv_pad) return;
+  const int b = unit / a.u.n_heads;
+  const int hkv = a.u.heads[unit % a.u.n_heads] / a.G;
+  uint2 kx = make_uint2(0u, 0u), vx = make_uint2(0u, 0u);
+  if (s < a.kv) {
+    const int j = a.vertical[static_cast<int64_t>(unit) * a.kv + s];
+    kx = reinterpret_cast<const uint2*>(a.k + b * a.k_sb + hkv * a.k_sh + j * a.k_sn)[lane];
+    vx = reinterpret_cast<const uint2*>(a.v + b * a.v_sb + hkv * a.v_sh + j * a.v_sn)[lane];
+  }
+  const int64_t row = static_cast<int64_t>(unit) * a.kv_pad + s;
+  reinterpret_cast<uint2*>(a.kc + row * kHeadDim)[lane] = kx;
+  reinterpret_cast<uint2*>(a.vc + row * kHeadDim)[lane] = vx;
+}
+
+}  // namespace
+
+cudaError_t launch_vs_index(const Geometry& g, const UnitMap& u, TensorView k, TensorView v,
+                            const int32_t* slash, int ks, const int32_t* vertical, int kv,
+                            uint32_t* tile_dist, int dist_words, int32_t* qdelta,
+                            int32_t* qdelta_count, uint32_t* col_chunks, int chunk_words,
+                            __nv_bfloat16* kc, __nv_bfloat16* vc, int kv_pad, cudaStream_t st,
+                            int* n_launch) {
+  cudaError_t e;
+  const int smem = dist_words * 4;
+  if (smem > 48 * 1024) {
+    e = cudaFuncSetAttribute(vs_tile_dist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+  }
+  vs_tile_dist_kernel<<<g.n_units, kTilesThreads, smem, st>>>(slash, ks, g.NB, g.NQ, tile_dist,
+                                                             dist_words, qdelta, qdelta_count);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  ++*n_launch;
+  const int64_t warps = static_cast<int64_t>(g.n_units) * g.NQ * chunk_words;
+  const int64_t blocks = (warps * 32 + 255) / 256;
+  vs_col_chunks_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+      vertical, kv, g.NB, g.NQ, tile_dist, dist_words, col_chunks, chunk_words, g.n_units);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  ++*n_launch;
+  GatherArgs a;
+  a.u = u;
+  a.G = g.G;
+  a.kv = kv;
+  a.kv_pad = kv_pad;
+  a.k = k.data; a.k_sb = k.sb; a.k_sh = k.sh; a.k_sn = k.sn;
+  a.v = v.data; a.v_sb = v.sb; a.v_sh = v.sh; a.v_sn = v.sn;
+  a.vertical = vertical;
+  a.kc = kc;
+  a.vc = vc;
+  vs_gather_kernel<<<dim3((kv_pad + 7) / 8, g.n_units), 256, 0, st>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  ++*n_launch;
+  return cudaSuccess;
+}
+
+}  // namespace msa

@@ -1,0 +1,252 @@
+"""Python binding of libmsa (argument marshalling only).
+
+Every function here forwards torch tensors to the C ABI declared in
+include/msa.h as raw device pointers plus the current CUDA stream; all
+computation happens in the library's CUDA kernels.  The library must have
+been built (``python -m dynamic_sparse_attention_slash_gb300.build`` or
+``__graft_entry__.build()``): there is no fallback.
+
+Host (CPU) tensors are accepted for the end-to-end path: they are copied to the
+device on the call's stream, the kernels run, and the output is copied back.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG_DIR, "libmsa.so")
+
+MSA_OK = 0
+MSA_ERR_INVALID = 1
+MSA_ERR_UNSUPPORTED = 2
+MSA_ERR_WORKSPACE = 3
+MSA_ERR_CUDA = 4
+MSA_ERR_TIMEOUT = 5
+
+MSA_KIND_VERTICAL_SLASH = 0
+MSA_KIND_BLOCK_SPARSE = 1
+MSA_KIND_STREAMING = 2
+
+MSA_STAGE_ESTIMATE = 0
+MSA_STAGE_TOPK = 1
+MSA_STAGE_INDEX = 2
+MSA_STAGE_PREFILL = 3
+MSA_STAGE_COUNT = 4
+
+EXPORTED_SYMBOLS = (
+    "msa_vertical_slash", "msa_block_sparse", "msa_streaming", "msa_workspace_bytes",
+    "msa_device_status", "msa_status_string", "msa_kernel_launches",
+)
+
+
+class MsaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+class MsaTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("B", ctypes.c_int64), ("H", ctypes.c_int64),
+                ("N", ctypes.c_int64), ("D", ctypes.c_int64), ("sb", ctypes.c_int64),
+                ("sh", ctypes.c_int64), ("sn", ctypes.c_int64)]
+
+
+class MsaIndexExport(ctypes.Structure):
+    _fields_ = [("v_score", ctypes.c_void_p), ("s_score", ctypes.c_void_p),
+                ("vertical", ctypes.c_void_p), ("slash", ctypes.c_void_p),
+                ("tile_dist", ctypes.c_void_p), ("block_count", ctypes.c_void_p),
+                ("block_ids", ctypes.c_void_p)]
+
+
+class MsaOpts(ctypes.Structure):
+    _fields_ = [("stream", ctypes.c_void_p), ("last_q", ctypes.c_int64), ("scale", ctypes.c_float),
+                ("heads", ctypes.POINTER(ctypes.c_int32)), ("n_heads", ctypes.c_int32),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("export_idx", ctypes.POINTER(MsaIndexExport)),
+                ("stage_events", ctypes.POINTER(ctypes.c_void_p)), ("flags", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def load_library():
+    """Loads libmsa.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build the CUDA library first "
+                          "(python -m dynamic_sparse_attention_slash_gb300.build)")
+    lib = ctypes.CDLL(LIB_PATH)
+    T = ctypes.POINTER(MsaTensor)
+    O = ctypes.POINTER(MsaOpts)
+    lib.msa_vertical_slash.argtypes = [T, T, T, ctypes.c_int64, ctypes.c_int64, T, O]
+    lib.msa_vertical_slash.restype = ctypes.c_int
+    lib.msa_block_sparse.argtypes = [T, T, T, ctypes.c_int64, T, O]
+    lib.msa_block_sparse.restype = ctypes.c_int
+    lib.msa_streaming.argtypes = [T, T, T, ctypes.c_int64, ctypes.c_int64, T, O]
+    lib.msa_streaming.restype = ctypes.c_int
+    lib.msa_workspace_bytes.argtypes = [ctypes.c_int, T, T, ctypes.c_int64, ctypes.c_int64,
+                                        ctypes.c_int32]
+    lib.msa_workspace_bytes.restype = ctypes.c_size_t
+    lib.msa_device_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    lib.msa_device_status.restype = ctypes.c_int
+    lib.msa_status_string.argtypes = [ctypes.c_int]
+    lib.msa_status_string.restype = ctypes.c_char_p
+    lib.msa_kernel_launches.argtypes = []
+    lib.msa_kernel_launches.restype = ctypes.c_uint64
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().msa_status_string(status).decode()
+
+
+def kernel_launches() -> int:
+    """Kernel launches libmsa has enqueued in this process."""
+    return int(load_library().msa_kernel_launches())
+
+
+def describe(t: torch.Tensor) -> MsaTensor:
+    """msa_tensor view of a [B, H, N, D] bf16 tensor (pointer, shape, element strides)."""
+    if t.dim() != 4:
+        raise ValueError("expected a [B, H, N, D] tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError("expected bf16")
+    if t.stride(3) != 1:
+        raise ValueError("the head dimension must be contiguous")
+    B, H, N, D = t.shape
+    return MsaTensor(t.data_ptr(), B, H, N, D, t.stride(0), t.stride(1), t.stride(2))
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def workspace_bytes(kind: int, q: torch.Tensor, k: torch.Tensor, p0: int = 0, p1: int = 0,
+                    n_heads: int = 0) -> int:
+    lib = load_library()
+    qt, kt = describe(q), describe(k)
+    return int(lib.msa_workspace_bytes(kind, ctypes.byref(qt), ctypes.byref(kt), p0, p1, n_heads))
+
+
+def device_status(workspace: torch.Tensor, stream=None) -> int:
+    return int(load_library().msa_device_status(ctypes.c_void_p(workspace.data_ptr()),
+                                                ctypes.c_void_p(_stream_ptr(stream))))
+
+
+class _Prepared:
+    """Keeps every buffer a call touches alive until the call returns.
+
+    Host inputs are copied to the current device on the call's stream; the
+    device output is copied back into `out` (or a new pinned tensor).
+    """
+
+    def __init__(self, q, k, v, out, stream):
+        self.host = q.device.type == "cpu"
+        self.stream = stream
+        self.host_out = None
+        if self.host:
+            dev = torch.device("cuda", torch.cuda.current_device())
+            s = stream if stream is not None else torch.cuda.current_stream(dev)
+            self.host_out = out
+            with torch.cuda.stream(s):
+                q, k, v = (t.to(dev, non_blocking=True) for t in (q, k, v))
+                out = torch.zeros_like(q) if out is None else out.to(dev, non_blocking=True)
+        elif out is None:
+            out = torch.zeros_like(q)
+        self.q, self.k, self.v, self.out = q, k, v, out
+
+    def result(self):
+        if not self.host:
+            return self.out
+        s = self.stream if self.stream is not None else torch.cuda.current_stream()
+        if self.host_out is None:
+            self.host_out = torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
+        with torch.cuda.stream(s):
+            self.host_out.copy_(self.out, non_blocking=True)
+        s.synchronize()
+        return self.host_out
+
+
+def _opts(q, k, kind, p0, p1, last_q, scale, heads, workspace, export, stage_events, stream,
+          keep):
+    opts = MsaOpts()
+    opts.stream = _stream_ptr(stream)
+    opts.last_q = int(last_q)
+    opts.scale = float(scale or 0.0)
+    if heads is not None:
+        arr = (ctypes.c_int32 * len(heads))(*[int(h) for h in heads])
+        keep.append(arr)
+        opts.heads = ctypes.cast(arr, ctypes.POINTER(ctypes.c_int32))
+        opts.n_heads = len(heads)
+    n_heads = len(heads) if heads is not None else 0
+    if workspace is None and kind is not None:
+        nbytes = workspace_bytes(kind, q, k, p0, p1, n_heads)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    if workspace is not None:
+        keep.append(workspace)
+        opts.workspace = workspace.data_ptr()
+        opts.workspace_bytes = workspace.numel() * workspace.element_size()
+    if export is not None:
+        ex = MsaIndexExport(**{name: (t.data_ptr() if t is not None else None)
+                               for name, t in export.items()})
+        keep.append(ex)
+        opts.export_idx = ctypes.pointer(ex)
+    if stage_events is not None:
+        arr = (ctypes.c_void_p * (2 * MSA_STAGE_COUNT))(*[ev.cuda_event for ev in stage_events])
+        keep.append(arr)
+        opts.stage_events = arr
+    return opts, workspace
+
+
+def _run(fn_name, kind, q, k, v, args, out, p0, p1, last_q, scale, heads, workspace, export,
+         stage_events, stream):
+    lib = load_library()
+    prep = _Prepared(q, k, v, out, stream)
+    keep = []
+    opts, _ = _opts(prep.q, prep.k, kind, p0, p1, last_q, scale, heads, workspace, export,
+                    stage_events, stream, keep)
+    qt, kt, vt, ot = describe(prep.q), describe(prep.k), describe(prep.v), describe(prep.out)
+    status = getattr(lib, fn_name)(ctypes.byref(qt), ctypes.byref(kt), ctypes.byref(vt), *args,
+                                   ctypes.byref(ot), ctypes.byref(opts))
+    if status != MSA_OK:
+        raise MsaError(status, fn_name)
+    return prep.result()
+
+
+def msa_vertical_slash(q, k, v, vertical_topk: int, slash: int, out=None, *, last_q: int = 64,
+                       scale: Optional[float] = None, heads: Optional[Sequence[int]] = None,
+                       workspace=None, export=None, stage_events=None, stream=None):
+    """Vertical-slash sparse attention (MInference 1.0 overview, section 2.2).
+
+    q [B,Hq,N,128], k/v [B,Hkv,N,128] bf16.  Writes the selected heads of `out`
+    (allocated with zeros when None) and returns it.
+    """
+    return _run("msa_vertical_slash", MSA_KIND_VERTICAL_SLASH, q, k, v,
+                (ctypes.c_int64(vertical_topk), ctypes.c_int64(slash)), out, vertical_topk, slash,
+                last_q, scale, heads, workspace, export, stage_events, stream)
+
+
+def msa_block_sparse(q, k, v, topk: int, out=None, *, scale: Optional[float] = None,
+                     heads: Optional[Sequence[int]] = None, workspace=None, export=None,
+                     stage_events=None, stream=None):
+    """Block-sparse attention (MInference 1.0 overview, section 2.2)."""
+    return _run("msa_block_sparse", MSA_KIND_BLOCK_SPARSE, q, k, v, (ctypes.c_int64(topk),), out,
+                topk, 0, 0, scale, heads, workspace, export, stage_events, stream)
+
+
+def msa_streaming(q, k, v, init_num: int, local_window_num: int, out=None, *,
+                  scale: Optional[float] = None, heads: Optional[Sequence[int]] = None,
+                  workspace=None, stage_events=None, stream=None):
+    """Streaming / A-shape attention (MInference 1.0 overview, kernel listing)."""
+    return _run("msa_streaming", MSA_KIND_STREAMING, q, k, v,
+                (ctypes.c_int64(init_num), ctypes.c_int64(local_window_num)), out, 0, 0, 0, scale,
+                heads, workspace, None, stage_events, stream)

@@ -1,0 +1,195 @@
+/*
+ * msa.h -- C ABI of libmsa: MInference-style dynamic sparse prefill attention
+ * for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The three entry points mirror the kernel-level API listed on the MInference
+ * 1.0 overview page (developer.volcengine.com article, "using only the kernel"):
+ *
+ *   vertical_slash_sparse_attention(q, k, v, vertical_topk, slash)
+ *   block_sparse_attention(q, k, v, topk)
+ *   streaming_forward(q, k, v, init_num, local_window_num)
+ *
+ * Each computes, for every selected query head, A(M) = Softmax(Q K^T / sqrt(d)
+ * - c (1 - M)) V (same page, section 1 "Problem Formulation") with masked
+ * entries excluded exactly (c -> infinity) and a per-head dynamic mask M built
+ * as that page's section 2.2 describes.  A row whose mask admits no key is
+ * written as zeros.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Tensors   q and out are [B, Hq, N, D]; k and v are [B, Hkv, N, D]; all bf16 in
+ *           device memory, innermost dimension contiguous, other strides given
+ *           in elements and multiples of 8 (16 bytes), base addresses 16-byte
+ *           aligned.  Query head h reads KV head h / (Hq / Hkv).
+ * Supported D = 128, N a positive multiple of 64, Hq a multiple of Hkv.  Other
+ *           shapes return MSA_ERR_UNSUPPORTED before anything is enqueued.
+ * Causal    Key j is admitted for query i only if j <= i.
+ * Blocks    Block quantities count 64-token blocks.
+ * Memory    The caller owns every buffer.  The library allocates no device
+ *           memory; entry points that need scratch space take it from
+ *           opts->workspace, sized by msa_workspace_bytes().  One workspace
+ *           must not be shared by calls that may overlap on the GPU.
+ * Streams   Work is enqueued on opts->stream (NULL: the legacy default
+ *           stream) and runs asynchronously; a return of MSA_OK means every
+ *           launch was enqueued.  Nothing synchronises with the host.
+ * Errors    No exception crosses this ABI.  Invalid arguments are rejected on
+ *           the host with MSA_ERR_INVALID / MSA_ERR_UNSUPPORTED /
+ *           MSA_ERR_WORKSPACE before any work is enqueued; a launch failure
+ *           returns MSA_ERR_CUDA.  Every device-side wait is bounded: a wait
+ *           that runs out records MSA_ERR_TIMEOUT in the workspace status word,
+ *           which msa_device_status() reads back.
+ */
+#ifndef MSA_H_
+#define MSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define MSA_OK 0
+#define MSA_ERR_INVALID 1     /* bad pointer, shape, stride or parameter value */
+#define MSA_ERR_UNSUPPORTED 2 /* valid but outside what this build handles (D != 128, N % 64 != 0) */
+#define MSA_ERR_WORKSPACE 3   /* workspace missing, misaligned or too small */
+#define MSA_ERR_CUDA 4        /* a CUDA call or kernel launch failed */
+#define MSA_ERR_TIMEOUT 5     /* a bounded device-side wait gave up (read by msa_device_status) */
+
+/* Workspace kinds for msa_workspace_bytes(). */
+#define MSA_KIND_VERTICAL_SLASH 0
+#define MSA_KIND_BLOCK_SPARSE 1
+#define MSA_KIND_STREAMING 2
+
+/* Stage ids for msa_opts.stage_events (CUDA events recorded around each stage). */
+#define MSA_STAGE_ESTIMATE 0 /* vertical-slash: last-query estimate (both passes) */
+#define MSA_STAGE_TOPK 1     /* vertical-slash: top-k of vertical and slash scores */
+#define MSA_STAGE_INDEX 2    /* vertical-slash: sparse format; block-sparse: pool, score, select */
+#define MSA_STAGE_PREFILL 3  /* sparse attention itself */
+#define MSA_STAGE_COUNT 4
+
+#define MSA_MAX_HEADS 1024 /* most query heads one call may select */
+
+/* A bf16 tensor [B, H, N, D] in device memory. Strides are in elements. */
+typedef struct msa_tensor {
+  void* data;
+  int64_t B, H, N, D;
+  int64_t sb, sh, sn; /* the D dimension is contiguous (stride 1) */
+} msa_tensor;
+
+/*
+ * Optional copies of intermediate index data, for tests and diagnostics.
+ * Every pointer is a caller-owned device buffer or NULL (skipped).  "units"
+ * are the selected (batch, head) pairs in order b * n_heads + t, where t is
+ * the position of the head in opts->heads.
+ *
+ * vertical-slash:
+ *   v_score   float [units][N]   column sums of the estimated attention
+ *   s_score   float [units][N]   diagonal sums, index = offset o = i - j
+ *   vertical  int32 [units][min(vertical_topk, N)] chosen key columns, ascending
+ *   slash     int32 [units][min(slash, N)]          chosen offsets, ascending
+ *   tile_dist uint32 [units][(N/64 + 32) / 32]      bit t set iff 64x64 key tile
+ *             m - t is active for row block m (the set is the same for every m)
+ * block-sparse:
+ *   block_count int32 [units][N/64]             blocks kept per row block
+ *   block_ids   int32 [units][N/64][min(topk, N/64)] kept key blocks, ascending
+ *               (entries past block_count are unspecified)
+ */
+typedef struct msa_index_export {
+  float* v_score;
+  float* s_score;
+  int32_t* vertical;
+  int32_t* slash;
+  uint32_t* tile_dist;
+  int32_t* block_count;
+  int32_t* block_ids;
+} msa_index_export;
+
+typedef struct msa_opts {
+  void* stream;          /* cudaStream_t; NULL = legacy default stream */
+  int64_t last_q;        /* vertical-slash estimate rows; 0 = 64; 1..64 accepted */
+  float scale;           /* logit scale; 0 = 1/sqrt(D) */
+  const int32_t* heads;  /* HOST array of query-head ids (ascending not required, no repeats); NULL = all */
+  int32_t n_heads;       /* length of heads (ignored when heads is NULL) */
+  void* workspace;       /* device scratch, 256-byte aligned */
+  size_t workspace_bytes;
+  const msa_index_export* export_idx; /* NULL = no export */
+  void* const* stage_events; /* NULL, or cudaEvent_t[2 * MSA_STAGE_COUNT]: start/stop per stage */
+  int32_t flags;             /* reserved, must be 0 */
+} msa_opts;
+
+/*
+ * Vertical-slash head (MInference 1.0 overview, section 2.2, "Vertical-Slash Head").
+ *
+ * For each selected query head: the last last_q query rows are multiplied with
+ * every key and soft-maxed causally (the estimate A-hat); the vertical score of
+ * key j is the column sum of A-hat, the slash score of offset o the sum along
+ * diagonal i - j = o.  The top min(vertical_topk, N) keys and top min(slash, N)
+ * offsets are kept (score descending, ties to the lower index).  Every kept
+ * offset is widened to the 64x64 key tiles its diagonal crosses; kept keys that
+ * no active tile of a row block covers become extra columns of that block.
+ * Attention then runs over active tiles plus columns.
+ *
+ * vertical_topk >= 1, slash >= 1 (larger than N is clamped).  Needs a workspace
+ * of msa_workspace_bytes(MSA_KIND_VERTICAL_SLASH, q, k, vertical_topk, slash).
+ */
+int msa_vertical_slash(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v,
+                       int64_t vertical_topk, int64_t slash, msa_tensor* out,
+                       const msa_opts* opts);
+
+/*
+ * Block-sparse head (same page, section 2.2, "Block-Sparse Head").
+ *
+ * Q and K are mean-pooled over 64-token blocks; block scores are
+ * scale * Qhat_m . Khat_n for n <= m.  Row block m keeps its own (diagonal)
+ * block plus the min(topk, m+1) - 1 best earlier blocks (score descending, ties
+ * to the lower block), then attends to the kept blocks.
+ *
+ * topk >= 1 (larger than N/64 is clamped).  Needs a workspace of
+ * msa_workspace_bytes(MSA_KIND_BLOCK_SPARSE, q, k, topk, 0).
+ */
+int msa_block_sparse(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v,
+                     int64_t topk, msa_tensor* out, const msa_opts* opts);
+
+/*
+ * Streaming / A-shape head (same page, kernel listing: streaming_forward).
+ *
+ * Row block m attends to key blocks [0, init_num) and [m - local_window_num + 1, m]
+ * (the window counts the query's own block), each cut to [0, m].
+ *
+ * init_num >= 0, local_window_num >= 1.  Uses the workspace only for the
+ * device status word (opts->workspace may be NULL: timeouts are then not
+ * reported).
+ */
+int msa_streaming(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v,
+                  int64_t init_num, int64_t local_window_num, msa_tensor* out,
+                  const msa_opts* opts);
+
+/*
+ * Workspace bytes needed by one call.  kind is MSA_KIND_*; p0/p1 are
+ * (vertical_topk, slash) for vertical-slash, (topk, unused) for block-sparse.
+ * n_heads is the number of selected query heads (<= 0: all of q's heads).
+ * Returns 0 for invalid arguments.
+ */
+size_t msa_workspace_bytes(int kind, const msa_tensor* q, const msa_tensor* k, int64_t p0,
+                           int64_t p1, int32_t n_heads);
+
+/*
+ * Reads (and clears) the device status word of a workspace after the work of
+ * an earlier call has been enqueued on `stream`; synchronises that stream.
+ * Returns MSA_OK, MSA_ERR_TIMEOUT, or MSA_ERR_CUDA if the copy itself failed.
+ */
+int msa_device_status(void* workspace, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* msa_status_string(int status);
+
+/* Number of kernel launches this library has enqueued in this process. */
+uint64_t msa_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H_ */

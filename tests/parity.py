@@ -1,0 +1,98 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path through the C ABI
+with index export, and compare it with the oracle under the stated rules.
+
+Rules (spec tolerances):
+* index sets are compared exactly; a top-k set may differ from the oracle's
+  only by elements whose oracle score lies within 1e-5 (relative) of the
+  oracle's k-th score, and then the downstream format and outputs are checked
+  against the oracle run on the GPU's own sets;
+* bf16 outputs: max |diff| <= 1e-2 and mean |diff| <= 1e-3 against the fp64
+  oracle given identical indices.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import msa_oracle as O
+from dynamic_sparse_attention_slash_gb300 import msa
+
+MAX_TOL = 1e-2
+MEAN_TOL = 1e-3
+TIE_REL = 1e-5
+
+
+def to_np(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def run_vs(q, k, v, vertical_topk, slash, last_q=64, heads=None):
+    """CUDA vertical-slash call with index export; returns (out, export dict of numpy)."""
+    B, Hq, N, _ = q.shape
+    heads_l = list(range(Hq)) if heads is None else list(heads)
+    U = B * len(heads_l)
+    kv, ks = min(vertical_topk, N), min(slash, N)
+    dev = q.device
+    ex = {
+        "v_score": torch.empty(U, N, dtype=torch.float32, device=dev),
+        "s_score": torch.empty(U, N, dtype=torch.float32, device=dev),
+        "vertical": torch.empty(U, kv, dtype=torch.int32, device=dev),
+        "slash": torch.empty(U, ks, dtype=torch.int32, device=dev),
+        "tile_dist": torch.empty(U, (N // 64 + 32) // 32, dtype=torch.int32, device=dev),
+    }
+    out = msa.msa_vertical_slash(q, k, v, vertical_topk, slash, last_q=last_q, heads=heads,
+                                 export=ex)
+    torch.cuda.synchronize()
+    return out, {name: t.cpu().numpy() for name, t in ex.items()}
+
+
+def run_bs(q, k, v, topk, heads=None):
+    B, Hq, N, _ = q.shape
+    heads_l = list(range(Hq)) if heads is None else list(heads)
+    U = B * len(heads_l)
+    NB = N // 64
+    kb = min(topk, NB)
+    dev = q.device
+    ex = {
+        "block_count": torch.empty(U, NB, dtype=torch.int32, device=dev),
+        "block_ids": torch.empty(U, NB, kb, dtype=torch.int32, device=dev),
+    }
+    out = msa.msa_block_sparse(q, k, v, topk, heads=heads, export=ex)
+    torch.cuda.synchronize()
+    return out, {name: t.cpu().numpy() for name, t in ex.items()}
+
+
+def check_topk(gpu_set, oracle_scores, k, what):
+    """Exact set equality, except near-ties at the k-th score (see module doc)."""
+    ref = O.topk_indices(oracle_scores, k)
+    got = np.asarray(gpu_set, dtype=np.int64)
+    assert np.all(np.diff(got) > 0), f"{what}: GPU set not strictly ascending"
+    if np.array_equal(got, ref):
+        return 0
+    assert got.size == ref.size, f"{what}: size {got.size} != {ref.size}"
+    kth = np.sort(oracle_scores)[::-1][min(k, oracle_scores.size) - 1]
+    diff = np.setxor1d(got, ref)
+    tol = TIE_REL * max(abs(kth), 1e-30)
+    bad = diff[np.abs(oracle_scores[diff] - kth) > tol]
+    assert bad.size == 0, (f"{what}: {diff.size} differing indices, {bad.size} not near-ties; "
+                           f"e.g. {bad[:5]} scores {oracle_scores[bad[:5]]} vs kth {kth}")
+    return int(diff.size)
+
+
+def dist_bits_to_active(words, NB):
+    """Expand the exported tile-distance bitset into the [NB, NB] active-tile matrix."""
+    words = np.asarray(words, dtype=np.int64) & 0xFFFFFFFF
+    bits = np.array([(words[t >> 5] >> (t & 31)) & 1 for t in range(NB)], dtype=bool)
+    act = np.zeros((NB, NB), dtype=bool)
+    for m in range(NB):
+        act[m, :m + 1] = bits[m - np.arange(m + 1)]
+    return act
+
+
+def compare_out(got, ref, what):
+    got = np.asarray(got, dtype=np.float64)
+    d = np.abs(got - ref)
+    mx, mean = float(d.max()), float(d.mean())
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    assert mx <= MAX_TOL and mean <= MEAN_TOL, f"{what}: max|d| {mx:.3e} mean|d| {mean:.3e}"
+    return mx, mean

@@ -1,0 +1,126 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/msa.h declares, sizes workspaces, and rejects bad arguments on the
+host before anything is enqueued (fake, never-dereferenced pointers)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dynamic_sparse_attention_slash_gb300 import build, msa
+    build.build()
+    return msa.load_library()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "msa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(msa_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_function(lib):
+    from dynamic_sparse_attention_slash_gb300 import msa
+    names = declared_functions()
+    assert set(msa.EXPORTED_SYMBOLS) <= set(names)
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def T(B=1, H=4, N=1024, D=128, ptr=0x10000, sb=None, sh=None, sn=None):
+    from dynamic_sparse_attention_slash_gb300.msa import MsaTensor
+    sn = D if sn is None else sn
+    sh = N * sn if sh is None else sh
+    sb = H * sh if sb is None else sb
+    return MsaTensor(ptr, B, H, N, D, sb, sh, sn)
+
+
+def opts(**kw):
+    from dynamic_sparse_attention_slash_gb300.msa import MsaOpts
+    o = MsaOpts()
+    for k_, v_ in kw.items():
+        setattr(o, k_, v_)
+    return o
+
+
+def call_vs(lib, q, k, v, out, kv=100, ks=100, o=None):
+    return lib.msa_vertical_slash(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), kv, ks,
+                                  ctypes.byref(out), ctypes.byref(o) if o is not None else None)
+
+
+def test_workspace_bytes(lib):
+    q, k = T(H=32), T(H=8)
+    vs = lib.msa_workspace_bytes(0, ctypes.byref(q), ctypes.byref(k), 1000, 6096, 0)
+    bs = lib.msa_workspace_bytes(1, ctypes.byref(q), ctypes.byref(k), 100, 0, 0)
+    st = lib.msa_workspace_bytes(2, ctypes.byref(q), ctypes.byref(k), 0, 0, 0)
+    assert vs > 32 * 1024 * 4 * 2 and bs > 0 and st == 256
+    assert vs % 256 == 0 and bs % 256 == 0
+    assert lib.msa_workspace_bytes(0, ctypes.byref(q), ctypes.byref(k), 0, 6096, 0) == 0
+    assert lib.msa_workspace_bytes(7, ctypes.byref(q), ctypes.byref(k), 1, 1, 0) == 0
+    # fewer heads need less
+    assert lib.msa_workspace_bytes(0, ctypes.byref(q), ctypes.byref(k), 1000, 6096, 4) < vs
+
+
+@pytest.mark.parametrize("case,expect", [
+    ("null_q", 1), ("d64", 2), ("n100", 2), ("misaligned", 1), ("gqa", 1), ("kv0", 1),
+    ("flags", 1), ("lastq", 1), ("head_range", 1), ("head_dup", 1), ("no_ws", 3),
+    ("small_ws", 3), ("ws_align", 3), ("odd_stride", 1), ("n_mismatch", 1),
+])
+def test_vertical_slash_rejects(lib, case, expect):
+    q, k, v, out = T(), T(H=2), T(H=2), T()
+    o = opts(workspace=0x100000, workspace_bytes=1 << 40)
+    kv = 100
+    if case == "null_q":
+        q = T(ptr=0)
+    elif case == "d64":
+        q, out = T(D=64), T(D=64)
+    elif case == "n100":
+        q, k, v, out = T(N=100), T(H=2, N=100), T(H=2, N=100), T(N=100)
+    elif case == "misaligned":
+        k = T(H=2, ptr=0x10008)
+    elif case == "gqa":
+        k, v = T(H=3), T(H=3)
+    elif case == "kv0":
+        kv = 0
+    elif case == "flags":
+        o.flags = 1
+    elif case == "lastq":
+        o.last_q = 65
+    elif case in ("head_range", "head_dup"):
+        arr = (ctypes.c_int32 * 2)(*([0, 4] if case == "head_range" else [1, 1]))
+        o.heads = ctypes.cast(arr, ctypes.POINTER(ctypes.c_int32))
+        o.n_heads = 2
+    elif case == "no_ws":
+        o = None
+    elif case == "small_ws":
+        o.workspace_bytes = 1024
+    elif case == "ws_align":
+        o.workspace = 0x100010
+    elif case == "odd_stride":
+        q = T(sn=130)
+    elif case == "n_mismatch":
+        v = T(H=2, N=2048)
+    assert call_vs(lib, q, k, v, out, kv=kv, o=o) == expect
+
+
+def test_block_sparse_and_streaming_reject(lib):
+    q, k, v, out = T(), T(H=2), T(H=2), T()
+    o = opts(workspace=0x100000, workspace_bytes=1 << 40)
+    args = [ctypes.byref(x) for x in (q, k, v)]
+    assert lib.msa_block_sparse(*args, 0, ctypes.byref(out), ctypes.byref(o)) == 1
+    assert lib.msa_block_sparse(*args, 5, ctypes.byref(out), None) == 3
+    assert lib.msa_streaming(*args, -1, 4, ctypes.byref(out), ctypes.byref(o)) == 1
+    assert lib.msa_streaming(*args, 1, 0, ctypes.byref(out), ctypes.byref(o)) == 1
+    small = opts(workspace=0x100000, workspace_bytes=64)
+    assert lib.msa_streaming(*args, 1, 4, ctypes.byref(out), ctypes.byref(small)) == 3
+
+
+def test_status_strings_and_counter(lib):
+    for code in range(6):
+        assert lib.msa_status_string(code)
+    assert lib.msa_status_string(99) == b"unknown status"
+    assert lib.msa_kernel_launches() >= 0

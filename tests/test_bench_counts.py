@@ -1,0 +1,39 @@
+"""The benchmark's exact pair counts (its FLOP numerator) agree with the
+oracle's mask popcounts on small cases."""
+import numpy as np
+import pytest
+
+import bench
+from oracle import msa_oracle as O
+
+
+def dist_words(S, N):
+    NB = N // 64
+    words = np.zeros((NB + 32) // 32, dtype=np.int64)
+    for o in S:
+        for t in ([o // 64] + ([o // 64 + 1] if o % 64 else [])):
+            words[t >> 5] |= 1 << (t & 31)
+    return words
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_vs_pairs_match_mask_popcount(seed):
+    rng = np.random.default_rng(seed)
+    N = 64 * int(rng.integers(1, 24))
+    S = np.sort(rng.choice(N, size=int(rng.integers(1, 10)), replace=False))
+    V = np.sort(rng.choice(N, size=int(rng.integers(1, 30)), replace=False))
+    act = O.vs_active_tiles(S, N)
+    cols = O.vs_columns(V, act, N)
+    q = k = v = np.zeros((N, 128))
+    _, counts = O.attend_blocks(q, k, v, O.vs_block_mask(act, cols, N), 1.0)
+    assert bench.vs_pairs(dist_words(S, N), V, N) == int(counts.sum())
+
+
+def test_bs_and_st_pairs():
+    N = 1024
+    rng = np.random.default_rng(0)
+    q, k = rng.standard_normal((N, 128)), rng.standard_normal((N, 128))
+    sel, _ = O.block_sparse_blocks(q, k, 3)
+    assert bench.bs_pairs([len(s) for s in sel]) == O.nnz_from_blocks(sel, N)
+    st = [O.streaming_blocks(m, 2, 3) for m in range(N // 64)]
+    assert bench.st_pairs(N, 2, 3) == O.nnz_from_blocks(st, N)

@@ -1,0 +1,166 @@
+"""CUDA path vs the fp64 oracle on sizes the oracle finishes in seconds.
+
+Every case spans several 128-row query tiles; the ragged cases end on a
+half tile (N % 128 == 64) and use vertical counts that are not multiples of
+the 128-key column chunk.  All calls go through the C ABI (ctypes binding).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import msa_oracle as O
+from dynamic_sparse_attention_slash_gb300 import inputs, msa
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+D = 128
+
+
+def qkv(B, Hq, Hkv, N, seed, vs=True, bs=False):
+    q, k, v = inputs.make_qkv(B, Hq, Hkv, N, seed, vs_planting=vs, bs_planting=bs, device="cpu")
+    return q.cuda(), k.cuda(), v.cuda()
+
+
+def np64(t):
+    return P.to_np(t)
+
+
+# ----------------------------------------------------------------------------- streaming / dense
+@pytest.mark.parametrize("N,Hq,Hkv", [(640, 2, 1), (1024, 4, 2), (64, 1, 1)])
+def test_streaming_full_window_is_dense_causal(N, Hq, Hkv):
+    q, k, v = qkv(1, Hq, Hkv, N, 11)
+    out = msa.msa_streaming(q, k, v, 0, N // 64)
+    torch.cuda.synchronize()
+    qn, kn, vn = np64(q), np64(k), np64(v)
+    for h in range(Hq):
+        ref = O.dense_causal(qn[0, h], kn[0, h // (Hq // Hkv)], vn[0, h // (Hq // Hkv)], 1 / math.sqrt(D))
+        P.compare_out(np64(out[0, h]), ref, f"dense h{h}")
+
+
+@pytest.mark.parametrize("N,init,local", [(1088, 1, 3), (2048, 2, 4), (1536, 0, 1), (960, 3, 2)])
+def test_streaming_matches_oracle(N, init, local):
+    q, k, v = qkv(1, 4, 2, N, 12)
+    out = msa.msa_streaming(q, k, v, init, local)
+    torch.cuda.synchronize()
+    ref, _ = O.streaming_forward(q.cpu(), k.cpu(), v.cpu(), init, local)
+    P.compare_out(np64(out[0]), ref[0], f"streaming N={N} init={init} local={local}")
+
+
+def test_streaming_head_subset_leaves_other_heads():
+    q, k, v = qkv(2, 4, 2, 512, 13)
+    out = torch.full_like(q, 7.0)
+    msa.msa_streaming(q, k, v, 1, 2, out=out, heads=[3, 0])
+    torch.cuda.synchronize()
+    ref, _ = O.streaming_forward(q.cpu(), k.cpu(), v.cpu(), 1, 2, heads=[3, 0])
+    for b in range(2):
+        P.compare_out(np64(out[b, 3]), ref[b, 0], "h3")
+        P.compare_out(np64(out[b, 0]), ref[b, 1], "h0")
+        assert (out[b, 1] == 7.0).all() and (out[b, 2] == 7.0).all()
+
+
+# ----------------------------------------------------------------------------- block-sparse
+@pytest.mark.parametrize("N,topk", [(2048, 5), (2112, 8), (1024, 100), (4096, 3), (640, 1)])
+def test_block_sparse_matches_oracle(N, topk):
+    q, k, v = qkv(1, 4, 2, N, 14, vs=False, bs=True)
+    out, ex = P.run_bs(q, k, v, topk)
+    qn, kn, vn = np64(q), np64(k), np64(v)
+    NB = N // 64
+    for h in range(4):
+        g = h // 2
+        sel, S = O.block_sparse_blocks(qn[0, h], kn[0, g], topk)
+        gpu_sel = []
+        for m in range(NB):
+            cnt = int(ex["block_count"][h, m])
+            assert cnt == min(topk, m + 1)
+            got = ex["block_ids"][h, m, :cnt]
+            assert got[-1] == m, "diagonal block must be kept"
+            if m > 0:
+                P.check_topk(got[:-1], S[m, :m], topk - 1, f"h{h} m{m}")
+            gpu_sel.append(got.astype(np.int64))
+        ref, _ = O.attend_blocks(qn[0, h], kn[0, g], vn[0, g], O.block_mask_from_blocks(gpu_sel, N),
+                                 1 / math.sqrt(D))
+        P.compare_out(np64(out[0, h]), ref, f"bs h{h}")
+
+
+# ----------------------------------------------------------------------------- vertical-slash
+def check_vs_case(q, k, v, vertical_topk, slash, last_q=64, heads=None):
+    out, ex = P.run_vs(q, k, v, vertical_topk, slash, last_q=last_q, heads=heads)
+    B, Hq, N, _ = q.shape
+    G = Hq // k.shape[1]
+    heads_l = list(range(Hq)) if heads is None else list(heads)
+    qn, kn, vn = np64(q), np64(k), np64(v)
+    scale = 1 / math.sqrt(D)
+    NB = N // 64
+    for b in range(B):
+        for t, h in enumerate(heads_l):
+            u = b * len(heads_l) + t
+            vs_, ss_, _ = O.estimate_vs(qn[b, h], kn[b, h // G], last_q, scale)
+            np.testing.assert_allclose(ex["v_score"][u], vs_, rtol=1e-4, atol=1e-6 * max(1, vs_.max()))
+            np.testing.assert_allclose(ex["s_score"][u], ss_, rtol=1e-4, atol=1e-6 * max(1, ss_.max()))
+            P.check_topk(ex["vertical"][u], vs_, vertical_topk, f"vertical u{u}")
+            P.check_topk(ex["slash"][u], ss_, slash, f"slash u{u}")
+            V = ex["vertical"][u].astype(np.int64)
+            S = ex["slash"][u].astype(np.int64)
+            act = O.vs_active_tiles(S, N)
+            np.testing.assert_array_equal(P.dist_bits_to_active(ex["tile_dist"][u], NB), act)
+            cols = O.vs_columns(V, act, N)
+            ref, _ = O.attend_blocks(qn[b, h], kn[b, h // G], vn[b, h // G],
+                                     O.vs_block_mask(act, cols, N), scale)
+            P.compare_out(np64(out[b, h]), ref, f"vs b{b} h{h}")
+    return out, ex
+
+
+def test_vertical_slash_tiny_workload():
+    """The 4096-token single-head workload in full: scores, sets, format, outputs."""
+    w, q, k, v, _ = inputs.make_workload("vs_tiny", device="cpu")
+    check_vs_case(q.cuda(), k.cuda(), v.cuda(), w.vertical_topk, w.slash)
+
+
+@pytest.mark.parametrize("N,kv,ks,last_q", [(2368, 300, 200, 64), (1088, 130, 40, 64),
+                                            (2048, 64, 2048, 32), (960, 960, 1, 64),
+                                            (64, 5, 3, 64)])
+def test_vertical_slash_ragged(N, kv, ks, last_q):
+    q, k, v = qkv(1, 4, 2, N, 15)
+    check_vs_case(q, k, v, kv, ks, last_q=last_q)
+
+
+def test_vertical_slash_batch_and_head_subset():
+    q, k, v = qkv(2, 4, 1, 1024, 16)
+    check_vs_case(q, k, v, 100, 150, heads=[2, 1])
+
+
+def test_vertical_topk_covering_all_keys_is_dense():
+    q, k, v = qkv(1, 2, 1, 1152, 17)
+    out, _ = P.run_vs(q, k, v, 5000, 2)
+    qn, kn, vn = np64(q), np64(k), np64(v)
+    for h in range(2):
+        P.compare_out(np64(out[0, h]), O.dense_causal(qn[0, h], kn[0, 0], vn[0, 0], 1 / math.sqrt(D)),
+                      f"dense-by-columns h{h}")
+
+
+# ----------------------------------------------------------------------------- determinism / status
+def test_repeat_calls_are_bit_identical_and_status_ok():
+    q, k, v = qkv(1, 4, 2, 2048, 18, bs=True)
+    ws = torch.empty(msa.workspace_bytes(msa.MSA_KIND_VERTICAL_SLASH, q, k, 300, 400),
+                     dtype=torch.uint8, device="cuda")
+    a = msa.msa_vertical_slash(q, k, v, 300, 400, workspace=ws)
+    b = msa.msa_vertical_slash(q, k, v, 300, 400, workspace=ws)
+    assert torch.equal(a, b)
+    assert msa.device_status(ws) == msa.MSA_OK
+    c = msa.msa_block_sparse(q, k, v, 7)
+    d = msa.msa_block_sparse(q, k, v, 7)
+    assert torch.equal(c, d)
+    e = msa.msa_streaming(q, k, v, 1, 3)
+    f = msa.msa_streaming(q, k, v, 1, 3)
+    assert torch.equal(e, f)
+
+
+def test_host_tensors_round_trip():
+    q, k, v = inputs.make_qkv(1, 2, 1, 640, 19, device="cpu")
+    out = msa.msa_streaming(q.pin_memory(), k.pin_memory(), v.pin_memory(), 1, 2)
+    assert out.device.type == "cpu"
+    ref, _ = O.streaming_forward(q, k, v, 1, 2)
+    P.compare_out(np64(out[0]), ref[0], "host path")
