@@ -70,7 +70,7 @@ int prepare(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v, const
   c.last_q = (opts && opts->last_q) ? static_cast<int>(opts->last_q) : kLastQMax;
   if (opts && (opts->last_q < 0 || opts->last_q > kLastQMax)) return MSA_ERR_INVALID;
   c.scale = (opts && opts->scale != 0.f) ? opts->scale : 1.0f / std::sqrt(static_cast<float>(q->D));
-  if (!std::isfinite(c.scale)) return MSA_ERR_INVALID;
+  if (!std::isfinite(c.scale) || c.scale <= 0.f) return MSA_ERR_INVALID;
   // head selection
   std::memset(&c.u, 0, sizeof(c.u));
   if (opts && opts->heads) {
@@ -122,8 +122,13 @@ constexpr size_t kStatusBytes = 256;
 struct VSLayout {
   int kv, ks, kv_pad, n_split, dist_words, chunk_words;
   size_t partial, v_score, s_score, vertical, slash, tile_dist, qdelta, qdelta_count, col_chunks,
-      kc, vc, total;
+      kc, vc, v16, total;
 };
+
+// f16 copy of v for the P.V product: [B][Hkv][N][128], contiguous.
+size_t v16_elems(const Geometry& g) {
+  return static_cast<size_t>(g.B) * g.Hkv * g.N * kHeadDim;
+}
 
 int vs_split(int units, int NB) {
   int s = (608 + units - 1) / units;
@@ -153,14 +158,15 @@ VSLayout vs_layout(const Geometry& g, int64_t vertical_topk, int64_t slash) {
   L.qdelta_count = c.take<int32_t>(U);
   L.col_chunks = c.take<uint32_t>(U * g.NQ * L.chunk_words);
   L.kc = c.take<__nv_bfloat16>(U * L.kv_pad * kHeadDim);
-  L.vc = c.take<__nv_bfloat16>(U * L.kv_pad * kHeadDim);
+  L.vc = c.take<__half>(U * L.kv_pad * kHeadDim);
+  L.v16 = c.take<__half>(v16_elems(g));
   L.total = (c.off + 255) & ~size_t{255};
   return L;
 }
 
 struct BSLayout {
   int kb, tile_cap;
-  size_t qpool, kpool, block_count, block_ids, tiles, tile_count, total;
+  size_t qpool, kpool, block_count, block_ids, tiles, tile_count, v16, total;
 };
 
 BSLayout bs_layout(const Geometry& g, int64_t topk) {
@@ -176,6 +182,20 @@ BSLayout bs_layout(const Geometry& g, int64_t topk) {
   L.block_ids = c.take<int32_t>(U * g.NB * L.kb);
   L.tiles = c.take<int32_t>(U * g.NQ * L.tile_cap);
   L.tile_count = c.take<int32_t>(U * g.NQ);
+  L.v16 = c.take<__half>(v16_elems(g));
+  L.total = (c.off + 255) & ~size_t{255};
+  return L;
+}
+
+struct STLayout {
+  size_t v16, total;
+};
+
+STLayout st_layout(const Geometry& g) {
+  STLayout L;
+  Carver c;
+  c.off = kStatusBytes;
+  L.v16 = c.take<__half>(v16_elems(g));
   L.total = (c.off + 255) & ~size_t{255};
   return L;
 }
@@ -193,7 +213,8 @@ T* at(void* ws, size_t off) {
 }
 
 // ------------------------------------------------------------------ TMA maps
-int make_map_4d(CUtensorMap* m, const msa_tensor* t) {
+int make_map_4d(CUtensorMap* m, const msa_tensor* t,
+                CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto fn = encode_fn();
   if (!fn) return MSA_ERR_CUDA;
   const int64_t sh = t->H > 1 ? t->sh : t->N * t->sn;
@@ -204,20 +225,34 @@ int make_map_4d(CUtensorMap* m, const msa_tensor* t) {
                            static_cast<cuuint64_t>(sb * 2)};
   cuuint32_t box[4] = {64, 128, 1, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t->data, dims, strides, box, es,
+  const CUresult r = fn(m, dtype, 4, t->data, dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MSA_OK : MSA_ERR_INVALID;
 }
 
-int make_map_rows(CUtensorMap* m, void* base, int64_t rows) {
+// Contiguous [B][H][N][128] f16 buffer (the staged copy of v).
+int make_map_f16(CUtensorMap* m, void* base, const Geometry& g) {
+  msa_tensor t;
+  t.data = base;
+  t.B = g.B;
+  t.H = g.Hkv;
+  t.N = g.N;
+  t.D = kHeadDim;
+  t.sn = kHeadDim;
+  t.sh = static_cast<int64_t>(g.N) * kHeadDim;
+  t.sb = t.sh * g.Hkv;
+  return make_map_4d(m, &t, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+}
+
+int make_map_rows(CUtensorMap* m, void* base, int64_t rows, CUtensorMapDataType dtype) {
   auto fn = encode_fn();
   if (!fn) return MSA_ERR_CUDA;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim * 2)};
   cuuint32_t box[2] = {64, 128};
   cuuint32_t es[2] = {1, 1};
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, es,
+  const CUresult r = fn(m, dtype, 2, base, dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MSA_OK : MSA_ERR_INVALID;
@@ -285,7 +320,7 @@ size_t msa_workspace_bytes(int kind, const msa_tensor* q, const msa_tensor* k, i
     if (p0 <= 0) return 0;
     return bs_layout(g, p0).total;
   }
-  if (kind == MSA_KIND_STREAMING) return kStatusBytes;
+  if (kind == MSA_KIND_STREAMING) return st_layout(g).total;
   return 0;
 }
 
@@ -300,9 +335,11 @@ int msa_vertical_slash(const msa_tensor* q, const msa_tensor* k, const msa_tenso
   if ((s = check_workspace(opts, L.total))) return s;
   void* ws = opts->workspace;
   CUtensorMap mq, mk, mv, mkc, mvc;
-  if ((s = make_map_4d(&mq, q)) || (s = make_map_4d(&mk, k)) || (s = make_map_4d(&mv, v)) ||
-      (s = make_map_rows(&mkc, at<void>(ws, L.kc), static_cast<int64_t>(c.g.n_units) * L.kv_pad)) ||
-      (s = make_map_rows(&mvc, at<void>(ws, L.vc), static_cast<int64_t>(c.g.n_units) * L.kv_pad)))
+  const int64_t crow = static_cast<int64_t>(c.g.n_units) * L.kv_pad;
+  if ((s = make_map_4d(&mq, q)) || (s = make_map_4d(&mk, k)) ||
+      (s = make_map_f16(&mv, at<void>(ws, L.v16), c.g)) ||
+      (s = make_map_rows(&mkc, at<void>(ws, L.kc), crow, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16)) ||
+      (s = make_map_rows(&mvc, at<void>(ws, L.vc), crow, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)))
     return s;
   const StageTimer tm{opts->stage_events, c.st};
   int launches = 0;
@@ -327,7 +364,10 @@ int msa_vertical_slash(const msa_tensor* q, const msa_tensor* k, const msa_tenso
                       at<int32_t>(ws, L.vertical), L.kv, at<uint32_t>(ws, L.tile_dist),
                       L.dist_words, at<int32_t>(ws, L.qdelta), at<int32_t>(ws, L.qdelta_count),
                       at<uint32_t>(ws, L.col_chunks), L.chunk_words, at<__nv_bfloat16>(ws, L.kc),
-                      at<__nv_bfloat16>(ws, L.vc), L.kv_pad, c.st, &launches);
+                      at<__half>(ws, L.vc), L.kv_pad, at<uint32_t>(ws, 0), c.st, &launches);
+  if (e == cudaSuccess)
+    e = launch_v_to_f16(view(v), c.g.B, c.g.Hkv, c.g.N, at<__half>(ws, L.v16), at<uint32_t>(ws, 0),
+                        c.st, &launches);
   tm.end(MSA_STAGE_INDEX);
   if (e != cudaSuccess) return finish(e, launches);
   PrefillParams p = base_prefill(c, out, at<uint32_t>(ws, 0));
@@ -371,13 +411,17 @@ int msa_block_sparse(const msa_tensor* q, const msa_tensor* k, const msa_tensor*
   void* ws = opts->workspace;
   CUtensorMap mq, mk, mv, mdummy;
   std::memset(&mdummy, 0, sizeof(mdummy));
-  if ((s = make_map_4d(&mq, q)) || (s = make_map_4d(&mk, k)) || (s = make_map_4d(&mv, v)))
+  if ((s = make_map_4d(&mq, q)) || (s = make_map_4d(&mk, k)) ||
+      (s = make_map_f16(&mv, at<void>(ws, L.v16), c.g)))
     return s;
   const StageTimer tm{opts->stage_events, c.st};
   int launches = 0;
   cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), c.st);
   if (e != cudaSuccess) return finish(e, launches);
   tm.begin(MSA_STAGE_INDEX);
+  e = launch_v_to_f16(view(v), c.g.B, c.g.Hkv, c.g.N, at<__half>(ws, L.v16), at<uint32_t>(ws, 0),
+                      c.st, &launches);
+  if (e != cudaSuccess) return finish(e, launches);
   e = launch_bs_index(c.g, c.u, view(q), view(k), static_cast<int>(L.kb < topk ? L.kb : topk),
                       at<float>(ws, L.qpool), at<float>(ws, L.kpool), at<int32_t>(ws, L.block_count),
                       at<int32_t>(ws, L.block_ids), at<int32_t>(ws, L.tiles),
@@ -411,23 +455,24 @@ int msa_streaming(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v,
   int s = prepare(q, k, v, out, opts, c);
   if (s) return s;
   if (init_num < 0 || local_window_num < 1) return MSA_ERR_INVALID;
-  uint32_t* status = nullptr;
-  if (opts && opts->workspace) {
-    if ((s = check_workspace(opts, kStatusBytes))) return s;
-    status = static_cast<uint32_t*>(opts->workspace);
-  }
+  const STLayout L = st_layout(c.g);
+  if ((s = check_workspace(opts, L.total))) return s;
+  void* ws = opts->workspace;
   CUtensorMap mq, mk, mv, mdummy;
   std::memset(&mdummy, 0, sizeof(mdummy));
-  if ((s = make_map_4d(&mq, q)) || (s = make_map_4d(&mk, k)) || (s = make_map_4d(&mv, v)))
+  if ((s = make_map_4d(&mq, q)) || (s = make_map_4d(&mk, k)) ||
+      (s = make_map_f16(&mv, at<void>(ws, L.v16), c.g)))
     return s;
-  const StageTimer tm{opts ? opts->stage_events : nullptr, c.st};
+  const StageTimer tm{opts->stage_events, c.st};
   int launches = 0;
-  cudaError_t e = cudaSuccess;
-  if (status) {  // without a workspace the kernel has nowhere to report a timeout
-    e = cudaMemsetAsync(status, 0, sizeof(uint32_t), c.st);
-    if (e != cudaSuccess) return finish(e, launches);
-  }
-  PrefillParams p = base_prefill(c, out, status);
+  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), c.st);
+  if (e != cudaSuccess) return finish(e, launches);
+  tm.begin(MSA_STAGE_INDEX);
+  e = launch_v_to_f16(view(v), c.g.B, c.g.Hkv, c.g.N, at<__half>(ws, L.v16), at<uint32_t>(ws, 0),
+                      c.st, &launches);
+  tm.end(MSA_STAGE_INDEX);
+  if (e != cudaSuccess) return finish(e, launches);
+  PrefillParams p = base_prefill(c, out, at<uint32_t>(ws, 0));
   p.kind = kPrefillST;
   const int64_t nb = c.g.NB;
   p.init_num = static_cast<int>(init_num < nb ? init_num : nb);
@@ -446,7 +491,9 @@ int msa_device_status(void* workspace, void* stream) {
     return MSA_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return MSA_ERR_CUDA;
   if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), st) != cudaSuccess) return MSA_ERR_CUDA;
-  return (h & kStatusTimeout) ? MSA_ERR_TIMEOUT : MSA_OK;
+  if (h & kStatusTimeout) return MSA_ERR_TIMEOUT;
+  if (h & kStatusRange) return MSA_ERR_RANGE;
+  return MSA_OK;
 }
 
 const char* msa_status_string(int status) {
@@ -457,6 +504,7 @@ const char* msa_status_string(int status) {
     case MSA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case MSA_ERR_CUDA: return "CUDA error";
     case MSA_ERR_TIMEOUT: return "device-side wait timed out";
+    case MSA_ERR_RANGE: return "a value of v lies outside the f16 range of the P.V product";
     default: return "unknown status";
   }
 }

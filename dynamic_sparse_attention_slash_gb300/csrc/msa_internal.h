@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace msa {
@@ -17,6 +18,7 @@ constexpr int kMaxUnits = 65535;
 
 // Device status word bits (first word of every workspace).
 constexpr uint32_t kStatusTimeout = 1u;
+constexpr uint32_t kStatusRange = 2u;  // a value of v outside the f16 range
 
 // A selected (batch, query head) pair and the KV head it reads.
 struct UnitMap {
@@ -75,12 +77,14 @@ cudaError_t launch_vs_index(const Geometry& g, const UnitMap& u, TensorView k, T
                             const int32_t* slash, int ks, const int32_t* vertical, int kv,
                             uint32_t* tile_dist, int dist_words, int32_t* qdelta,
                             int32_t* qdelta_count, uint32_t* col_chunks, int chunk_words,
-                            __nv_bfloat16* kc, __nv_bfloat16* vc, int kv_pad, cudaStream_t st,
-                            int* n_launch);
+                            __nv_bfloat16* kc, __half* vc, int kv_pad, uint32_t* status,
+                            cudaStream_t st, int* n_launch);
 cudaError_t launch_bs_index(const Geometry& g, const UnitMap& u, TensorView q, TensorView k,
                             int topk, float* qpool, float* kpool, int32_t* block_count,
                             int32_t* block_ids, int32_t* tiles, int32_t* tile_count,
                             int tile_cap, cudaStream_t st, int* n_launch);
+cudaError_t launch_v_to_f16(TensorView v, int B, int Hkv, int N, __half* dst, uint32_t* status,
+                            cudaStream_t st, int* n_launch);
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                            const CUtensorMap& mv, const CUtensorMap& mkc, const CUtensorMap& mvc,
                            cudaStream_t st, int* n_launch);

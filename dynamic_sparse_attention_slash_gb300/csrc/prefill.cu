@@ -299,7 +299,7 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idO = idesc_bf16_f32(128, 128, false, true);
+      constexpr uint32_t idO = idesc_f32acc(128, 128, /*bf16=*/false, false, true);  // f16 P, f16 V
       const uint32_t q_addr = smem_u32(sm.q);
       bool ok = n == 0 || mbar_wait(&sm.q_full, 0, abort);
       tc_fence_after();
@@ -357,13 +357,13 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
       // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[buf], (i >> 1) & 1, abort))) { ok = false; break; }
       tc_fence_after();
+      // raw logits (unscaled) of this row; scale * log2(e) is folded in below
       float x[128];
+      {
+        uint32_t raw[128];
+        tmem_ld128(s_col, raw);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t raw[32];
-        tmem_ld32(s_col + 32 * c, raw);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) x[32 * c + e] = __uint_as_float(raw[e]) * P.scale_log2;
+        for (int e = 0; e < 128; ++e) x[e] = __uint_as_float(raw[e]);
       }
       // ---- mask
       if (it.cols) {
@@ -390,23 +390,28 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
           }
         }
       }
-      // ---- online softmax
-      float mx = -INFINITY;
+      // ---- online softmax (8 independent partial maxima / sums per row)
+      float mx8[8];
 #pragma unroll
-      for (int e = 0; e < 128; ++e) mx = fmaxf(mx, x[e]);
-      const float m_new = fmaxf(m_run, mx);
+      for (int e = 0; e < 8; ++e) mx8[e] = x[e];
+#pragma unroll
+      for (int e = 8; e < 128; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], x[e]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float m_new = fmaxf(m_run, mx * P.scale_log2);
       const bool grow = m_new > m_run + kRescaleThreshold;  // false when both are -inf
       const float m_use = grow ? m_new : m_run;
-      const float base = m_use == -INFINITY ? 0.f : m_use;
-      float rs = 0.f;
+      const float neg_base = m_use == -INFINITY ? 0.f : -m_use;
+      float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       uint32_t pk[64];
 #pragma unroll
       for (int e = 0; e < 64; ++e) {
-        const float p0 = ex2_approx(x[2 * e] - base);
-        const float p1 = ex2_approx(x[2 * e + 1] - base);
-        rs += p0 + p1;
-        pk[e] = pack_bf16x2(p0, p1);
+        const float p0 = ex2_approx(fmaf(x[2 * e], P.scale_log2, neg_base));
+        const float p1 = ex2_approx(fmaf(x[2 * e + 1], P.scale_log2, neg_base));
+        rs8[e & 7] += p0 + p1;
+        pk[e] = pack_f16x2(p0, p1);
       }
+      const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
       const bool correct = grow && m_run != -INFINITY;  // O holds earlier rows' weight
       const float alpha = correct ? ex2_approx(m_run - m_new) : 1.f;
       l_run = (m_run == -INFINITY ? 0.f : l_run * alpha) + rs;
@@ -452,19 +457,16 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
     const bool warp_ok = ok;
     if (warp_ok && n > 0) {
       const float inv = have ? 1.f / l_run : 0.f;
+      uint32_t o[128];
+      tmem_ld128(lane_base + kColO, o);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t o[32];
-        tmem_ld32(lane_base + kColO + 32 * c, o);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv);
-          w.y = pack_bf16x2(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
-          w.z = pack_bf16x2(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
-          w.w = pack_bf16x2(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
-          outv[4 * c + e] = w;
-        }
+      for (int e = 0; e < 16; ++e) {
+        uint4 w;
+        w.x = pack_bf16x2(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv);
+        w.y = pack_bf16x2(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
+        w.z = pack_bf16x2(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
+        w.w = pack_bf16x2(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
+        outv[e] = w;
       }
     } else {
 #pragma unroll
@@ -484,7 +486,53 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
   if (tid == 0 && sm.abort && P.status) atomicOr(P.status, kStatusTimeout);
 }
 
+
+// v (bf16, any strides, [B][Hkv][N][128]) -> dst (f16, contiguous, same shape).
+// The P.V product runs in f16 (P rounded to f16 keeps 3 more mantissa bits than
+// bf16); every bf16 value of magnitude <= 65504 is exactly representable in
+// f16 (tiny values become f16 subnormals, error < 3e-8).  Larger magnitudes
+// set the range bit of the status word.
+__global__ void v_to_f16_kernel(const __nv_bfloat16* __restrict__ v, int64_t sb, int64_t sh,
+                                int64_t sn, int Hkv, int N, int64_t rows, __half* __restrict__ dst,
+                                uint32_t* status) {
+  const int64_t n16 = rows * 16;
+  bool bad = false;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n16;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = idx >> 4;
+    const int c = static_cast<int>(idx & 15);
+    const int64_t bh = row / N;
+    const int n = static_cast<int>(row % N);
+    const int b = static_cast<int>(bh / Hkv), h = static_cast<int>(bh % Hkv);
+    const uint4 raw = *reinterpret_cast<const uint4*>(v + b * sb + h * sh + n * sn + c * 8);
+    const __nv_bfloat162* in = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    uint4 o;
+    uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float lo = __low2float(in[e]), hi = __high2float(in[e]);
+      bad |= fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
+      ow[e] = pack_f16x2(lo, hi);
+    }
+    *reinterpret_cast<uint4*>(dst + row * kHeadDim + c * 8) = o;
+  }
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0 && status)
+    atomicOr(status, kStatusRange);
+}
+
 }  // namespace
+
+cudaError_t launch_v_to_f16(TensorView v, int B, int Hkv, int N, __half* dst, uint32_t* status,
+                            cudaStream_t st, int* n_launch) {
+  const int64_t rows = static_cast<int64_t>(B) * Hkv * N;
+  int64_t blocks = (rows * 16 + 255) / 256;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  v_to_f16_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(v.data, v.sb, v.sh, v.sn, Hkv, N,
+                                                                 rows, dst, status);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) ++*n_launch;
+  return e;
+}
 
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                            const CUtensorMap& mv, const CUtensorMap& mkc, const CUtensorMap& mvc,

@@ -103,10 +103,12 @@ struct GatherArgs {
   int64_t v_sb, v_sh, v_sn;
   const int32_t* vertical;
   __nv_bfloat16* kc;
-  __nv_bfloat16* vc;
+  __half* vc;
+  uint32_t* status;
 };
 
-// One warp per gathered row; rows past kv are zero.
+// One warp per gathered row; rows past kv are zero.  K rows stay bf16; V rows
+// are converted to f16 (exact within the f16 range) for the f16 P.V product.
 __global__ void vs_gather_kernel(const __grid_constant__ GatherArgs a) {
   const int unit = blockIdx.y;
   const int s = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -115,14 +117,23 @@ __global__ void vs_gather_kernel(const __grid_constant__ GatherArgs a) {
   const int b = unit / a.u.n_heads;
   const int hkv = a.u.heads[unit % a.u.n_heads] / a.G;
   uint2 kx = make_uint2(0u, 0u), vx = make_uint2(0u, 0u);
+  bool bad = false;
   if (s < a.kv) {
     const int j = a.vertical[static_cast<int64_t>(unit) * a.kv + s];
     kx = reinterpret_cast<const uint2*>(a.k + b * a.k_sb + hkv * a.k_sh + j * a.k_sn)[lane];
-    vx = reinterpret_cast<const uint2*>(a.v + b * a.v_sb + hkv * a.v_sh + j * a.v_sn)[lane];
+    const uint2 raw = reinterpret_cast<const uint2*>(a.v + b * a.v_sb + hkv * a.v_sh + j * a.v_sn)[lane];
+    const __nv_bfloat162* in = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    const float f0 = __low2float(in[0]), f1 = __high2float(in[0]);
+    const float f2 = __low2float(in[1]), f3 = __high2float(in[1]);
+    bad = fabsf(f0) > 65504.f || fabsf(f1) > 65504.f || fabsf(f2) > 65504.f || fabsf(f3) > 65504.f;
+    __half2 h01 = __floats2half2_rn(f0, f1), h23 = __floats2half2_rn(f2, f3);
+    vx.x = *reinterpret_cast<uint32_t*>(&h01);
+    vx.y = *reinterpret_cast<uint32_t*>(&h23);
   }
   const int64_t row = static_cast<int64_t>(unit) * a.kv_pad + s;
   reinterpret_cast<uint2*>(a.kc + row * kHeadDim)[lane] = kx;
   reinterpret_cast<uint2*>(a.vc + row * kHeadDim)[lane] = vx;
+  if (__any_sync(0xffffffffu, bad) && lane == 0 && a.status) atomicOr(a.status, kStatusRange);
 }
 
 }  // namespace
@@ -131,8 +142,8 @@ cudaError_t launch_vs_index(const Geometry& g, const UnitMap& u, TensorView k, T
                             const int32_t* slash, int ks, const int32_t* vertical, int kv,
                             uint32_t* tile_dist, int dist_words, int32_t* qdelta,
                             int32_t* qdelta_count, uint32_t* col_chunks, int chunk_words,
-                            __nv_bfloat16* kc, __nv_bfloat16* vc, int kv_pad, cudaStream_t st,
-                            int* n_launch) {
+                            __nv_bfloat16* kc, __half* vc, int kv_pad, uint32_t* status,
+                            cudaStream_t st, int* n_launch) {
   cudaError_t e;
   const int smem = dist_words * 4;
   if (smem > 48 * 1024) {
@@ -159,6 +170,7 @@ cudaError_t launch_vs_index(const Geometry& g, const UnitMap& u, TensorView k, T
   a.vertical = vertical;
   a.kc = kc;
   a.vc = vc;
+  a.status = status;
   vs_gather_kernel<<<dim3((kv_pad + 7) / 8, g.n_units), 256, 0, st>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   ++*n_launch;

@@ -26,6 +26,7 @@ MSA_ERR_UNSUPPORTED = 2
 MSA_ERR_WORKSPACE = 3
 MSA_ERR_CUDA = 4
 MSA_ERR_TIMEOUT = 5
+MSA_ERR_RANGE = 6
 
 MSA_KIND_VERTICAL_SLASH = 0
 MSA_KIND_BLOCK_SPARSE = 1

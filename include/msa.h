@@ -26,9 +26,13 @@
  * Causal    Key j is admitted for query i only if j <= i.
  * Blocks    Block quantities count 64-token blocks.
  * Memory    The caller owns every buffer.  The library allocates no device
- *           memory; entry points that need scratch space take it from
+ *           memory; every entry point takes its scratch space from
  *           opts->workspace, sized by msa_workspace_bytes().  One workspace
  *           must not be shared by calls that may overlap on the GPU.
+ * Precision S = Q K^T is a bf16 x bf16 product with f32 accumulation; the
+ *           softmax runs in f32; P and a staged f16 copy of v (exact for
+ *           |v| <= 65504, which is checked) form the P.V product with f32
+ *           accumulation; out is written as bf16 (round to nearest even).
  * Streams   Work is enqueued on opts->stream (NULL: the legacy default
  *           stream) and runs asynchronously; a return of MSA_OK means every
  *           launch was enqueued.  Nothing synchronises with the host.
@@ -56,6 +60,7 @@ extern "C" {
 #define MSA_ERR_WORKSPACE 3   /* workspace missing, misaligned or too small */
 #define MSA_ERR_CUDA 4        /* a CUDA call or kernel launch failed */
 #define MSA_ERR_TIMEOUT 5     /* a bounded device-side wait gave up (read by msa_device_status) */
+#define MSA_ERR_RANGE 6       /* |v| > 65504 somewhere: outside the f16 range of P.V (read by msa_device_status) */
 
 /* Workspace kinds for msa_workspace_bytes(). */
 #define MSA_KIND_VERTICAL_SLASH 0
@@ -65,7 +70,7 @@ extern "C" {
 /* Stage ids for msa_opts.stage_events (CUDA events recorded around each stage). */
 #define MSA_STAGE_ESTIMATE 0 /* vertical-slash: last-query estimate (both passes) */
 #define MSA_STAGE_TOPK 1     /* vertical-slash: top-k of vertical and slash scores */
-#define MSA_STAGE_INDEX 2    /* vertical-slash: sparse format; block-sparse: pool, score, select */
+#define MSA_STAGE_INDEX 2    /* sparse format / pooling and selection, and the f16 copy of v */
 #define MSA_STAGE_PREFILL 3  /* sparse attention itself */
 #define MSA_STAGE_COUNT 4
 
@@ -158,9 +163,8 @@ int msa_block_sparse(const msa_tensor* q, const msa_tensor* k, const msa_tensor*
  * Row block m attends to key blocks [0, init_num) and [m - local_window_num + 1, m]
  * (the window counts the query's own block), each cut to [0, m].
  *
- * init_num >= 0, local_window_num >= 1.  Uses the workspace only for the
- * device status word (opts->workspace may be NULL: timeouts are then not
- * reported).
+ * init_num >= 0, local_window_num >= 1.  Needs a workspace of
+ * msa_workspace_bytes(MSA_KIND_STREAMING, q, k, 0, 0).
  */
 int msa_streaming(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v,
                   int64_t init_num, int64_t local_window_num, msa_tensor* out,
@@ -178,7 +182,8 @@ size_t msa_workspace_bytes(int kind, const msa_tensor* q, const msa_tensor* k, i
 /*
  * Reads (and clears) the device status word of a workspace after the work of
  * an earlier call has been enqueued on `stream`; synchronises that stream.
- * Returns MSA_OK, MSA_ERR_TIMEOUT, or MSA_ERR_CUDA if the copy itself failed.
+ * Returns MSA_OK, MSA_ERR_TIMEOUT, MSA_ERR_RANGE, or MSA_ERR_CUDA if the copy
+ * itself failed.
  */
 int msa_device_status(void* workspace, void* stream);
 

@@ -1,7 +1,7 @@
 """Helpers shared by the GPU parity tests: run the CUDA path through the C ABI
 with index export, and compare it with the oracle under the stated rules.
 
-Rules (spec tolerances):
+Rules (the method's stated parity tolerances):
 * index sets are compared exactly; a top-k set may differ from the oracle's
   only by elements whose oracle score lies within 1e-5 (relative) of the
   oracle's k-th score, and then the downstream format and outputs are checked
@@ -94,5 +94,8 @@ def compare_out(got, ref, what):
     d = np.abs(got - ref)
     mx, mean = float(d.max()), float(d.mean())
     assert np.isfinite(got).all(), f"{what}: non-finite output"
-    assert mx <= MAX_TOL and mean <= MEAN_TOL, f"{what}: max|d| {mx:.3e} mean|d| {mean:.3e}"
+    at = np.unravel_index(int(d.argmax()), d.shape)
+    assert mx <= MAX_TOL and mean <= MEAN_TOL, (
+        f"{what}: max|d| {mx:.3e} at {tuple(int(x) for x in at)} (ref {ref[at]:.5f}, "
+        f"got {got[at]:.5f}) mean|d| {mean:.3e}")
     return mx, mean

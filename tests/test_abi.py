@@ -57,8 +57,9 @@ def test_workspace_bytes(lib):
     vs = lib.msa_workspace_bytes(0, ctypes.byref(q), ctypes.byref(k), 1000, 6096, 0)
     bs = lib.msa_workspace_bytes(1, ctypes.byref(q), ctypes.byref(k), 100, 0, 0)
     st = lib.msa_workspace_bytes(2, ctypes.byref(q), ctypes.byref(k), 0, 0, 0)
-    assert vs > 32 * 1024 * 4 * 2 and bs > 0 and st == 256
-    assert vs % 256 == 0 and bs % 256 == 0
+    assert vs > 32 * 1024 * 4 * 2 and bs > 0 and st > 256
+    assert st >= 8 * 1024 * 128 * 2  # staged f16 copy of v
+    assert vs % 256 == 0 and bs % 256 == 0 and st % 256 == 0
     assert lib.msa_workspace_bytes(0, ctypes.byref(q), ctypes.byref(k), 0, 6096, 0) == 0
     assert lib.msa_workspace_bytes(7, ctypes.byref(q), ctypes.byref(k), 1, 1, 0) == 0
     # fewer heads need less
@@ -120,7 +121,7 @@ def test_block_sparse_and_streaming_reject(lib):
 
 
 def test_status_strings_and_counter(lib):
-    for code in range(6):
+    for code in range(7):
         assert lib.msa_status_string(code)
     assert lib.msa_status_string(99) == b"unknown status"
     assert lib.msa_kernel_launches() >= 0
