@@ -85,21 +85,24 @@ def attend_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, rows, allowed_keys,
     key outputs zeros.
     """
     rows = list(rows)
-    d = q.shape[1]
+    N, d = q.shape
     out = np.zeros((len(rows), d), dtype=np.float64)
     counts = np.zeros(len(rows), dtype=np.int64)
     for r, i in enumerate(rows):
         J = np.asarray(allowed_keys(i))
+        admit = np.zeros(i + 1, dtype=bool)
         if J.dtype == bool:
-            J = np.nonzero(J)[0]
-        J = J[J <= i]
-        counts[r] = J.size
-        if J.size == 0:
+            admit[:] = J[:i + 1]
+        else:
+            admit[J[J <= i]] = True
+        counts[r] = int(admit.sum())
+        if counts[r] == 0:
             continue
-        z = (k[J] @ q[i]) * scale
+        z = (k[:i + 1] @ q[i]) * scale
+        z = np.where(admit, z, -np.inf)
         p = np.exp(z - z.max())
         p /= p.sum()
-        out[r] = p @ v[J]
+        out[r] = p @ v[:i + 1]
     return out, counts
 
 
@@ -172,18 +175,20 @@ def topk_indices(scores, k: int) -> np.ndarray:
     return np.sort(order[:k]).astype(np.int64)
 
 
-def vs_active_tiles(slash_idx, N: int) -> np.ndarray:
+def vs_active_tiles(slash_idx, N: int, row_blocks=None) -> np.ndarray:
     """64x64 tiles crossed by the selected diagonals [MInf-2.2] (sparse format, tile part).
 
     Tile (m, n), n <= m, is active iff some selected offset o has a row
     i in [64m, 64m+63] with i - o inside key tile n, i.e. iff the key range
     [64m - o, 64m + 63 - o] (cut at 0) meets [64n, 64n + 63].
-    Returns a boolean [NB, NB] matrix (row block m, key block n).
+    Returns a boolean [NB, NB] matrix (row block m, key block n); with
+    `row_blocks`, a [len(row_blocks), NB] matrix for those row blocks only.
     """
     NB = (N + BLOCK - 1) // BLOCK
     S = np.asarray(slash_idx, dtype=np.int64)
-    active = np.zeros((NB, NB), dtype=bool)
-    for m in range(NB):
+    blocks = range(NB) if row_blocks is None else list(row_blocks)
+    active = np.zeros((len(blocks), NB), dtype=bool)
+    for r, m in enumerate(blocks):
         first_row = m * BLOCK
         last_row = min(N, (m + 1) * BLOCK) - 1
         lo = first_row - S
@@ -192,7 +197,7 @@ def vs_active_tiles(slash_idx, N: int) -> np.ndarray:
         lo = np.maximum(lo[keep], 0)
         hi = hi[keep]
         for n_lo, n_hi in zip(lo // BLOCK, hi // BLOCK):
-            active[m, n_lo:n_hi + 1] = True
+            active[r, n_lo:n_hi + 1] = True
     return active
 
 
@@ -208,6 +213,23 @@ def vs_columns(vertical_idx, active: np.ndarray, N: int):
         c = c[~active[m, c // BLOCK]]
         cols.append(c)
     return cols
+
+
+def vs_row_block_mask(slash_idx, vertical_idx, N):
+    """Keys admitted for row block m, built for that block alone from the chosen
+    offsets and columns (same rule as vs_active_tiles + vs_columns; for long
+    sequences where the full [NB, NB] tile matrix is not needed)."""
+    V = np.asarray(vertical_idx, dtype=np.int64)
+
+    def mask(m):
+        act = vs_active_tiles(slash_idx, N, [m])[0]
+        last_row = min(N, (m + 1) * BLOCK) - 1
+        c = V[V <= last_row]
+        c = c[~act[c // BLOCK]]
+        allow = np.repeat(act, BLOCK)[:N].copy()
+        allow[c] = True
+        return allow
+    return mask
 
 
 def vs_block_mask(active, cols, N):

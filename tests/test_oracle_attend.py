@@ -128,3 +128,14 @@ def test_attend_rows_and_blocks_agree():
     out_r, cnt_r = O.attend_rows(q, k, v, range(N), lambda i: bm[i // 64], 0.09)
     np.testing.assert_allclose(out_b, out_r, rtol=1e-12, atol=1e-13)
     assert (cnt_b == cnt_r).all()
+
+
+def test_half_ulp_bound_helper():
+    """The output bound's half-ulp term: bf16 spacing is 2^(e-7) on [2^e, 2^(e+1))."""
+    from tests.parity import half_ulp_bf16
+    for x, expect in [(1.0, 2 ** -8), (1.99, 2 ** -8), (2.0, 2 ** -7), (4.14, 2 ** -6),
+                      (-4.14, 2 ** -6), (0.3, 2 ** -10)]:
+        assert half_ulp_bf16(x) == expect
+    # rounding 4.14387 to bf16 (step 1/32 there) lands within half a step
+    r = torch.tensor(4.14387, dtype=torch.float64).to(torch.bfloat16).double().item()
+    assert abs(r - 4.14387) <= half_ulp_bf16(4.14387)

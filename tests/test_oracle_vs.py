@@ -220,3 +220,16 @@ def test_gqa_head_mapping():
     for t, h in enumerate([1, 2]):
         ref, _ = O.vertical_slash_head(q[0, h], k[0, h // 2], v[0, h // 2], 16, 32)
         np.testing.assert_array_equal(out[0, t], ref)
+
+
+def test_row_block_mask_agrees_with_full_format():
+    N = 640
+    rng = np.random.default_rng(9)
+    S = np.sort(rng.choice(N, 7, replace=False))
+    V = np.sort(rng.choice(N, 25, replace=False))
+    act = O.vs_active_tiles(S, N)
+    full = O.vs_block_mask(act, O.vs_columns(V, act, N), N)
+    lazy = O.vs_row_block_mask(S, V, N)
+    for m in range(N // 64):
+        np.testing.assert_array_equal(full(m), lazy(m))
+        np.testing.assert_array_equal(O.vs_active_tiles(S, N, [m])[0], act[m])
