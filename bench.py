@@ -277,7 +277,8 @@ def main():
         ws["bs"] = torch.empty(msa.workspace_bytes(msa.MSA_KIND_BLOCK_SPARSE, q, k, w.block_topk,
                                                    0, len(heads["bs"])), dtype=torch.uint8, device=dev)
     if heads["st"]:
-        ws["st"] = torch.empty(256, dtype=torch.uint8, device=dev)
+        ws["st"] = torch.empty(msa.workspace_bytes(msa.MSA_KIND_STREAMING, q, k, 0, 0,
+                                                   len(heads["st"])), dtype=torch.uint8, device=dev)
 
     def new_events():
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * msa.MSA_STAGE_COUNT)]

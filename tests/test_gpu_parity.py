@@ -164,3 +164,17 @@ def test_host_tensors_round_trip():
     assert out.device.type == "cpu"
     ref, _ = O.streaming_forward(q, k, v, 1, 2)
     P.compare_out(np64(out[0]), ref[0], "host path")
+
+
+def test_value_outside_f16_range_is_reported():
+    """v is staged to f16 for P.V; a value beyond 65504 must be reported, not hidden."""
+    q, k, v = qkv(1, 2, 1, 256, 20)
+    v[0, 0, 5, 3] = 1.0e5
+    ws = torch.empty(msa.workspace_bytes(msa.MSA_KIND_STREAMING, q, k), dtype=torch.uint8,
+                     device="cuda")
+    msa.msa_streaming(q, k, v, 1, 2, workspace=ws)
+    assert msa.device_status(ws) == msa.MSA_ERR_RANGE
+    assert msa.device_status(ws) == msa.MSA_OK  # reading clears the word
+    v[0, 0, 5, 3] = 60000.0
+    msa.msa_streaming(q, k, v, 1, 2, workspace=ws)
+    assert msa.device_status(ws) == msa.MSA_OK
