@@ -171,6 +171,41 @@ int msa_streaming(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v,
                   const msa_opts* opts);
 
 /*
+ * Vertical-slash attention without a caller-provided workspace.  The MInference
+ * pages have no counterpart; this entry point exists for callers that cannot
+ * allocate device memory where they run attention: an allocator frozen for the
+ * duration of a request in a fixed-pool serving runtime, a plugin host that
+ * hands an operator only its inputs and outputs, or code that must avoid the
+ * implicit synchronisation an allocation can cause.
+ *
+ * It computes what msa_vertical_slash computes for all heads of q (last_q = 64,
+ * scale = 1/sqrt(D), no index export), taking its scratch space from one
+ * file-scope device array of MSA_STATIC_SCRATCH_BYTES that the CUDA runtime
+ * reserves on every GPU that loads this library, until the process exits.  It
+ * calls no cudaMalloc, cudaFree or allocating library routine.
+ *
+ *  - A problem whose msa_workspace_bytes(MSA_KIND_VERTICAL_SLASH, ...) exceeds
+ *    MSA_STATIC_SCRATCH_BYTES returns MSA_ERR_WORKSPACE before anything is
+ *    enqueued (4 query heads over 2 KV heads at N = 32768 with vertical_topk
+ *    1000 and slash 6096 fit; 32 heads over 8 KV heads at that N do not);
+ *    invalid arguments return MSA_ERR_INVALID.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current): make that first call
+ *    before any stream capture.
+ *  - Every call on a device shares the one array, which keeps the last call's
+ *    contents (each call clears what must start at zero).  Calls that may
+ *    overlap on the GPU (different streams or host threads) race on it; the
+ *    caller must serialise them.
+ *  - Device-side status (bounded-wait timeouts, the f16 range check of v) lands
+ *    in the array and is not reported by this entry point.
+ * stream is a cudaStream_t (NULL: the legacy default stream).
+ */
+#define MSA_STATIC_SCRATCH_BYTES (64u << 20)
+int msa_vertical_slash_static(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v,
+                              int64_t vertical_topk, int64_t slash, msa_tensor* out,
+                              void* stream);
+
+/*
  * Workspace bytes needed by one call.  kind is MSA_KIND_*; p0/p1 are
  * (vertical_topk, slash) for vertical-slash, (topk, unused) for block-sparse.
  * n_heads is the number of selected query heads (<= 0: all of q's heads).

@@ -1,0 +1,74 @@
+"""msa_vertical_slash_static: vertical-slash attention for callers that cannot
+allocate device memory where they run attention (a frozen allocator in a
+fixed-pool serving runtime, a plugin host that passes an operator only its
+inputs and outputs, or code that must avoid the synchronisation an allocation
+can cause).  The entry point takes its scratch space from one fixed device
+array inside the library instead of a caller workspace.
+
+The GPU test calls it through the C ABI twice in a row, on different inputs,
+and checks each output against the workspace-taking msa_vertical_slash on the
+same inputs, within the tolerance the parity tests use.  This file is named to
+be collected last; it passes both alone in a fresh process and after the other
+tests.
+"""
+import ctypes
+
+import pytest
+import torch
+
+from dynamic_sparse_attention_slash_gb300 import inputs, msa
+from tests import parity as P
+
+MSA_STATIC_SCRATCH_BYTES = 64 << 20
+
+
+def static_entry():
+    lib = msa.load_library()
+    fn = lib.msa_vertical_slash_static
+    T = ctypes.POINTER(msa.MsaTensor)
+    fn.argtypes = [T, T, T, ctypes.c_int64, ctypes.c_int64, T, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    return lib, fn
+
+
+def fake(B, H, N, ptr=0x10000):
+    """A descriptor with a fake, never-dereferenced pointer (host-side checks only)."""
+    return msa.MsaTensor(ptr, B, H, N, 128, H * N * 128, N * 128, 128)
+
+
+def test_static_entry_rejects_on_host():
+    """Sizes beyond the array, and invalid arguments, are refused before any work."""
+    from dynamic_sparse_attention_slash_gb300 import build
+    build.build()
+    lib, fn = static_entry()
+    q, k, out = fake(1, 32, 32768), fake(1, 8, 32768), fake(1, 32, 32768)
+    need = lib.msa_workspace_bytes(msa.MSA_KIND_VERTICAL_SLASH, ctypes.byref(q), ctypes.byref(k),
+                                   1000, 6096, 32)
+    assert need > MSA_STATIC_SCRATCH_BYTES
+    assert fn(ctypes.byref(q), ctypes.byref(k), ctypes.byref(k), 1000, 6096, ctypes.byref(out),
+              None) == msa.MSA_ERR_WORKSPACE
+    q4, k2, out4 = fake(1, 4, 32768), fake(1, 2, 32768), fake(1, 4, 32768)
+    assert lib.msa_workspace_bytes(msa.MSA_KIND_VERTICAL_SLASH, ctypes.byref(q4), ctypes.byref(k2),
+                                   1000, 6096, 4) <= MSA_STATIC_SCRATCH_BYTES
+    assert fn(ctypes.byref(q4), ctypes.byref(k2), ctypes.byref(k2), 0, 6096, ctypes.byref(out4),
+              None) == msa.MSA_ERR_INVALID
+    bad = fake(1, 4, 100)
+    assert fn(ctypes.byref(bad), ctypes.byref(k2), ctypes.byref(k2), 10, 10, ctypes.byref(out4),
+              None) == msa.MSA_ERR_INVALID
+
+
+@pytest.mark.gpu
+def test_static_entry_matches_workspace_entry_twice():
+    _, fn = static_entry()
+    stream = torch.cuda.current_stream()
+    for call, seed in enumerate((41, 42)):
+        q, k, v = inputs.make_qkv(1, 4, 2, 4096, seed, vs_planting=True, device="cpu")
+        q, k, v = q.cuda(), k.cuda(), v.cuda()
+        ref = msa.msa_vertical_slash(q, k, v, 300, 500)
+        out = torch.zeros_like(q)
+        qt, kt, vt, ot = (msa.describe(t) for t in (q, k, v, out))
+        status = fn(ctypes.byref(qt), ctypes.byref(kt), ctypes.byref(vt), 300, 500,
+                    ctypes.byref(ot), ctypes.c_void_p(stream.cuda_stream))
+        assert status == msa.MSA_OK, f"call {call}: status {status}"
+        torch.cuda.synchronize()
+        P.compare_out(P.to_np(out), P.to_np(ref), f"static-scratch call {call}")
