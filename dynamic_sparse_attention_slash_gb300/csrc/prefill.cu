@@ -393,25 +393,32 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
       // ---- online softmax (8 independent partial maxima / sums per row)
       float mx8[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) mx8[e] = x[e];
+      for (int a = 0; a < 8; ++a) {
+        float m = fmax3(x[a], x[8 + a], x[16 + a]);
 #pragma unroll
-      for (int e = 8; e < 128; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], x[e]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int e = 24; e < 120; e += 16) m = fmax3(m, x[e + a], x[e + 8 + a]);
+        mx8[a] = fmaxf(m, x[120 + a]);
+      }
+      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                             fmaxf(mx8[6], mx8[7]));
       const float m_new = fmaxf(m_run, mx * P.scale_log2);
       const bool grow = m_new > m_run + kRescaleThreshold;  // false when both are -inf
       const float m_use = grow ? m_new : m_run;
       const float neg_base = m_use == -INFINITY ? 0.f : -m_use;
-      float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      const float2 scale2 = make_float2(P.scale_log2, P.scale_log2);
+      const float2 nb2 = make_float2(neg_base, neg_base);
+      float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                       make_float2(0.f, 0.f)};
       uint32_t pk[64];
 #pragma unroll
       for (int e = 0; e < 64; ++e) {
-        const float p0 = ex2_approx(fmaf(x[2 * e], P.scale_log2, neg_base));
-        const float p1 = ex2_approx(fmaf(x[2 * e + 1], P.scale_log2, neg_base));
-        rs8[e & 7] += p0 + p1;
-        pk[e] = pack_f16x2(p0, p1);
+        const float2 a = ffma2(make_float2(x[2 * e], x[2 * e + 1]), scale2, nb2);
+        const float2 pe = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+        rs2[e & 3] = fadd2(rs2[e & 3], pe);
+        pk[e] = pack_f16x2(pe.x, pe.y);
       }
-      const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+      const float2 rsa = fadd2(fadd2(rs2[0], rs2[1]), fadd2(rs2[2], rs2[3]));
+      const float rs = rsa.x + rsa.y;
       const bool correct = grow && m_run != -INFINITY;  // O holds earlier rows' weight
       const float alpha = correct ? ex2_approx(m_run - m_new) : 1.f;
       l_run = (m_run == -INFINITY ? 0.f : l_run * alpha) + rs;
