@@ -160,44 +160,48 @@ __global__ void __launch_bounds__(kSelThreads) bs_select_kernel(const __grid_con
 }
 
 struct TileArgs {
-  int NB, NQ, kb, tile_cap, n_units;
+  int NB, npair, kb, tile_cap, n_units;
   const int32_t* block_count;
   const int32_t* block_ids;
-  int32_t* tiles;       // [units][NQ][tile_cap] (q << 4) | quadrant bits (a*2 + b)
-  int32_t* tile_count;  // [units][NQ]
+  int32_t* tiles;       // [units][npair][tile_cap] (q << 8) | maskB << 4 | maskA
+  int32_t* tile_count;  // [units][npair]
 };
 
-// One thread per (unit, query tile p): merge the two row blocks' ascending
-// block lists into 128-key tiles with quadrant masks.
+// One thread per (unit, pair c of 128-row query tiles): merge the ascending
+// block lists of row blocks 4c .. 4c+3 into 128-key tiles with one 4-bit
+// quadrant mask per query tile (bit a*2 + b: row half a sees key half b).
 __global__ void bs_tiles_kernel(TileArgs a) {
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (gid >= static_cast<int64_t>(a.n_units) * a.NQ) return;
-  const int unit = static_cast<int>(gid / a.NQ), p = static_cast<int>(gid % a.NQ);
-  const int m0 = 2 * p, m1 = 2 * p + 1;
-  const int32_t* l0 = a.block_ids + (static_cast<int64_t>(unit) * a.NB + m0) * a.kb;
-  const int c0 = a.block_count[static_cast<int64_t>(unit) * a.NB + m0];
-  const int32_t* l1 = l0 + a.kb;
-  const int c1 = m1 < a.NB ? a.block_count[static_cast<int64_t>(unit) * a.NB + m1] : 0;
+  if (gid >= static_cast<int64_t>(a.n_units) * a.npair) return;
+  const int unit = static_cast<int>(gid / a.npair), c = static_cast<int>(gid % a.npair);
+  const int32_t* lists[4];
+  int cnt[4], pos[4] = {0, 0, 0, 0};
+  for (int j = 0; j < 4; ++j) {
+    const int m = 4 * c + j;
+    lists[j] = a.block_ids + (static_cast<int64_t>(unit) * a.NB + m) * a.kb;
+    cnt[j] = m < a.NB ? a.block_count[static_cast<int64_t>(unit) * a.NB + m] : 0;
+  }
   int32_t* out = a.tiles + gid * a.tile_cap;
-  int i0 = 0, i1 = 0, n = 0, cur_q = -1, cur_mask = 0;
-  while (i0 < c0 || i1 < c1) {
-    int blk, half;
-    if (i1 >= c1 || (i0 < c0 && l0[i0] <= l1[i1])) {
-      blk = l0[i0++];
-      half = 0;
-    } else {
-      blk = l1[i1++];
-      half = 1;
-    }
-    const int q = blk >> 1, bit = half * 2 + (blk & 1);
+  int n = 0, cur_q = -1, cur_mask = 0;
+  for (;;) {
+    int best = -1, blk = 0;
+    for (int j = 0; j < 4; ++j)
+      if (pos[j] < cnt[j] && (best < 0 || lists[j][pos[j]] < blk)) {
+        best = j;
+        blk = lists[j][pos[j]];
+      }
+    if (best < 0) break;
+    ++pos[best];
+    const int q = blk >> 1;
+    const int bit = (best >> 1) * 4 + (best & 1) * 2 + (blk & 1);  // tile, row half, key half
     if (q != cur_q) {
-      if (cur_q >= 0) out[n++] = (cur_q << 4) | cur_mask;
+      if (cur_q >= 0) out[n++] = (cur_q << 8) | cur_mask;
       cur_q = q;
       cur_mask = 0;
     }
     cur_mask |= 1 << bit;
   }
-  if (cur_q >= 0) out[n++] = (cur_q << 4) | cur_mask;
+  if (cur_q >= 0) out[n++] = (cur_q << 8) | cur_mask;
   a.tile_count[gid] = n;
 }
 
@@ -249,7 +253,7 @@ cudaError_t launch_bs_index(const Geometry& g, const UnitMap& u, TensorView q, T
   ++*n_launch;
   TileArgs ta;
   ta.NB = g.NB;
-  ta.NQ = g.NQ;
+  ta.npair = (g.NQ + 1) / 2;
   ta.kb = sa.kb;
   ta.tile_cap = tile_cap;
   ta.n_units = g.n_units;
@@ -257,7 +261,7 @@ cudaError_t launch_bs_index(const Geometry& g, const UnitMap& u, TensorView q, T
   ta.block_ids = block_ids;
   ta.tiles = tiles;
   ta.tile_count = tile_count;
-  const int64_t threads = static_cast<int64_t>(g.n_units) * g.NQ;
+  const int64_t threads = static_cast<int64_t>(g.n_units) * ta.npair;
   bs_tiles_kernel<<<static_cast<unsigned>((threads + 127) / 128), 128, 0, st>>>(ta);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   ++*n_launch;

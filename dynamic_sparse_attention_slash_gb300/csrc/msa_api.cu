@@ -154,7 +154,7 @@ VSLayout vs_layout(const Geometry& g, int64_t vertical_topk, int64_t slash) {
   L.vertical = c.take<int32_t>(U * L.kv);
   L.slash = c.take<int32_t>(U * L.ks);
   L.tile_dist = c.take<uint32_t>(U * L.dist_words);
-  L.qdelta = c.take<int32_t>(U * g.NQ);
+  L.qdelta = c.take<int32_t>(U * (g.NQ + 1));
   L.qdelta_count = c.take<int32_t>(U);
   L.col_chunks = c.take<uint32_t>(U * g.NQ * L.chunk_words);
   L.kc = c.take<__nv_bfloat16>(U * L.kv_pad * kHeadDim);
@@ -172,7 +172,7 @@ struct BSLayout {
 BSLayout bs_layout(const Geometry& g, int64_t topk) {
   BSLayout L;
   L.kb = static_cast<int>(topk < g.NB ? topk : g.NB);
-  L.tile_cap = 2 * L.kb;
+  L.tile_cap = 4 * L.kb;  // a pair of query tiles spans four row blocks
   const size_t U = static_cast<size_t>(g.n_units);
   Carver c;
   c.off = kStatusBytes;
@@ -180,8 +180,9 @@ BSLayout bs_layout(const Geometry& g, int64_t topk) {
   L.kpool = c.take<float>(static_cast<size_t>(g.B) * g.Hkv * g.NB * kHeadDim);
   L.block_count = c.take<int32_t>(U * g.NB);
   L.block_ids = c.take<int32_t>(U * g.NB * L.kb);
-  L.tiles = c.take<int32_t>(U * g.NQ * L.tile_cap);
-  L.tile_count = c.take<int32_t>(U * g.NQ);
+  const size_t npair = static_cast<size_t>(g.NQ + 1) / 2;
+  L.tiles = c.take<int32_t>(U * npair * L.tile_cap);
+  L.tile_count = c.take<int32_t>(U * npair);
   L.v16 = c.take<__half>(v16_elems(g));
   L.total = (c.off + 255) & ~size_t{255};
   return L;
@@ -283,6 +284,7 @@ PrefillParams base_prefill(const Call& c, msa_tensor* out, uint32_t* status) {
   PrefillParams p;
   std::memset(&p, 0, sizeof(p));
   p.g = c.g;
+  p.npair = (c.g.NQ + 1) / 2;
   p.scale_log2 = c.scale * 1.4426950408889634f;
   p.out = static_cast<__nv_bfloat16*>(out->data);
   p.out_sb = out->sb;

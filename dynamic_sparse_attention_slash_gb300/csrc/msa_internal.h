@@ -44,13 +44,14 @@ enum PrefillKind : int { kPrefillVS = 0, kPrefillBS = 1, kPrefillST = 2 };
 struct PrefillParams {
   Geometry g;
   int kind;
+  int npair;         // ceil(NQ / 2): pairs of 128-row query tiles, one CTA each
   float scale_log2;  // scale * log2(e)
   __nv_bfloat16* out;
   int64_t out_sb, out_sh, out_sn;
   // vertical-slash plan (per unit strides)
   const uint32_t* tile_dist;  // [units][dist_words] bit t: tile distance t active
   int dist_words;
-  const int32_t* qdelta;       // [units][NQ+1] ascending active 128-tile distances
+  const int32_t* qdelta;       // [units][NQ+1] ascending tile distances used by a query-tile pair
   const int32_t* qdelta_count; // [units]
   const uint32_t* col_chunks;  // [units][NQ][chunk_words] bit c: column chunk c needed
   int chunk_words;
@@ -58,8 +59,8 @@ struct PrefillParams {
   int kv;                      // number of chosen columns
   int kv_pad;                  // rows per unit in the gathered K/V buffers (multiple of 128)
   // block-sparse plan
-  const int32_t* bs_tiles;       // [units][NQ][bs_tile_cap] (q << 4) | quadrant mask
-  const int32_t* bs_tile_count;  // [units][NQ]
+  const int32_t* bs_tiles;       // [units][npair][bs_tile_cap] (q << 8) | maskB << 4 | maskA
+  const int32_t* bs_tile_count;  // [units][npair]
   int bs_tile_cap;
   // streaming plan
   int init_num, local_num;

@@ -5,64 +5,88 @@
 // modification", Fig. 7: keep a running row max and row sum, rescale the output,
 // divide by the row sum at the end).
 //
-// One CTA computes 128 query rows (row blocks 2p and 2p+1) of one (batch, head)
-// unit over a list of work items, each 128 keys wide:
+// One CTA computes 256 query rows of one (batch, head) unit: two adjacent
+// 128-row query tiles pA = 2c and pB = 2c + 1 (row blocks 4c .. 4c+3), which
+// share every K/V tile they load.  Work items are 128 keys wide:
 //   * a key tile q: keys [128q, 128q+128) of the KV head, with a 4-bit quadrant
-//     mask (bit a*2+b: row half a may see key half b) and the causal cut on the
-//     diagonal tile;
+//     mask per query tile (bit a*2+b: row half a may see key half b) and the
+//     causal cut on each tile's diagonal;
 //   * a column chunk c (vertical-slash only): gathered K/V rows of chosen keys
 //     [128c, 128c+128) of the unit's ascending vertical list, each admitted for
 //     a row iff the key is <= the row and outside the row block's active tiles.
+// The item list is the union of the two query tiles' lists; a tile that does
+// not use an item sees it fully masked.  (Skipping such items per tile was
+// measured slower on GB300: it lengthens the single MMA thread's issue path,
+// which the tensor core waits on.)
 //
-// Warp roles (256 threads):
-//   warp 0   TMA producer for Q and K (one thread)
-//   warp 1   TMEM allocator and tcgen05.mma issuer (one thread)
-//   warp 2   TMA producer for V (one thread)
-//   warp 3   idle
-//   warps 4-7 softmax: thread r owns query row r (TMEM lane r): reads S from
-//            TMEM, masks, online softmax in fp32 (exp2 with log2(e) folded into
-//            the scale), writes P as bf16 back over S, rescales O in TMEM when
-//            the row max grows by more than 2^8, and writes the output row.
+// Warp roles (384 threads; the control warpgroup gives registers to the two
+// softmax warpgroups with setmaxnreg):
+//   warp 0    TMA producer for Q and K (one thread)
+//   warp 1    TMEM allocator and tcgen05.mma issuer (one thread)
+//   warp 2    TMA producer for V (one thread)
+//   warp 3    idle
+//   warps 4-7 softmax of query tile A, warps 8-11 of query tile B: thread r owns
+//            query row r of its tile (TMEM lane r): reads S from TMEM, masks,
+//            runs the online softmax in fp32 (exp2 with log2(e) folded into the
+//            scale), writes P as f16 back over S, rescales O in TMEM when the
+//            row max grows by more than 2^8, and writes the output row.
 //
-// TMEM (512 columns): S/P double buffer at columns [0,128) and [128,256), the
-// output accumulator O at [256,384).  S = Q K^T reads Q and K from 128B-swizzled
-// shared memory (K-major); O += P V reads P from TMEM and V from shared memory
-// (MN-major).  Every mbarrier wait is bounded (see sm103_ptx.cuh); a timeout
-// sets the status word and the CTA drains its copies and MMAs and exits.
+// TMEM (512 columns): S/P of tile A at [0,128), of tile B at [128,256); the
+// output accumulators O_A at [256,384) and O_B at [384,512).  S = Q K^T reads Q
+// and K from 128B-swizzled shared memory (K-major); O += P V reads P from TMEM
+// and V from shared memory (MN-major).  The MMA issue order per item i is
+// PV_A(i-1), S_A(i), PV_B(i-1), S_B(i): since tcgen05 operations of one thread
+// complete in order, the completion of S_t(i) also certifies that PV_t(i-1) is
+// done, so the softmax may rescale O_t without another wait, while the tensor
+// core works on the other tile.  Every mbarrier wait is bounded (see
+// sm103_ptx.cuh); a timeout sets the status word and the CTA drains its copies
+// and MMAs and exits.
 #include "msa_internal.h"
 #include "sm103_ptx.cuh"
 
 namespace msa {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr int kStagesK = 3;
 constexpr int kStagesV = 2;
-constexpr int kTileBytes = 128 * 128 * 2;  // one 128 x 128 bf16 tile (two 64-column halves)
+constexpr int kTileBytes = 128 * 128 * 2;  // one 128 x 128 16-bit tile (two 64-column halves)
 constexpr int kHalfBytes = kTileBytes / 2;
-constexpr int kMaxDistWords = 1040;         // tile-distance bitset capacity (N up to 2M)
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O when the max grows by > 2^8
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+// TMEM columns: S/P of tile t at kColS + 128 t, O of tile t at kColO + 128 t
+constexpr uint32_t kColS = 0, kColO = 256;
+// Register split: the control warpgroup drops to kCtrlRegs, the two softmax
+// warpgroups rise to kSoftRegs.  128 * 64 + 256 * 208 = 61440 registers, within
+// the 384 * 160 = 61440 the launch is checked to provide.
+constexpr int kCtrlRegs = 56;
+constexpr int kSoftRegs = 208;
+constexpr int kMinLaunchRegs = 160;
 
 struct __align__(1024) Smem {
-  uint8_t q[kTileBytes];
+  uint8_t q[2][kTileBytes];
   uint8_t k[kStagesK][kTileBytes];
   uint8_t v[kStagesV][kTileBytes];
   uint64_t q_full;
   uint64_t k_full[kStagesK], k_empty[kStagesK];
   uint64_t v_full[kStagesV], v_empty[kStagesV];
-  uint64_t s_full[2], p_full[2];
-  uint64_t o_bar, final_bar;
+  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t final_bar;
   uint32_t tmem_base;
   int abort;
-  uint32_t dist[kMaxDistWords];
 };
 
 struct Item {
-  bool cols;      // column chunk (true) or key tile (false)
-  int idx;        // key tile q or chunk c
-  uint32_t qmask; // quadrant mask of a key tile
+  bool cols;          // column chunk (true) or key tile (false)
+  int idx;            // key tile q or chunk c
+  uint32_t qmask[2];  // quadrant masks of a key tile for query tiles A and B
 };
+
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftRegs));
+}
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
+}
 
 __device__ __forceinline__ int unit_batch(const PrefillParams& P, int unit) {
   return unit / P.units.n_heads;
@@ -71,52 +95,73 @@ __device__ __forceinline__ int unit_head(const PrefillParams& P, int unit) {
   return P.units.heads[unit % P.units.n_heads];
 }
 
-// Number of active 128-tile distances <= p (qdelta is ascending).
-__device__ __forceinline__ int vs_tiles_upto(const PrefillParams& P, int unit, int p) {
-  const int32_t* qd = P.qdelta + static_cast<int64_t>(unit) * P.g.NQ;
+__device__ __forceinline__ bool dist_bit(const uint32_t* dist, int t) {
+  return t >= 0 && ((dist[t >> 5] >> (t & 31)) & 1u);
+}
+
+// Number of union distances <= pB (the pair list is ascending).
+__device__ __forceinline__ int vs_tiles_upto(const PrefillParams& P, int unit, int pB) {
+  const int32_t* qd = P.qdelta + static_cast<int64_t>(unit) * (P.g.NQ + 1);
   int lo = 0, hi = P.qdelta_count[unit];
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
-    if (qd[mid] <= p) lo = mid + 1; else hi = mid;
+    if (qd[mid] <= pB) lo = mid + 1; else hi = mid;
   }
   return lo;
 }
 
-__device__ __forceinline__ const uint32_t* vs_chunk_words(const PrefillParams& P, int unit, int p) {
-  return P.col_chunks + (static_cast<int64_t>(unit) * P.g.NQ + p) * P.chunk_words;
+// Column-chunk word x of the pair: chunks needed by query tile pA or pB.
+__device__ __forceinline__ uint32_t vs_chunk_word(const PrefillParams& P, int unit, int pA, int x) {
+  const uint32_t* w = P.col_chunks + (static_cast<int64_t>(unit) * P.g.NQ + pA) * P.chunk_words;
+  uint32_t word = w[x];
+  if (pA + 1 < P.g.NQ) word |= w[P.chunk_words + x];
+  return word;
 }
 
-__device__ __forceinline__ int vs_n_chunks(const PrefillParams& P, int unit, int p) {
-  const uint32_t* w = vs_chunk_words(P, unit, p);
+__device__ __forceinline__ int vs_n_chunks(const PrefillParams& P, int unit, int pA) {
   int n = 0;
-  for (int i = 0; i < P.chunk_words; ++i) n += __popc(w[i]);
+  for (int x = 0; x < P.chunk_words; ++x) n += __popc(vs_chunk_word(P, unit, pA, x));
   return n;
 }
 
-// Streaming: key tiles [0, sink_hi) and [loc_lo, p] (merged when they overlap).
-__device__ __forceinline__ void st_ranges(const PrefillParams& P, int p, int& sink_hi, int& loc_lo) {
-  sink_hi = min((P.init_num + 1) >> 1, p + 1);
-  loc_lo = max(0, 2 * p - P.local_num + 1) >> 1;
+// Last key tile a pair may touch: pB, or NQ - 1 when pB is past the sequence
+// (an odd number of query tiles leaves the last pair with one real tile).
+__device__ __forceinline__ int pair_qmax(const PrefillParams& P, int pA) {
+  return min(pA + 1, P.g.NQ - 1);
+}
+
+// Streaming: key tiles [0, sink_hi) and [loc_lo, qmax] (merged when they overlap).
+__device__ __forceinline__ void st_ranges(const PrefillParams& P, int pA, int& sink_hi, int& loc_lo) {
+  sink_hi = min((P.init_num + 1) >> 1, pair_qmax(P, pA) + 1);
+  loc_lo = max(0, 2 * pA - P.local_num + 1) >> 1;
   if (sink_hi >= loc_lo) {
     sink_hi = 0;
     loc_lo = 0;
   }
 }
 
-__device__ __forceinline__ int n_items(const PrefillParams& P, int unit, int p) {
-  if (P.kind == kPrefillVS) return vs_n_chunks(P, unit, p) + vs_tiles_upto(P, unit, p);
-  if (P.kind == kPrefillBS) return P.bs_tile_count[static_cast<int64_t>(unit) * P.g.NQ + p];
-  int sink_hi, loc_lo;
-  st_ranges(P, p, sink_hi, loc_lo);
-  return sink_hi + (p - loc_lo + 1);
+// Key tiles of a vertical-slash pair: n_hi distances <= pB in the ascending
+// list; the smallest (distance 0, key tile pB) is dropped when pB is past the
+// sequence.  Item t maps to distance list[n_hi - 1 - t].
+__device__ __forceinline__ int vs_n_tiles(const PrefillParams& P, int unit, int pA, int n_hi) {
+  const int32_t* qd = P.qdelta + static_cast<int64_t>(unit) * (P.g.NQ + 1);
+  const bool drop = pA + 1 > P.g.NQ - 1 && n_hi > 0 && qd[0] == 0;
+  return n_hi - (drop ? 1 : 0);
 }
 
-__device__ __forceinline__ bool dist_bit(const uint32_t* dist, int t) {
-  return t >= 0 && ((dist[t >> 5] >> (t & 31)) & 1u);
+__device__ __forceinline__ int n_items(const PrefillParams& P, int unit, int c, int n_chunks,
+                                       int n_tiles) {
+  const int pA = 2 * c;
+  if (P.kind == kPrefillVS) return n_chunks + n_tiles;
+  if (P.kind == kPrefillBS) return P.bs_tile_count[static_cast<int64_t>(unit) * P.npair + c];
+  int sink_hi, loc_lo;
+  st_ranges(P, pA, sink_hi, loc_lo);
+  return sink_hi + (pair_qmax(P, pA) - loc_lo + 1);
 }
 
 // Quadrant mask of key tile q for query tile p (bit a*2 + b).
-__device__ __forceinline__ uint32_t quad_mask_vs(const PrefillParams& P, const uint32_t* dist, int p, int q) {
+__device__ __forceinline__ uint32_t quad_mask_vs(const PrefillParams& P, const uint32_t* dist,
+                                                 int p, int q) {
   uint32_t mask = 0;
 #pragma unroll
   for (int a = 0; a < 2; ++a) {
@@ -142,46 +187,51 @@ __device__ __forceinline__ uint32_t quad_mask_st(const PrefillParams& P, int p, 
   return mask;
 }
 
-// Item i of query tile p.  Vertical-slash: column chunks first (ascending),
-// then key tiles ascending (largest distance first).  `dist` may be null when
-// the caller does not need the quadrant mask.
-__device__ __forceinline__ Item get_item(const PrefillParams& P, int unit, int p, int i,
-                                         const uint32_t* dist, int n_chunks, int n_tiles) {
+// Item i of pair c.  Vertical-slash: column chunks first (ascending), then key
+// tiles ascending (largest distance first; n_hi from vs_tiles_upto).  `dist`
+// may be null when the caller does not need the quadrant masks.
+__device__ __forceinline__ Item get_item(const PrefillParams& P, int unit, int c, int i,
+                                         const uint32_t* dist, int n_chunks, int n_hi) {
+  const int pA = 2 * c, pB = pA + 1;
   Item it;
   it.cols = false;
-  it.qmask = 0xFu;
+  it.qmask[0] = it.qmask[1] = 0xFu;
   if (P.kind == kPrefillVS) {
     if (i < n_chunks) {
-      const uint32_t* w = vs_chunk_words(P, unit, p);
       int seen = 0;
       for (int x = 0;; ++x) {
-        const int c = __popc(w[x]);
-        if (seen + c > i) {
-          uint32_t word = w[x];
+        uint32_t word = vs_chunk_word(P, unit, pA, x);
+        const int cnt = __popc(word);
+        if (seen + cnt > i) {
           for (int skip = i - seen; skip > 0; --skip) word &= word - 1;
           it.cols = true;
           it.idx = 32 * x + (__ffs(word) - 1);
           return it;
         }
-        seen += c;
+        seen += cnt;
       }
     }
     const int t = i - n_chunks;
-    const int32_t* qd = P.qdelta + static_cast<int64_t>(unit) * P.g.NQ;
-    it.idx = p - qd[n_tiles - 1 - t];
-    if (dist) it.qmask = quad_mask_vs(P, dist, p, it.idx);
+    const int32_t e = P.qdelta[static_cast<int64_t>(unit) * (P.g.NQ + 1) + n_hi - 1 - t];
+    it.idx = pB - e;
+    if (dist) {
+      it.qmask[0] = quad_mask_vs(P, dist, pA, it.idx);
+      it.qmask[1] = quad_mask_vs(P, dist, pB, it.idx);
+    }
     return it;
   }
   if (P.kind == kPrefillBS) {
-    const int32_t e = P.bs_tiles[(static_cast<int64_t>(unit) * P.g.NQ + p) * P.bs_tile_cap + i];
-    it.idx = e >> 4;
-    it.qmask = static_cast<uint32_t>(e & 15);
-    return it;
+    const int32_t e = P.bs_tiles[(static_cast<int64_t>(unit) * P.npair + c) * P.bs_tile_cap + i];
+    it.idx = e >> 8;
+    it.qmask[0] = static_cast<uint32_t>(e & 15);
+    it.qmask[1] = static_cast<uint32_t>((e >> 4) & 15);
+  } else {
+    int sink_hi, loc_lo;
+    st_ranges(P, pA, sink_hi, loc_lo);
+    it.idx = i < sink_hi ? i : loc_lo + (i - sink_hi);
+    it.qmask[0] = quad_mask_st(P, pA, it.idx);
+    it.qmask[1] = quad_mask_st(P, pB, it.idx);
   }
-  int sink_hi, loc_lo;
-  st_ranges(P, p, sink_hi, loc_lo);
-  it.idx = i < sink_hi ? i : loc_lo + (i - sink_hi);
-  it.qmask = quad_mask_st(P, p, it.idx);
   return it;
 }
 
@@ -200,9 +250,13 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
                                       ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int unit = blockIdx.y;
-  const int p = P.g.NQ - 1 - static_cast<int>(blockIdx.x);  // heavy (late) tiles first
+  const int c = P.npair - 1 - static_cast<int>(blockIdx.x);  // heavy (late) pairs first
+  const int pA = 2 * c;
   const int b = unit_batch(P, unit), h = unit_head(P, unit), hkv = h / P.g.G;
   volatile int* abort = &sm.abort;
+  const uint32_t* dist = P.kind == kPrefillVS
+                             ? P.tile_dist + static_cast<int64_t>(unit) * P.dist_words
+                             : nullptr;
 
   if (tid == 0) {
     mbar_init(&sm.q_full, 1);
@@ -214,11 +268,11 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
       mbar_init(&sm.v_full[s], 1);
       mbar_init(&sm.v_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&sm.s_full[s], 1);
-      mbar_init(&sm.p_full[s], 4);  // one arrival per softmax warp
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&sm.s_full[t], 1);
+      mbar_init(&sm.p_full[t], 4);  // one arrival per softmax warp of the tile
+      mbar_init(&sm.o_full[t], 1);
     }
-    mbar_init(&sm.o_bar, 1);
     mbar_init(&sm.final_bar, 1);
     sm.abort = 0;
     fence_mbar_init();
@@ -227,35 +281,38 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
     tmem_alloc(&sm.tmem_base, 512);
     tmem_relinquish();
   }
-  if (P.kind == kPrefillVS && warp >= 4) {
-    const uint32_t* d = P.tile_dist + static_cast<int64_t>(unit) * P.dist_words;
-    for (int w = tid - 128; w < P.dist_words; w += 128) sm.dist[w] = d[w];
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
-  int n_chunks = 0, n_tiles = 0;
+  int n_chunks = 0, n_hi = 0, n_tiles = 0;
   if (P.kind == kPrefillVS) {
-    n_chunks = vs_n_chunks(P, unit, p);
-    n_tiles = vs_tiles_upto(P, unit, p);
+    n_chunks = vs_n_chunks(P, unit, pA);
+    n_hi = vs_tiles_upto(P, unit, pA + 1);
+    n_tiles = vs_n_tiles(P, unit, pA, n_hi);
   }
-  const int n = n_items(P, unit, p);
+  const int n = n_items(P, unit, c, n_chunks, n_tiles);
 
+  if (warp < 4) {
+  // ============================================================== control warpgroup
+  setmaxnreg_dec();
   if (warp == 0) {
     // ------------------------------------------------------------ Q + K producer
     if (lane == 0) {
       tma_prefetch_desc(&mq);
       tma_prefetch_desc(&mk);
-      mbar_arrive_expect_tx(&sm.q_full, kTileBytes);
-      tma_load_4d(sm.q, &mq, &sm.q_full, 0, 128 * p, h, b);
-      tma_load_4d(sm.q + kHalfBytes, &mq, &sm.q_full, 64, 128 * p, h, b);
+      mbar_arrive_expect_tx(&sm.q_full, 2 * kTileBytes);
+      for (int t = 0; t < 2; ++t) {  // a tile past the sequence reloads the last one (never stored)
+        const int qrow = 128 * min(pA + t, P.g.NQ - 1);
+        tma_load_4d(sm.q[t], &mq, &sm.q_full, 0, qrow, h, b);
+        tma_load_4d(sm.q[t] + kHalfBytes, &mq, &sm.q_full, 64, qrow, h, b);
+      }
       int issued = 0;
       for (int i = 0; i < n; ++i) {
         const int s = i % kStagesK;
         if (!mbar_wait(&sm.k_empty[s], ((i / kStagesK) & 1) ^ 1, abort)) break;
-        const Item it = get_item(P, unit, p, i, nullptr, n_chunks, n_tiles);
+        const Item it = get_item(P, unit, c, i, nullptr, n_chunks, n_hi);
         mbar_arrive_expect_tx(&sm.k_full[s], kTileBytes);
         if (it.cols) {
           const int row = unit * P.kv_pad + 128 * it.idx;
@@ -280,7 +337,7 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
       for (int i = 0; i < n; ++i) {
         const int s = i % kStagesV;
         if (!mbar_wait(&sm.v_empty[s], ((i / kStagesV) & 1) ^ 1, abort)) break;
-        const Item it = get_item(P, unit, p, i, nullptr, n_chunks, n_tiles);
+        const Item it = get_item(P, unit, c, i, nullptr, n_chunks, n_hi);
         mbar_arrive_expect_tx(&sm.v_full[s], kTileBytes);
         if (it.cols) {
           const int row = unit * P.kv_pad + 128 * it.idx;
@@ -300,62 +357,79 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idO = idesc_f32acc(128, 128, /*bf16=*/false, false, true);  // f16 P, f16 V
-      const uint32_t q_addr = smem_u32(sm.q);
       bool ok = n == 0 || mbar_wait(&sm.q_full, 0, abort);
       tc_fence_after();
-      auto issue_pv = [&](int j) -> bool {
-        const int buf = j & 1, sv = j % kStagesV;
-        if (!mbar_wait(&sm.p_full[buf], (j >> 1) & 1, abort)) return false;
-        if (!mbar_wait(&sm.v_full[sv], (j / kStagesV) & 1, abort)) return false;
+      // O_t += P_t(j) V(j); the second tile's product releases the V stage
+      auto issue_pv = [&](int t, int j) -> bool {
+        const int sv = j % kStagesV;
+        if (!mbar_wait(&sm.p_full[t], j & 1, abort)) return false;
+        if (t == 0 && !mbar_wait(&sm.v_full[sv], (j / kStagesV) & 1, abort)) return false;
         tc_fence_after();
         const uint32_t v_addr = smem_u32(sm.v[sv]);
-        const uint32_t p_col = tmem + (buf ? kColS1 : kColS0);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t bd = sdesc_sw128(v_addr + kk * 2048, kHalfBytes, 1024);
-          mma_ts(tmem + kColO, p_col + kk * 8, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + (kColO + 128 * t), tmem + (kColS + 128 * t) + kk * 8, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&sm.v_empty[sv]);
-        mma_commit(&sm.o_bar);
+        if (t == 1) mma_commit(&sm.v_empty[sv]);
         return true;
       };
-      for (int i = 0; ok && i < n; ++i) {
-        const int sk = i % kStagesK, buf = i & 1;
-        if (!mbar_wait(&sm.k_full[sk], (i / kStagesK) & 1, abort)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(sm.k[sk]);
-        const uint32_t s_col = tmem + (buf ? kColS1 : kColS0);
+      auto issue_s = [&](int t, int i) {
+        const uint32_t q_addr = smem_u32(sm.q[t]);
+        const uint32_t k_addr = smem_u32(sm.k[i % kStagesK]);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          mma_ss(s_col, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
-                 idS, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + (kColS + 128 * t), sdesc_sw128(q_addr + off, 16, 1024),
+                 sdesc_sw128(k_addr + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&sm.s_full[buf]);
-        mma_commit(&sm.k_empty[sk]);
-        if (i >= 1 && !issue_pv(i - 1)) { ok = false; break; }
+        mma_commit(&sm.s_full[t]);
+      };
+      for (int i = 0; ok && i < n; ++i) {
+        if (i >= 1 && !issue_pv(0, i - 1)) { ok = false; break; }
+        if (!mbar_wait(&sm.k_full[i % kStagesK], (i / kStagesK) & 1, abort)) { ok = false; break; }
+        tc_fence_after();
+        issue_s(0, i);
+        if (i >= 1 && !issue_pv(1, i - 1)) { ok = false; break; }
+        issue_s(1, i);
+        mma_commit(&sm.k_empty[i % kStagesK]);
       }
-      if (ok && n > 0) issue_pv(n - 1);
+      if (ok && n > 0) {
+        if (issue_pv(0, n - 1)) {
+          mma_commit(&sm.o_full[0]);
+          if (issue_pv(1, n - 1)) mma_commit(&sm.o_full[1]);
+        }
+      }
       // every MMA issued above must complete before TMEM is released
       mma_commit(&sm.final_bar);
       wait_drain(&sm.final_bar, 0);
     }
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax
-    const int r = tid - 128;                 // query row within the tile == TMEM lane
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+  if (tid == 0 && sm.abort && P.status) atomicOr(P.status, kStatusTimeout);
+  } else {
+  // ============================================================== softmax warpgroups
+  setmaxnreg_inc();
+  {
+    const int t = (warp - 4) >> 2;           // query tile of this warpgroup
+    const int p = pA + t;
+    const int r = (tid - 128) & 127;         // query row within the tile == TMEM lane
     const int half = r >> 6;                 // row block 2p + half
     const int row = 128 * p + r;             // query index i
     const int mblk = 2 * p + half;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    named_bar_sync(1, 128);                  // dist bitset copy complete
+    const uint32_t s_col = lane_base + (kColS + 128 * t);
+    const uint32_t o_col = lane_base + (kColO + 128 * t);
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
+    int k = 0;  // items processed so far
     for (int i = 0; i < n; ++i) {
-      const Item it = get_item(P, unit, p, i, sm.dist, n_chunks, n_tiles);
-      const int buf = i & 1;
-      const uint32_t s_col = lane_base + (buf ? kColS1 : kColS0);
+      const Item it = get_item(P, unit, c, i, dist, n_chunks, n_hi);
       // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[buf], (i >> 1) & 1, abort))) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[t], k & 1, abort))) { ok = false; break; }
       tc_fence_after();
       // raw logits (unscaled) of this row; scale * log2(e) is folded in below
       float x[128];
@@ -374,13 +448,14 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
           bool keep = false;
           if (e < valid) {
             const int j = V[e];
-            keep = j <= row && !dist_bit(sm.dist, mblk - (j >> 6));
+            keep = j <= row && !dist_bit(dist, mblk - (j >> 6));
           }
           if (!keep) x[e] = -INFINITY;
         }
       } else {
-        const bool lo_ok = (it.qmask >> (half * 2)) & 1u;
-        const bool hi_ok = (it.qmask >> (half * 2 + 1)) & 1u;
+        const uint32_t qm = t ? it.qmask[1] : it.qmask[0];
+        const bool lo_ok = (qm >> (half * 2)) & 1u;
+        const bool hi_ok = (qm >> (half * 2 + 1)) & 1u;
         const bool diag = it.idx == p;
         if (!lo_ok || !hi_ok || diag) {
 #pragma unroll
@@ -390,7 +465,7 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
           }
         }
       }
-      // ---- online softmax (8 independent partial maxima / sums per row)
+      // ---- online softmax (8 independent chains of 3-input max, paired sums)
       float mx8[8];
 #pragma unroll
       for (int a = 0; a < 8; ++a) {
@@ -419,24 +494,19 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
       }
       const float2 rsa = fadd2(fadd2(rs2[0], rs2[1]), fadd2(rs2[2], rs2[3]));
       const float rs = rsa.x + rsa.y;
-      const bool correct = grow && m_run != -INFINITY;  // O holds earlier rows' weight
+      const bool correct = grow && m_run != -INFINITY;  // O holds earlier items' weight
       const float alpha = correct ? ex2_approx(m_run - m_new) : 1.f;
       l_run = (m_run == -INFINITY ? 0.f : l_run * alpha) + rs;
       m_run = m_use;
-      // PV of the previous item must be complete before O is touched
-      if (i >= 1 && !__all_sync(0xffffffffu, mbar_wait(&sm.o_bar, (i - 1) & 1, abort))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
+      // PV_t(i-1) completed before S_t(i) did (in-order tcgen05), so O_t is ready
       if (__any_sync(0xffffffffu, correct)) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int q4 = 0; q4 < 4; ++q4) {
           uint32_t o[32];
-          tmem_ld32(lane_base + kColO + 32 * c, o);
+          tmem_ld32(o_col + 32 * q4, o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(lane_base + kColO + 32 * c, o);
+          tmem_st32(o_col + 32 * q4, o);
         }
       }
       {
@@ -452,20 +522,20 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.p_full[buf]);
+      if (lane == 0) mbar_arrive(&sm.p_full[t]);
+      ++k;
     }
     // ---- epilogue
     uint4 outv[16];
-    bool have = ok && n > 0 && l_run > 0.f;
-    if (ok && n > 0) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_bar, (n - 1) & 1, abort))) ok = false;
+    const bool have = ok && k > 0 && l_run > 0.f;
+    if (ok && k > 0) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full[t], 0, abort))) ok = false;
       tc_fence_after();
     }
-    const bool warp_ok = ok;
-    if (warp_ok && n > 0) {
+    if (ok && k > 0) {
       const float inv = have ? 1.f / l_run : 0.f;
       uint32_t o[128];
-      tmem_ld128(lane_base + kColO, o);
+      tmem_ld128(o_col, o);
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         uint4 w;
@@ -487,12 +557,9 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
     }
   }
   tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 512);
-  if (tid == 0 && sm.abort && P.status) atomicOr(P.status, kStatusTimeout);
+  __syncthreads();  // pairs with the control warpgroup's; TMEM is released after it
+  }
 }
-
 
 // v (bf16, any strides, [B][Hkv][N][128]) -> dst (f16, contiguous, same shape).
 // The P.V product runs in f16 (P rounded to f16 keeps 3 more mantissa bits than
@@ -507,11 +574,11 @@ __global__ void v_to_f16_kernel(const __nv_bfloat16* __restrict__ v, int64_t sb,
   for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n16;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t row = idx >> 4;
-    const int c = static_cast<int>(idx & 15);
+    const int cc = static_cast<int>(idx & 15);
     const int64_t bh = row / N;
     const int n = static_cast<int>(row % N);
     const int b = static_cast<int>(bh / Hkv), h = static_cast<int>(bh % Hkv);
-    const uint4 raw = *reinterpret_cast<const uint4*>(v + b * sb + h * sh + n * sn + c * 8);
+    const uint4 raw = *reinterpret_cast<const uint4*>(v + b * sb + h * sh + n * sn + cc * 8);
     const __nv_bfloat162* in = reinterpret_cast<const __nv_bfloat162*>(&raw);
     uint4 o;
     uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
@@ -521,7 +588,7 @@ __global__ void v_to_f16_kernel(const __nv_bfloat16* __restrict__ v, int64_t sb,
       bad |= fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
       ow[e] = pack_f16x2(lo, hi);
     }
-    *reinterpret_cast<uint4*>(dst + row * kHeadDim + c * 8) = o;
+    *reinterpret_cast<uint4*>(dst + row * kHeadDim + cc * 8) = o;
   }
   if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0 && status)
     atomicOr(status, kStatusRange);
@@ -544,12 +611,22 @@ cudaError_t launch_v_to_f16(TensorView v, int B, int Hkv, int N, __half* dst, ui
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                            const CUtensorMap& mv, const CUtensorMap& mkc, const CUtensorMap& mvc,
                            cudaStream_t st, int* n_launch) {
+  // The register split above needs the launch to provide kMinLaunchRegs per
+  // thread; refuse to launch (rather than wait forever) if the build differs.
+  static int launch_regs = -1;
+  if (launch_regs < 0) {
+    cudaFuncAttributes attr;
+    cudaError_t e = cudaFuncGetAttributes(&attr, sparse_prefill_kernel);
+    if (e != cudaSuccess) return e;
+    launch_regs = attr.numRegs;
+  }
+  if (launch_regs < kMinLaunchRegs) return cudaErrorInvalidConfiguration;
   const int smem = static_cast<int>(sizeof(Smem)) + 1024;
   cudaError_t e = cudaFuncSetAttribute(sparse_prefill_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  if (p.g.n_units == 0 || p.g.NQ == 0) return cudaSuccess;
-  sparse_prefill_kernel<<<dim3(p.g.NQ, p.g.n_units), kThreads, smem, st>>>(p, mq, mk, mv, mkc, mvc);
+  if (p.g.n_units == 0 || p.npair == 0) return cudaSuccess;
+  sparse_prefill_kernel<<<dim3(p.npair, p.g.n_units), kThreads, smem, st>>>(p, mq, mk, mv, mkc, mvc);
   e = cudaGetLastError();
   if (e == cudaSuccess) ++*n_launch;
   return e;

@@ -9,9 +9,11 @@
 //    through rows [64m, 64m+63] lands on keys [64(m-a) - b, 64(m-a) + 63 - b],
 //    which meets tiles m-a and m-a-1 (only m-a when b == 0).  The set is the
 //    same for every row block.
-//  * qdelta: ascending distances D between 128-row query tiles and 128-key
-//    tiles that hold at least one active 64x64 quadrant (quadrant distances
-//    2D-1, 2D, 2D+1).
+//  * qdelta: for the attention CTAs, which each serve two adjacent 128-row
+//    query tiles pA and pB = pA + 1, the ascending distances D = pB - q to the
+//    128-key tiles q that hold an active 64x64 quadrant for either query tile.
+//    A 128x128 tile at query-tile distance E holds quadrant distances 2E-1, 2E
+//    and 2E+1; query tile pB sees key tile q at E = D and pA at E = D - 1.
 //  * col_chunks: per 128-row query tile p, bit c is set iff some chosen key in
 //    positions [128c, 128c+128) of the ascending vertical list is needed as a
 //    column by row block 2p or 2p+1, i.e. lies at or before the block's last
@@ -44,13 +46,13 @@ __global__ void __launch_bounds__(kTilesThreads) vs_tile_dist_kernel(
   __syncthreads();
   uint32_t* dst = tile_dist + static_cast<int64_t>(unit) * dist_words;
   for (int w = tid; w < dist_words; w += kTilesThreads) dst[w] = bits[w];
-  auto bit = [&](int t) -> bool { return (bits[t >> 5] >> (t & 31)) & 1u; };
-  int32_t* qd = qdelta + static_cast<int64_t>(unit) * NQ;
+  auto bit = [&](int t) -> bool { return t >= 0 && t <= NB && ((bits[t >> 5] >> (t & 31)) & 1u); };
+  auto tile_active = [&](int e) -> bool { return e >= 0 && (bit(2 * e) || bit(2 * e + 1) || bit(2 * e - 1)); };
+  int32_t* qd = qdelta + static_cast<int64_t>(unit) * (NQ + 1);
   int written = 0;
-  for (int base = 0; base < NQ; base += kTilesThreads) {
+  for (int base = 0; base <= NQ; base += kTilesThreads) {
     const int d = base + tid;
-    bool act = false;
-    if (d < NQ) act = bit(2 * d) || bit(2 * d + 1) || (d > 0 && bit(2 * d - 1));
+    const bool act = d <= NQ && (tile_active(d) || tile_active(d - 1));
     int total;
     const int pos = block_exclusive_scan<kTilesThreads>(act ? 1 : 0, warp_sums, &total);
     if (act) qd[written + pos] = d;
