@@ -101,11 +101,11 @@ __device__ __forceinline__ bool dist_bit(const uint32_t* dist, int t) {
 
 // Number of union distances <= pB (the pair list is ascending).
 __device__ __forceinline__ int vs_tiles_upto(const PrefillParams& P, int unit, int pB) {
-  const int32_t* qd = P.qdelta + static_cast<int64_t>(unit) * (P.g.NQ + 1);
+  const int32_t* qd = P.qdelta + static_cast<int64_t>(unit) * (P.g.NQ + 1);  // (D << 5) | bits
   int lo = 0, hi = P.qdelta_count[unit];
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
-    if (qd[mid] <= pB) lo = mid + 1; else hi = mid;
+    if ((qd[mid] >> 5) <= pB) lo = mid + 1; else hi = mid;
   }
   return lo;
 }
@@ -145,7 +145,7 @@ __device__ __forceinline__ void st_ranges(const PrefillParams& P, int pA, int& s
 // sequence.  Item t maps to distance list[n_hi - 1 - t].
 __device__ __forceinline__ int vs_n_tiles(const PrefillParams& P, int unit, int pA, int n_hi) {
   const int32_t* qd = P.qdelta + static_cast<int64_t>(unit) * (P.g.NQ + 1);
-  const bool drop = pA + 1 > P.g.NQ - 1 && n_hi > 0 && qd[0] == 0;
+  const bool drop = pA + 1 > P.g.NQ - 1 && n_hi > 0 && (qd[0] >> 5) == 0;
   return n_hi - (drop ? 1 : 0);
 }
 
@@ -159,20 +159,7 @@ __device__ __forceinline__ int n_items(const PrefillParams& P, int unit, int c, 
   return sink_hi + (pair_qmax(P, pA) - loc_lo + 1);
 }
 
-// Quadrant mask of key tile q for query tile p (bit a*2 + b).
-__device__ __forceinline__ uint32_t quad_mask_vs(const PrefillParams& P, const uint32_t* dist,
-                                                 int p, int q) {
-  uint32_t mask = 0;
-#pragma unroll
-  for (int a = 0; a < 2; ++a) {
-#pragma unroll
-    for (int b = 0; b < 2; ++b) {
-      const int m = 2 * p + a, n = 2 * q + b;
-      if (m < P.g.NB && n <= m && dist_bit(dist, m - n)) mask |= 1u << (a * 2 + b);
-    }
-  }
-  return mask;
-}
+// Quadrant mask of key tile q for query tile p (bit a*2 + b), streaming head.
 __device__ __forceinline__ uint32_t quad_mask_st(const PrefillParams& P, int p, int q) {
   uint32_t mask = 0;
 #pragma unroll
@@ -188,10 +175,9 @@ __device__ __forceinline__ uint32_t quad_mask_st(const PrefillParams& P, int p, 
 }
 
 // Item i of pair c.  Vertical-slash: column chunks first (ascending), then key
-// tiles ascending (largest distance first; n_hi from vs_tiles_upto).  `dist`
-// may be null when the caller does not need the quadrant masks.
+// tiles ascending (largest distance first; n_hi from vs_tiles_upto).
 __device__ __forceinline__ Item get_item(const PrefillParams& P, int unit, int c, int i,
-                                         const uint32_t* dist, int n_chunks, int n_hi) {
+                                         int n_chunks, int n_hi) {
   const int pA = 2 * c, pB = pA + 1;
   Item it;
   it.cols = false;
@@ -213,11 +199,20 @@ __device__ __forceinline__ Item get_item(const PrefillParams& P, int unit, int c
     }
     const int t = i - n_chunks;
     const int32_t e = P.qdelta[static_cast<int64_t>(unit) * (P.g.NQ + 1) + n_hi - 1 - t];
-    it.idx = pB - e;
-    if (dist) {
-      it.qmask[0] = quad_mask_vs(P, dist, pA, it.idx);
-      it.qmask[1] = quad_mask_vs(P, dist, pB, it.idx);
+    it.idx = pB - (e >> 5);
+    // quadrant (a, b) of tile pB sits at distance 2D + a - b (bit a - b + 3 of
+    // the packed window), of tile pA at 2D - 2 + a - b (bit a - b + 1)
+    uint32_t ma = 0, mb = 0;
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        if (2 * pA + a < P.g.NB) ma |= ((e >> (a - b + 1)) & 1u) << (a * 2 + b);
+        if (2 * pB + a < P.g.NB) mb |= ((e >> (a - b + 3)) & 1u) << (a * 2 + b);
+      }
     }
+    it.qmask[0] = ma;
+    it.qmask[1] = mb;
     return it;
   }
   if (P.kind == kPrefillBS) {
@@ -312,7 +307,7 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
       for (int i = 0; i < n; ++i) {
         const int s = i % kStagesK;
         if (!mbar_wait(&sm.k_empty[s], ((i / kStagesK) & 1) ^ 1, abort)) break;
-        const Item it = get_item(P, unit, c, i, nullptr, n_chunks, n_hi);
+        const Item it = get_item(P, unit, c, i, n_chunks, n_hi);
         mbar_arrive_expect_tx(&sm.k_full[s], kTileBytes);
         if (it.cols) {
           const int row = unit * P.kv_pad + 128 * it.idx;
@@ -337,7 +332,7 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
       for (int i = 0; i < n; ++i) {
         const int s = i % kStagesV;
         if (!mbar_wait(&sm.v_empty[s], ((i / kStagesV) & 1) ^ 1, abort)) break;
-        const Item it = get_item(P, unit, c, i, nullptr, n_chunks, n_hi);
+        const Item it = get_item(P, unit, c, i, n_chunks, n_hi);
         mbar_arrive_expect_tx(&sm.v_full[s], kTileBytes);
         if (it.cols) {
           const int row = unit * P.kv_pad + 128 * it.idx;
@@ -427,7 +422,7 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
     bool ok = true;
     int k = 0;  // items processed so far
     for (int i = 0; i < n; ++i) {
-      const Item it = get_item(P, unit, c, i, dist, n_chunks, n_hi);
+      const Item it = get_item(P, unit, c, i, n_chunks, n_hi);
       // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[t], k & 1, abort))) { ok = false; break; }
       tc_fence_after();

@@ -14,6 +14,8 @@
 //    128-key tiles q that hold an active 64x64 quadrant for either query tile.
 //    A 128x128 tile at query-tile distance E holds quadrant distances 2E-1, 2E
 //    and 2E+1; query tile pB sees key tile q at E = D and pA at E = D - 1.
+//    Entries are (D << 5) | bits 2D-3 .. 2D+1 of tile_dist, the bits that the
+//    quadrant masks of both query tiles read.
 //  * col_chunks: per 128-row query tile p, bit c is set iff some chosen key in
 //    positions [128c, 128c+128) of the ascending vertical list is needed as a
 //    column by row block 2p or 2p+1, i.e. lies at or before the block's last
@@ -55,7 +57,9 @@ __global__ void __launch_bounds__(kTilesThreads) vs_tile_dist_kernel(
     const bool act = d <= NQ && (tile_active(d) || tile_active(d - 1));
     int total;
     const int pos = block_exclusive_scan<kTilesThreads>(act ? 1 : 0, warp_sums, &total);
-    if (act) qd[written + pos] = d;
+    uint32_t near = 0;  // tile-distance bits 2d-3 .. 2d+1: all the quadrant masks need
+    for (int k = 0; k < 5; ++k) near |= (bit(2 * d - 3 + k) ? 1u : 0u) << k;
+    if (act) qd[written + pos] = (d << 5) | static_cast<int>(near);
     written += total;
   }
   if (tid == 0) qdelta_count[unit] = written;
