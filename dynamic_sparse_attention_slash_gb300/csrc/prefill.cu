@@ -58,7 +58,7 @@ constexpr uint32_t kColS = 0, kColO = 256;
 // Register split: the control warpgroup drops to kCtrlRegs, the two softmax
 // warpgroups rise to kSoftRegs.  128 * 64 + 256 * 208 = 61440 registers, within
 // the 384 * 160 = 61440 the launch is checked to provide.
-constexpr int kCtrlRegs = 56;
+constexpr int kCtrlRegs = 64;
 constexpr int kSoftRegs = 208;
 constexpr int kMinLaunchRegs = 160;
 
@@ -354,35 +354,45 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
       constexpr uint32_t idO = idesc_f32acc(128, 128, /*bf16=*/false, false, true);  // f16 P, f16 V
       bool ok = n == 0 || mbar_wait(&sm.q_full, 0, abort);
       tc_fence_after();
+      // Operand descriptors are built once; a K-step only adds a constant to the
+      // start-address field (16-byte units), which cannot carry out of it.
+      const uint64_t q_desc0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
+      const uint64_t q_desc1 = sdesc_sw128(smem_u32(sm.q[1]), 16, 1024);
+      const uint64_t k_desc0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
+      const uint64_t v_desc0 = sdesc_sw128(smem_u32(sm.v[0]), kHalfBytes, 1024);
+      constexpr uint64_t kStageStep = kTileBytes >> 4;
       // O_t += P_t(j) V(j); the second tile's product releases the V stage
       auto issue_pv = [&](int t, int j) -> bool {
         const int sv = j % kStagesV;
         if (!mbar_wait(&sm.p_full[t], j & 1, abort)) return false;
         if (t == 0 && !mbar_wait(&sm.v_full[sv], (j / kStagesV) & 1, abort)) return false;
         tc_fence_after();
-        const uint32_t v_addr = smem_u32(sm.v[sv]);
+        const uint64_t vd = v_desc0 + sv * kStageStep;
+        const uint32_t o_tm = tmem + kColO + 128 * t, p_tm = tmem + kColS + 128 * t;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bd = sdesc_sw128(v_addr + kk * 2048, kHalfBytes, 1024);
-          mma_ts(tmem + (kColO + 128 * t), tmem + (kColS + 128 * t) + kk * 8, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(o_tm, p_tm + kk * 8, vd + ((kk * 2048) >> 4), idO, (j > 0 || kk > 0) ? 1u : 0u);
         if (t == 1) mma_commit(&sm.v_empty[sv]);
         return true;
       };
+      // S_t(i) = Q_t K(i)^T
       auto issue_s = [&](int t, int i) {
-        const uint32_t q_addr = smem_u32(sm.q[t]);
-        const uint32_t k_addr = smem_u32(sm.k[i % kStagesK]);
+        const uint64_t qd = t ? q_desc1 : q_desc0;
+        const uint64_t kd = k_desc0 + (i % kStagesK) * kStageStep;
+        const uint32_t s_tm = tmem + kColS + 128 * t;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          mma_ss(tmem + (kColS + 128 * t), sdesc_sw128(q_addr + off, 16, 1024),
-                 sdesc_sw128(k_addr + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+          mma_ss(s_tm, qd + off, kd + off, idS, kk > 0 ? 1u : 0u);
         }
         mma_commit(&sm.s_full[t]);
       };
       for (int i = 0; ok && i < n; ++i) {
-        if (i >= 1 && !issue_pv(0, i - 1)) { ok = false; break; }
+        // K(i) is normally resident long before; waiting for it next to P_A's
+        // wait keeps a wait out of the middle of the MMA stream (a wait there
+        // stalls behind the queued P.V MMAs and lets the tensor pipe drain)
         if (!mbar_wait(&sm.k_full[i % kStagesK], (i / kStagesK) & 1, abort)) { ok = false; break; }
+        if (i >= 1 && !issue_pv(0, i - 1)) { ok = false; break; }
         tc_fence_after();
         issue_s(0, i);
         if (i >= 1 && !issue_pv(1, i - 1)) { ok = false; break; }
