@@ -37,3 +37,14 @@ def test_bs_and_st_pairs():
     assert bench.bs_pairs([len(s) for s in sel]) == O.nnz_from_blocks(sel, N)
     st = [O.streaming_blocks(m, 2, 3) for m in range(N // 64)]
     assert bench.st_pairs(N, 2, 3) == O.nnz_from_blocks(st, N)
+
+
+def test_measured_traffic_is_tied_to_kernel_source(monkeypatch):
+    """The bench reports the captured DRAM traffic only for the workload and the
+    kernel source it was measured on; anything else gives null."""
+    import bench
+    assert bench.measured_traffic("vs_32k", "vs") is None
+    assert bench.measured_traffic("mixed_128k", "bs") is None
+    stale = dict(bench.MEASURED_TRAFFIC, sha256="0" * 64)
+    monkeypatch.setattr(bench, "MEASURED_TRAFFIC", stale)
+    assert bench.measured_traffic("mixed_128k", "vs") is None
