@@ -24,7 +24,8 @@ from bf16 inputs converted exactly.  Sources, by page title and section:
 * [KV-1.5x] "How KV sparsity achieves 1.5x acceleration for vLLM" (Novita AI
             blog), section "Key Techniques / 2. Attention modification": the
             token score is a sum of softmax probabilities over a window of the
-            last queries, computed from the row max and the row sum l.
+            last queries, computed from the row max and the row sum l that the
+            attention pass exports; each head keeps its top-scoring tokens.
 
 Readings where the pages are silent or garbled (each one is listed in the
 design notes with its reason):
@@ -43,7 +44,11 @@ design notes with its reason):
 * the block-sparse head keeps the diagonal block plus the top-(topk-1) earlier
   blocks by pooled score; streaming keeps blocks [0, init_num) and the
   ``local_window_num`` blocks ending at the query's own block;
-* query head h reads KV head h // (Hq / Hkv).
+* query head h reads KV head h // (Hq / Hkv);
+* KV selection: the exported normaliser is lse = rowmax + ln(l); a window row's
+  probabilities are those of the attention the call computed (zero outside
+  its key set J_i); the score is per query head; no pooling of the score
+  before its top-k (the page names none).
 
 Parity pins for every function live in tests/test_oracle_*.py.
 """
@@ -381,6 +386,60 @@ def streaming_forward(q, k, v, init_num, local_window_num, heads=None, scale=Non
             out[b, t], recs[(b, h)] = streaming_head(q[b, h], k[b, g], v[b, g], init_num,
                                                      local_window_num, scale)
     return out, recs
+
+
+# ----------------------------------------------------------------------------- KV selection
+def row_lse(q, k, rows, block_mask, scale: float) -> np.ndarray:
+    """Row normaliser of the masked causal attention [KV-1.5x] (the "rowmax / l"
+    pair the attention pass exports, as one number):
+    lse_i = ln sum_{j in J_i} exp(z_ij), z_ij = scale * q_i . k_j, where J_i is
+    the set of keys j <= i that block_mask(i // 64) admits; -inf for an empty J_i.
+    """
+    out = np.full(len(rows), -np.inf)
+    for r, i in enumerate(rows):
+        allow = np.asarray(block_mask(i // BLOCK), dtype=bool)[: i + 1]
+        if not allow.any():
+            continue
+        z = (k[: i + 1][allow] @ q[i]) * scale
+        zmax = z.max()
+        out[r] = zmax + np.log(np.exp(z - zmax).sum())
+    return out
+
+
+def kv_score(q, k, window_lse, block_mask, window: int, scale: float) -> np.ndarray:
+    """Token score for keeping KV entries [KV-1.5x]: for the query rows of the
+    instruction window i in [N - window, N),
+        S_j = sum over window rows i with j in J_i of exp(z_ij - lse_i),
+    i.e. the attention probability of key j in row i under the row normaliser of
+    the attention pass, summed over the window ("kq" order on the page: one sum
+    per key).  window_lse[r] is lse of row N - window + r.
+    """
+    N = q.shape[0]
+    S = np.zeros(N, dtype=np.float64)
+    for r, i in enumerate(range(N - window, N)):
+        if not np.isfinite(window_lse[r]):
+            continue
+        allow = np.asarray(block_mask(i // BLOCK), dtype=bool)[: i + 1]
+        keys = np.nonzero(allow)[0]
+        z = (k[keys] @ q[i]) * scale
+        S[keys] += np.exp(z - window_lse[r])
+    return S
+
+
+def kv_select_head(q, k, block_mask, window: int, keep_k: int, scale: float | None = None,
+                   lse_rows=None):
+    """KV selection of one head after its attention pass [KV-1.5x]: the row
+    normalisers, the window score S and the keep set (the keep_k keys with the
+    highest S, ties to the lower index, ascending; top-k as everywhere else).
+    lse_rows: rows whose lse is returned (default: every row)."""
+    N, d = q.shape
+    scale = default_scale(d) if scale is None else scale
+    rows = np.arange(N) if lse_rows is None else np.asarray(lse_rows)
+    lse = row_lse(q, k, rows, block_mask, scale)
+    win = np.arange(N - window, N)
+    lse_w = row_lse(q, k, win, block_mask, scale)
+    S = kv_score(q, k, lse_w, block_mask, window, scale)
+    return {"lse": lse, "lse_rows": rows, "score": S, "keep": topk_indices(S, keep_k)}
 
 
 # ----------------------------------------------------------------------------- counting
