@@ -50,11 +50,18 @@ UNIT = "TFLOP/s"
 MEASURED_TRAFFIC = {
     "workload": "mixed_128k",
     "kind": "vs",
-    "bytes": 2.53e9 + 0.65489e9,
+    "bytes": 2.53e9 + 0.654e9,
     "sources": ("dynamic_sparse_attention_slash_gb300/csrc/prefill.cu",
                 "dynamic_sparse_attention_slash_gb300/csrc/sm103_ptx.cuh"),
-    "sha256": "fb73cbeb84b7fbd35ea4a395916e3fdfb5cef5f9d681ee301e71d703c9ffcc09",
+    "sha256": "d941acb562cbaa8ab9b6ab4b3cc0728cf5f306cad4dbf12bc1b6aaa4bc0ccd23",
 }
+
+
+# KV selection after the prefill: the observation window (query rows) follows
+# the KV-sparsity page's worked example (256 instruction tokens); the page gives
+# no kept count per head, 4096 is used here.
+KV_WINDOW = 256
+KV_KEEP = 4096
 
 
 def measured_traffic(workload: str, kind: str):
@@ -281,6 +288,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=24, help="oracle rows per head (reference arm)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
+    ap.add_argument("--no-kv-select", action="store_true",
+                    help="skip the KV-selection measurement (window score + keep set)")
     args = ap.parse_args()
     rank, local, world = dist_setup()
     if args.impl == "reference":
@@ -318,18 +327,19 @@ def main():
             e.record(stream)
         return evs
 
-    def step(events=None, export=None, qq=q, kk=k, vv=v, oo=out):
+    def step(events=None, export=None, qq=q, kk=k, vv=v, oo=out, kv=None):
         ev = events or {}
         if heads["vs"]:
             msa.msa_vertical_slash(qq, kk, vv, w.vertical_topk, w.slash, oo, last_q=w.last_q,
                                    heads=heads["vs"], workspace=ws["vs"], stage_events=ev.get("vs"),
-                                   export=(export or {}).get("vs"))
+                                   export=(export or {}).get("vs"), kv_select=kv)
         if heads["bs"]:
             msa.msa_block_sparse(qq, kk, vv, w.block_topk, oo, heads=heads["bs"], workspace=ws["bs"],
-                                 stage_events=ev.get("bs"), export=(export or {}).get("bs"))
+                                 stage_events=ev.get("bs"), export=(export or {}).get("bs"),
+                                 kv_select=kv)
         if heads["st"]:
             msa.msa_streaming(qq, kk, vv, w.init_num, w.local_window_num, oo, heads=heads["st"],
-                              workspace=ws["st"], stage_events=ev.get("st"))
+                              workspace=ws["st"], stage_events=ev.get("st"), kv_select=kv)
 
     # exact work of one step, from the GPU's own index sets
     U_vs, U_bs = B * len(heads["vs"]), B * len(heads["bs"])
@@ -468,6 +478,31 @@ def main():
                  "sdpa_tflops": (4 * D * dense_pairs / (sdpa_ms * 1e-3) / 1e12) if sdpa_ms else None}
         del dout
 
+    # ---- KV selection after the prefill (a separate measurement, not part of the
+    # step): row normalisers exported by the attention kernel, the score of every
+    # key over the last KV_WINDOW query rows, and the KV_KEEP best keys per head
+    kvsel = None
+    if not args.no_kv_select and rank == 0:
+        kvb = msa.kv_select_buffers(q, KV_WINDOW, KV_KEEP)
+        step(kv=kvb)  # warm-up
+        ev = {kind: new_events() for kind in ("vs", "bs", "st") if heads[kind]}
+        torch.cuda.synchronize()
+        step(events=ev, kv=kvb)
+        torch.cuda.synchronize()
+        kv_ms = {kind: e[2 * msa.MSA_STAGE_KV_SELECT].elapsed_time(e[2 * msa.MSA_STAGE_KV_SELECT + 1])
+                 for kind, e in ev.items()}
+        pf_ms = {kind: e[2 * msa.MSA_STAGE_PREFILL].elapsed_time(e[2 * msa.MSA_STAGE_PREFILL + 1])
+                 for kind, e in ev.items()}
+        n_heads = sum(B * len(heads[kind]) for kind in ev)
+        # logits of the window rows against their causal keys, as dense work
+        win_pairs = KV_WINDOW * N - KV_WINDOW * (KV_WINDOW - 1) // 2
+        kvsel = {"window": KV_WINDOW, "keep_k": KV_KEEP, "ms": kv_ms, "ms_total": sum(kv_ms.values()),
+                 "prefill_ms_with_lse_export": pf_ms,
+                 "share_of_prefill": sum(kv_ms.values()) / max(sum(pf_ms.values()), 1e-9),
+                 "score_tflops_dense_window": 2 * D * win_pairs * n_heads
+                 / (sum(kv_ms.values()) * 1e-3) / 1e12}
+        del kvb
+
     # ---- CPU oracle on the host cores (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -498,6 +533,7 @@ def main():
             "density_vs_dense_causal": sum(pairs.values()) / dense_pairs,
             "dense_causal": dense,
             "device_status": status,
+            "kv_select": kvsel,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

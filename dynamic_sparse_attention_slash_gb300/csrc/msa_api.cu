@@ -65,6 +65,13 @@ int prepare(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v, const
   if (v->H != k->H || out->H != q->H) return MSA_ERR_INVALID;
   if (q->H % k->H != 0) return MSA_ERR_INVALID;
   if (opts && opts->flags != 0) return MSA_ERR_INVALID;
+  if (const msa_kv_select* kv = opts ? opts->kv_select : nullptr) {
+    if (!kv->lse || !aligned(kv->lse, 4)) return MSA_ERR_INVALID;
+    if (kv->keep && !kv->score) return MSA_ERR_INVALID;
+    if (kv->score && (!aligned(kv->score, 4) || kv->window < 1 || kv->window > q->N))
+      return MSA_ERR_INVALID;
+    if (kv->keep && (!aligned(kv->keep, 4) || kv->keep_k < 1)) return MSA_ERR_INVALID;
+  }
   c.opts = opts;
   c.st = opts ? static_cast<cudaStream_t>(opts->stream) : nullptr;
   c.last_q = (opts && opts->last_q) ? static_cast<int>(opts->last_q) : kLastQMax;
@@ -283,6 +290,7 @@ int finish(cudaError_t e, int launches) {
 PrefillParams base_prefill(const Call& c, msa_tensor* out, uint32_t* status) {
   PrefillParams p;
   std::memset(&p, 0, sizeof(p));
+  p.lse = (c.opts && c.opts->kv_select) ? c.opts->kv_select->lse : nullptr;
   p.g = c.g;
   p.npair = (c.g.NQ + 1) / 2;
   p.scale_log2 = c.scale * 1.4426950408889634f;
@@ -293,6 +301,32 @@ PrefillParams base_prefill(const Call& c, msa_tensor* out, uint32_t* status) {
   p.status = status;
   p.units = c.u;
   return p;
+}
+
+// KV selection after the prefill: the window score from the exported row
+// normalisers, then the keep set.  Nothing to do without opts->kv_select->score.
+cudaError_t run_kv_select(const Call& c, const msa_tensor* q, const msa_tensor* k,
+                          const KvMask& mask, const StageTimer& tm, int* launches) {
+  const msa_kv_select* kv = c.opts ? c.opts->kv_select : nullptr;
+  if (!kv || !kv->score) return cudaSuccess;
+  tm.begin(MSA_STAGE_KV_SELECT);
+  cudaError_t e = launch_kv_score(c.g, c.u, view(q), view(k), kv->lse, kv->score,
+                                  static_cast<int>(kv->window), mask, c.st, launches);
+  if (e == cudaSuccess && kv->keep) {
+    const int kk = static_cast<int>(kv->keep_k < c.g.N ? kv->keep_k : c.g.N);
+    e = launch_topk_units(kv->score, c.g.N, kk, c.g.Hq, c.u, c.g.n_units, kv->keep, c.st,
+                          launches);
+  }
+  tm.end(MSA_STAGE_KV_SELECT);
+  return e;
+}
+
+KvMask base_mask(const Call& c, int kind) {
+  KvMask m;
+  std::memset(&m, 0, sizeof(m));
+  m.kind = kind;
+  m.NB = c.g.NB;
+  return m;
 }
 
 }  // namespace
@@ -387,6 +421,15 @@ int msa_vertical_slash(const msa_tensor* q, const msa_tensor* k, const msa_tenso
   e = launch_prefill(p, mq, mk, mv, mkc, mvc, c.st, &launches);
   tm.end(MSA_STAGE_PREFILL);
   if (e != cudaSuccess) return finish(e, launches);
+  {
+    KvMask km = base_mask(c, kPrefillVS);
+    km.tile_dist = p.tile_dist;
+    km.dist_words = p.dist_words;
+    km.vertical = p.vertical;
+    km.kv = p.kv;
+    e = run_kv_select(c, q, k, km, tm, &launches);
+    if (e != cudaSuccess) return finish(e, launches);
+  }
   if (const msa_index_export* x = opts->export_idx) {
     const size_t U = static_cast<size_t>(c.g.n_units);
     auto cp = [&](void* dst, size_t off, size_t bytes) {
@@ -439,6 +482,14 @@ int msa_block_sparse(const msa_tensor* q, const msa_tensor* k, const msa_tensor*
   e = launch_prefill(p, mq, mk, mv, mdummy, mdummy, c.st, &launches);
   tm.end(MSA_STAGE_PREFILL);
   if (e != cudaSuccess) return finish(e, launches);
+  {
+    KvMask km = base_mask(c, kPrefillBS);
+    km.block_count = at<int32_t>(ws, L.block_count);
+    km.block_ids = at<int32_t>(ws, L.block_ids);
+    km.kb = L.kb;
+    e = run_kv_select(c, q, k, km, tm, &launches);
+    if (e != cudaSuccess) return finish(e, launches);
+  }
   if (const msa_index_export* x = opts->export_idx) {
     const size_t U = static_cast<size_t>(c.g.n_units);
     if (x->block_count)
@@ -482,6 +533,12 @@ int msa_streaming(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v,
   tm.begin(MSA_STAGE_PREFILL);
   e = launch_prefill(p, mq, mk, mv, mdummy, mdummy, c.st, &launches);
   tm.end(MSA_STAGE_PREFILL);
+  if (e == cudaSuccess) {
+    KvMask km = base_mask(c, kPrefillST);
+    km.init_num = p.init_num;
+    km.local_num = p.local_num;
+    e = run_kv_select(c, q, k, km, tm, &launches);
+  }
   return finish(e, launches);
 }
 

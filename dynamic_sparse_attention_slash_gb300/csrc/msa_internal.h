@@ -64,8 +64,28 @@ struct PrefillParams {
   int bs_tile_cap;
   // streaming plan
   int init_num, local_num;
+  // row normalisers lse_i (natural log) for KV selection: [B][Hq][N] f32, or null
+  float* lse;
   uint32_t* status;
   UnitMap units;
+};
+
+// Key set J_i of the call's attention, for the KV-selection score: which 64-key
+// blocks row block m admits (then the causal cut j <= i), plus vertical columns.
+struct KvMask {
+  int kind;                    // PrefillKind
+  int NB;
+  // vertical-slash: tile-distance bitset and the ascending vertical columns
+  const uint32_t* tile_dist;   // [units][dist_words]
+  int dist_words;
+  const int32_t* vertical;     // [units][kv]
+  int kv;
+  // block-sparse: kept blocks per row block, ascending
+  const int32_t* block_count;  // [units][NB]
+  const int32_t* block_ids;    // [units][NB][kb]
+  int kb;
+  // streaming
+  int init_num, local_num;
 };
 
 // ---------------------------------------------------------------- launches
@@ -74,6 +94,13 @@ cudaError_t launch_vs_estimate(const Geometry& g, const UnitMap& u, TensorView q
                                float* v_score, float* s_score, cudaStream_t st, int* n_launch);
 cudaError_t launch_topk(const float* scores, int64_t n, int64_t row_stride, int rows, int k,
                         int32_t* out_idx, int64_t out_stride, cudaStream_t st, int* n_launch);
+// Top-k of the rows of the selected units in [B][Hq][n] scores into [B][Hq][min(k, n)].
+cudaError_t launch_topk_units(const float* scores, int64_t n, int k, int Hq, const UnitMap& u,
+                              int units, int32_t* out_idx, cudaStream_t st, int* n_launch);
+// KV-selection score S of the selected units ([B][Hq][N] lse in, score out).
+cudaError_t launch_kv_score(const Geometry& g, const UnitMap& u, TensorView q, TensorView k,
+                            const float* lse, float* score, int window, const KvMask& mask,
+                            cudaStream_t st, int* n_launch);
 cudaError_t launch_vs_index(const Geometry& g, const UnitMap& u, TensorView k, TensorView v,
                             const int32_t* slash, int ks, const int32_t* vertical, int kv,
                             uint32_t* tile_dist, int dist_words, int32_t* qdelta,

@@ -559,6 +559,12 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
                                             static_cast<int64_t>(row) * P.out_sn);
 #pragma unroll
       for (int e = 0; e < 16; ++e) dst[e] = outv[e];
+      if (P.lse) {
+        // ln sum_j exp(z_ij) = (m + log2 l) ln 2: m is the (lazily updated) row
+        // max in log2 units, l the row sum relative to it
+        const float lse = have ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+        P.lse[(static_cast<int64_t>(b) * P.g.Hq + h) * P.g.N + row] = lse;
+      }
     }
   }
   tc_fence_before();

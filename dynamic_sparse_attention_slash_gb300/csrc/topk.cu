@@ -18,17 +18,14 @@ constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kItems = 8;  // consecutive elements per thread in the compaction pass
 
-__global__ void __launch_bounds__(kThreads) topk_rows_kernel(const float* __restrict__ scores,
-                                                             int64_t n, int64_t row_stride, int k,
-                                                             int32_t* __restrict__ out,
-                                                             int64_t out_stride) {
+// Top-k of one row s[0, n) into o[0, min(k, n)).
+__device__ __forceinline__ void topk_row(const float* __restrict__ s, int64_t n, int k,
+                                         int32_t* __restrict__ o) {
   __shared__ int hist[kWarps][256];
   __shared__ int total_hist[256];
   __shared__ int warp_sums[kWarps + 1];
   __shared__ uint32_t s_prefix, s_mask;
   __shared__ int s_need;
-  const float* s = scores + static_cast<int64_t>(blockIdx.x) * row_stride;
-  int32_t* o = out + static_cast<int64_t>(blockIdx.x) * out_stride;
   const int tid = threadIdx.x, warp = tid >> 5;
   if (k >= n) {
     for (int64_t j = tid; j < n; j += kThreads) o[j] = static_cast<int32_t>(j);
@@ -112,7 +109,37 @@ __global__ void __launch_bounds__(kThreads) topk_rows_kernel(const float* __rest
   }
 }
 
+// One CTA per row; row r at scores + r * row_stride.
+__global__ void __launch_bounds__(kThreads) topk_rows_kernel(const float* __restrict__ scores,
+                                                             int64_t n, int64_t row_stride, int k,
+                                                             int32_t* __restrict__ out,
+                                                             int64_t out_stride) {
+  topk_row(scores + static_cast<int64_t>(blockIdx.x) * row_stride, n, k,
+           out + static_cast<int64_t>(blockIdx.x) * out_stride);
+}
+
+// One CTA per selected (batch, head) unit u; its row lives at query-head index
+// (u / n_heads) * Hq + heads[u % n_heads] of [B][Hq][n] scores and [B][Hq][k] out.
+__global__ void __launch_bounds__(kThreads) topk_units_kernel(const float* __restrict__ scores,
+                                                              int64_t n, int k, int Hq,
+                                                              const __grid_constant__ UnitMap u,
+                                                              int32_t* __restrict__ out) {
+  const int unit = blockIdx.x;
+  const int64_t row = static_cast<int64_t>(unit / u.n_heads) * Hq + u.heads[unit % u.n_heads];
+  const int kk = k < n ? k : static_cast<int>(n);
+  topk_row(scores + row * n, n, k, out + row * kk);
+}
+
 }  // namespace
+
+cudaError_t launch_topk_units(const float* scores, int64_t n, int k, int Hq, const UnitMap& u,
+                              int units, int32_t* out_idx, cudaStream_t st, int* n_launch) {
+  if (units <= 0) return cudaSuccess;
+  topk_units_kernel<<<units, kThreads, 0, st>>>(scores, n, k, Hq, u, out_idx);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) ++*n_launch;
+  return e;
+}
 
 cudaError_t launch_topk(const float* scores, int64_t n, int64_t row_stride, int rows, int k,
                         int32_t* out_idx, int64_t out_stride, cudaStream_t st, int* n_launch) {

@@ -36,7 +36,8 @@ MSA_STAGE_ESTIMATE = 0
 MSA_STAGE_TOPK = 1
 MSA_STAGE_INDEX = 2
 MSA_STAGE_PREFILL = 3
-MSA_STAGE_COUNT = 4
+MSA_STAGE_KV_SELECT = 4
+MSA_STAGE_COUNT = 5
 
 EXPORTED_SYMBOLS = (
     "msa_vertical_slash", "msa_block_sparse", "msa_streaming", "msa_workspace_bytes",
@@ -63,12 +64,18 @@ class MsaIndexExport(ctypes.Structure):
                 ("block_ids", ctypes.c_void_p)]
 
 
+class MsaKvSelect(ctypes.Structure):
+    _fields_ = [("lse", ctypes.c_void_p), ("score", ctypes.c_void_p), ("keep", ctypes.c_void_p),
+                ("window", ctypes.c_int64), ("keep_k", ctypes.c_int64)]
+
+
 class MsaOpts(ctypes.Structure):
     _fields_ = [("stream", ctypes.c_void_p), ("last_q", ctypes.c_int64), ("scale", ctypes.c_float),
                 ("heads", ctypes.POINTER(ctypes.c_int32)), ("n_heads", ctypes.c_int32),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
                 ("export_idx", ctypes.POINTER(MsaIndexExport)),
-                ("stage_events", ctypes.POINTER(ctypes.c_void_p)), ("flags", ctypes.c_int32)]
+                ("stage_events", ctypes.POINTER(ctypes.c_void_p)), ("flags", ctypes.c_int32),
+                ("kv_select", ctypes.POINTER(MsaKvSelect))]
 
 
 _lib = None
@@ -178,7 +185,7 @@ class _Prepared:
 
 
 def _opts(q, k, kind, p0, p1, last_q, scale, heads, workspace, export, stage_events, stream,
-          keep):
+          keep, kv_select=None):
     opts = MsaOpts()
     opts.stream = _stream_ptr(stream)
     opts.last_q = int(last_q)
@@ -205,16 +212,28 @@ def _opts(q, k, kind, p0, p1, last_q, scale, heads, workspace, export, stage_eve
         arr = (ctypes.c_void_p * (2 * MSA_STAGE_COUNT))(*[ev.cuda_event for ev in stage_events])
         keep.append(arr)
         opts.stage_events = arr
+    if kv_select is not None:
+        def ptr(name):
+            t = kv_select.get(name)
+            if t is None:
+                return None
+            if not t.is_cuda:
+                raise ValueError(f"kv_select['{name}'] must be a CUDA tensor (the kernels write it)")
+            return t.data_ptr()
+        kv = MsaKvSelect(ptr("lse"), ptr("score"), ptr("keep"), int(kv_select.get("window", 0)),
+                         int(kv_select.get("keep_k", 0)))
+        keep.append(kv)
+        opts.kv_select = ctypes.pointer(kv)
     return opts, workspace
 
 
 def _run(fn_name, kind, q, k, v, args, out, p0, p1, last_q, scale, heads, workspace, export,
-         stage_events, stream):
+         stage_events, stream, kv_select=None):
     lib = load_library()
     prep = _Prepared(q, k, v, out, stream)
     keep = []
     opts, _ = _opts(prep.q, prep.k, kind, p0, p1, last_q, scale, heads, workspace, export,
-                    stage_events, stream, keep)
+                    stage_events, stream, keep, kv_select)
     qt, kt, vt, ot = describe(prep.q), describe(prep.k), describe(prep.v), describe(prep.out)
     status = getattr(lib, fn_name)(ctypes.byref(qt), ctypes.byref(kt), ctypes.byref(vt), *args,
                                    ctypes.byref(ot), ctypes.byref(opts))
@@ -223,31 +242,48 @@ def _run(fn_name, kind, q, k, v, args, out, p0, p1, last_q, scale, heads, worksp
     return prep.result()
 
 
+def kv_select_buffers(q, window: int, keep_k: int = 0, score: bool = True):
+    """Device buffers for the KV selection of a call on q [B,Hq,N,d]: lse and
+    score f32 [B,Hq,N], keep int32 [B,Hq,min(keep_k,N)] (keep_k = 0: no keep set).
+    Pass the returned dict as kv_select=."""
+    B, Hq, N, _ = q.shape
+    f = dict(dtype=torch.float32, device=q.device)
+    out = {"lse": torch.zeros((B, Hq, N), **f), "score": None, "keep": None,
+           "window": int(window), "keep_k": int(keep_k)}
+    if score:
+        out["score"] = torch.zeros((B, Hq, N), **f)
+        if keep_k > 0:
+            out["keep"] = torch.zeros((B, Hq, min(keep_k, N)), dtype=torch.int32, device=q.device)
+    return out
+
+
 def msa_vertical_slash(q, k, v, vertical_topk: int, slash: int, out=None, *, last_q: int = 64,
                        scale: Optional[float] = None, heads: Optional[Sequence[int]] = None,
-                       workspace=None, export=None, stage_events=None, stream=None):
+                       workspace=None, export=None, stage_events=None, stream=None,
+                       kv_select=None):
     """Vertical-slash sparse attention (MInference 1.0 overview, section 2.2).
 
     q [B,Hq,N,128], k/v [B,Hkv,N,128] bf16.  Writes the selected heads of `out`
-    (allocated with zeros when None) and returns it.
+    (allocated with zeros when None) and returns it.  kv_select (see
+    kv_select_buffers) adds the row normalisers and the KV-selection score.
     """
     return _run("msa_vertical_slash", MSA_KIND_VERTICAL_SLASH, q, k, v,
                 (ctypes.c_int64(vertical_topk), ctypes.c_int64(slash)), out, vertical_topk, slash,
-                last_q, scale, heads, workspace, export, stage_events, stream)
+                last_q, scale, heads, workspace, export, stage_events, stream, kv_select)
 
 
 def msa_block_sparse(q, k, v, topk: int, out=None, *, scale: Optional[float] = None,
                      heads: Optional[Sequence[int]] = None, workspace=None, export=None,
-                     stage_events=None, stream=None):
+                     stage_events=None, stream=None, kv_select=None):
     """Block-sparse attention (MInference 1.0 overview, section 2.2)."""
     return _run("msa_block_sparse", MSA_KIND_BLOCK_SPARSE, q, k, v, (ctypes.c_int64(topk),), out,
-                topk, 0, 0, scale, heads, workspace, export, stage_events, stream)
+                topk, 0, 0, scale, heads, workspace, export, stage_events, stream, kv_select)
 
 
 def msa_streaming(q, k, v, init_num: int, local_window_num: int, out=None, *,
                   scale: Optional[float] = None, heads: Optional[Sequence[int]] = None,
-                  workspace=None, stage_events=None, stream=None):
+                  workspace=None, stage_events=None, stream=None, kv_select=None):
     """Streaming / A-shape attention (MInference 1.0 overview, kernel listing)."""
     return _run("msa_streaming", MSA_KIND_STREAMING, q, k, v,
                 (ctypes.c_int64(init_num), ctypes.c_int64(local_window_num)), out, 0, 0, 0, scale,
-                heads, workspace, None, stage_events, stream)
+                heads, workspace, None, stage_events, stream, kv_select)

@@ -72,7 +72,8 @@ extern "C" {
 #define MSA_STAGE_TOPK 1     /* vertical-slash: top-k of vertical and slash scores */
 #define MSA_STAGE_INDEX 2    /* sparse format / pooling and selection, and the f16 copy of v */
 #define MSA_STAGE_PREFILL 3  /* sparse attention itself */
-#define MSA_STAGE_COUNT 4
+#define MSA_STAGE_KV_SELECT 4 /* KV-selection score and keep set (only with opts->kv_select) */
+#define MSA_STAGE_COUNT 5
 
 #define MSA_MAX_HEADS 1024 /* most query heads one call may select */
 
@@ -111,6 +112,37 @@ typedef struct msa_index_export {
   int32_t* block_ids;
 } msa_index_export;
 
+/*
+ * KV selection after the prefill ("How KV sparsity achieves 1.5x acceleration
+ * for vLLM", Novita AI blog, section "2. Attention modification", and the
+ * PyramidKV score it quotes): the attention kernel also returns each row's
+ * softmax normaliser (row max and running sum, here combined into one number); a
+ * second pass in key-major ("kq") order forms the probabilities of the query
+ * rows of the instruction window [N - window, N) from it and sums them per key;
+ * each head then keeps the keep_k keys with the highest sums.
+ *
+ * Every buffer is caller-owned device memory, contiguous, indexed by the query
+ * head h of q (not by the position in opts->heads); entries of heads that are
+ * not selected are left untouched.  J_i below is the key set row i attends to
+ * under the call's mask (causal, sparse).
+ *   lse     float [B][Hq][N], required: lse_i = ln sum_{j in J_i} exp(z_ij) with
+ *           z_ij = scale * q_i . k_j, i.e. rowmax_i + ln(rowsum_i); -inf for a row
+ *           with no key.  Written for every row of the selected heads.
+ *   score   float [B][Hq][N] or NULL (skip the score and the keep set):
+ *           S_j = sum over window rows i with j in J_i of exp(z_ij - lse_i).
+ *   keep    int32 [B][Hq][min(keep_k, N)] or NULL: the keys with the highest S
+ *           (ties to the lower index), ascending.  Needs score.
+ *   window  1 <= window <= N when score is set.
+ *   keep_k  >= 1 when keep is set (larger than N is clamped).
+ */
+typedef struct msa_kv_select {
+  float* lse;
+  float* score;
+  int32_t* keep;
+  int64_t window;
+  int64_t keep_k;
+} msa_kv_select;
+
 typedef struct msa_opts {
   void* stream;          /* cudaStream_t; NULL = legacy default stream */
   int64_t last_q;        /* vertical-slash estimate rows; 0 = 64; 1..64 accepted */
@@ -120,8 +152,10 @@ typedef struct msa_opts {
   void* workspace;       /* device scratch, 256-byte aligned */
   size_t workspace_bytes;
   const msa_index_export* export_idx; /* NULL = no export */
-  void* const* stage_events; /* NULL, or cudaEvent_t[2 * MSA_STAGE_COUNT]: start/stop per stage */
+  void* const* stage_events; /* NULL, or cudaEvent_t[2 * MSA_STAGE_COUNT]: start/stop per stage
+                                (a stage a call does not run records nothing) */
   int32_t flags;             /* reserved, must be 0 */
+  const msa_kv_select* kv_select; /* NULL = no row normalisers, no KV selection */
 } msa_opts;
 
 /*

@@ -125,3 +125,44 @@ def test_status_strings_and_counter(lib):
         assert lib.msa_status_string(code)
     assert lib.msa_status_string(99) == b"unknown status"
     assert lib.msa_kernel_launches() >= 0
+
+
+def test_struct_layout_matches_header(tmp_path):
+    """The ctypes mirror of msa_opts / msa_kv_select has the C layout (gcc)."""
+    from dynamic_sparse_attention_slash_gb300.msa import MsaKvSelect, MsaOpts
+    src = tmp_path / "layout.c"
+    src.write_text(
+        '#include <stddef.h>\n#include <stdio.h>\n#include "msa.h"\n'
+        'int main(void) { printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(msa_opts), '
+        'offsetof(msa_opts, flags), offsetof(msa_opts, kv_select), sizeof(msa_kv_select), '
+        'offsetof(msa_kv_select, window), offsetof(msa_kv_select, keep_k)); return 0; }\n')
+    exe = tmp_path / "layout"
+    import subprocess
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    assert got == [ctypes.sizeof(MsaOpts), MsaOpts.flags.offset, MsaOpts.kv_select.offset,
+                   ctypes.sizeof(MsaKvSelect), MsaKvSelect.window.offset,
+                   MsaKvSelect.keep_k.offset]
+
+
+def test_kv_select_rejected_on_host(lib):
+    from dynamic_sparse_attention_slash_gb300 import msa
+    q, k, v, out = T(), T(), T(), T()
+
+    def status(**kw):
+        kv = msa.MsaKvSelect(**kw)
+        o = opts(kv_select=ctypes.pointer(kv))
+        return call_vs(lib, q, k, v, out, o=o)
+
+    ok_buf = 0x20000
+    assert status(lse=None, score=ok_buf, window=64) == msa.MSA_ERR_INVALID
+    assert status(lse=ok_buf, score=ok_buf, window=0) == msa.MSA_ERR_INVALID
+    assert status(lse=ok_buf, score=ok_buf, window=1025) == msa.MSA_ERR_INVALID
+    assert status(lse=ok_buf, keep=ok_buf, keep_k=8) == msa.MSA_ERR_INVALID   # keep needs score
+    assert status(lse=ok_buf, score=ok_buf, window=64, keep=ok_buf, keep_k=0) == msa.MSA_ERR_INVALID
+    assert status(lse=ok_buf + 2, window=64) == msa.MSA_ERR_INVALID           # misaligned
+    # a valid selection block passes validation and then fails on the missing workspace
+    assert status(lse=ok_buf, score=ok_buf, window=64, keep=ok_buf, keep_k=8) == \
+        msa.MSA_ERR_WORKSPACE
