@@ -17,6 +17,11 @@ from bf16 inputs converted exactly.  Sources, by page title and section:
             and slash index sets, convert them to a sparse format, run
             block-sparse attention) and the block-sparse head (mean-pool Q and
             K, block-level weights, top-k block index, sparse attention).
+* [MInf-2.1] same page, section 2.1 "Kernel-Aware Optimal Sparse Pattern
+            Search": candidates of each pattern share a FLOPs target measured
+            as the kernel computes it; one reference example picks, per head,
+            the pattern and setting with the best recall of the attention
+            output.
 * [MInf-API] same page, the "using only the kernel" listing: the entry points
             vertical_slash_sparse_attention(q,k,v,vertical_topk,slash),
             block_sparse_attention(q,k,v,topk) and
@@ -48,7 +53,11 @@ design notes with its reason):
 * KV selection: the exported normaliser is lse = rowmax + ln(l); a window row's
   probabilities are those of the attention the call computed (zero outside
   its key set J_i); the score is per query head; no pooling of the score
-  before its top-k (the page names none).
+  before its top-k (the page names none);
+* pattern search: "recall of the attention output" is the dense attention
+  mass a mask keeps, averaged over rows; per pattern the search uses the most
+  expensive setting within the FLOPs budget; the best recall wins, ties to the
+  earlier pattern.
 
 Parity pins for every function live in tests/test_oracle_*.py.
 """
@@ -440,6 +449,88 @@ def kv_select_head(q, k, block_mask, window: int, keep_k: int, scale: float | No
     lse_w = row_lse(q, k, win, block_mask, scale)
     S = kv_score(q, k, lse_w, block_mask, window, scale)
     return {"lse": lse, "lse_rows": rows, "score": S, "keep": topk_indices(S, keep_k)}
+
+
+# ----------------------------------------------------------------------------- pattern search
+def mass_recall(q, k, rows, block_mask, scale: float) -> np.ndarray:
+    """Recall of the dense attention that a mask keeps [MInf-2.1]: for each row i,
+    sum over j in J_i of the dense causal softmax A_dense[i, j] (1 for the dense
+    mask, 0 for a row whose J_i is empty).  Computed from the dense softmax
+    itself, not from normalisers."""
+    out = np.zeros(len(rows))
+    for r, i in enumerate(rows):
+        z = (k[: i + 1] @ q[i]) * scale
+        a = np.exp(z - z.max())
+        a /= a.sum()
+        allow = np.asarray(block_mask(i // BLOCK), dtype=bool)[: i + 1]
+        out[r] = a[allow].sum()
+    return out
+
+
+def choose_setting(flops, budget: float) -> int:
+    """Index of the candidate setting of one pattern that the search uses at a
+    FLOPs budget [MInf-2.1] ("candidates of similar cost"): the most expensive
+    setting whose kernel FLOPs do not exceed the budget; if every setting
+    exceeds it, the cheapest (ties to the earlier setting)."""
+    flops = np.asarray(flops, dtype=np.float64)
+    fit = np.nonzero(flops <= budget)[0]
+    if fit.size:
+        return int(fit[np.argmax(flops[fit])])  # argmax: first of equal maxima
+    return int(np.argmin(flops))
+
+
+def choose_pattern(recalls) -> int:
+    """Pattern with the highest recall of the attention output [MInf-2.1]; ties
+    go to the earlier pattern (vertical-slash, block-sparse, streaming)."""
+    return int(np.argmax(np.asarray(recalls, dtype=np.float64)))
+
+
+def mask_nnz(block_mask, N: int) -> int:
+    """Admitted (i, j) pairs, j <= i, of a mask given per 64-row block."""
+    total = 0
+    for m in range((N + BLOCK - 1) // BLOCK):
+        allow = np.asarray(block_mask(m), dtype=bool)[:N]
+        c = np.cumsum(allow)
+        r0, r1 = m * BLOCK, min(N, (m + 1) * BLOCK)
+        total += int(c[r0:r1].sum())
+    return total
+
+
+def pattern_masks(q, k, pattern: str, setting, scale: float):
+    """Block mask of one head under one candidate: ("vs", (vertical_topk, slash)),
+    ("bs", topk) or ("st", (init_num, local_window_num))."""
+    N = q.shape[0]
+    if pattern == "vs":
+        idx = vertical_slash_indices(q, k, setting[0], setting[1], 64, scale)
+        return vs_block_mask(idx["active"], idx["columns"], N)
+    if pattern == "bs":
+        sel, _ = block_sparse_blocks(q, k, setting, scale)
+        return block_mask_from_blocks(sel, N)
+    NB = (N + BLOCK - 1) // BLOCK
+    return block_mask_from_blocks([streaming_blocks(m, setting[0], setting[1]) for m in range(NB)], N)
+
+
+def pattern_search_head(q, k, candidates, budget_flops: float, rows=None, scale=None):
+    """Kernel-aware pattern search for one head [MInf-2.1].
+
+    candidates: {"vs": [(vertical_topk, slash), ...], "bs": [topk, ...],
+    "st": [(init_num, local_window_num), ...]}; FLOPs of a candidate are the
+    kernel's 4 * d * (admitted causal pairs); recall is the mean of mass_recall
+    over `rows` (default: every row).  Returns the chosen pattern, its setting,
+    and the per-pattern (setting index, FLOPs, recall) records."""
+    N, d = q.shape
+    scale = default_scale(d) if scale is None else scale
+    rows = np.arange(N) if rows is None else np.asarray(rows)
+    order = [p for p in ("vs", "bs", "st") if candidates.get(p)]
+    recs = {}
+    for p in order:
+        masks = [pattern_masks(q, k, p, st, scale) for st in candidates[p]]
+        flops = [4 * d * mask_nnz(mk, N) for mk in masks]
+        i = choose_setting(flops, budget_flops)
+        rec = float(mass_recall(q, k, rows, masks[i], scale).mean())
+        recs[p] = {"setting": i, "flops": flops, "recall": rec}
+    best = order[choose_pattern([recs[p]["recall"] for p in order])]
+    return best, candidates[best][recs[best]["setting"]], recs
 
 
 # ----------------------------------------------------------------------------- counting
