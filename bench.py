@@ -35,6 +35,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 from dynamic_sparse_attention_slash_gb300 import inputs  # noqa: E402
+from dynamic_sparse_attention_slash_gb300.flops import bs_pairs, st_pairs, vs_pairs  # noqa: E402,F401
 
 D = 128
 METRIC = "sparse prefill attention effective TFLOP/s at 128K tokens"
@@ -63,6 +64,14 @@ MEASURED_TRAFFIC = {
 KV_WINDOW = 256
 KV_KEEP = 4096
 
+# Kernel-aware pattern search on the benchmark's own example: four settings per
+# pattern around the workload's settings, at a budget of 10 % of the dense
+# causal attention FLOPs per head.
+SEARCH_BUDGET_FRAC = 0.10
+SEARCH_CANDIDATES = {"vs": [(1000, 128), (1000, 256), (1000, 512), (1000, 1024)],
+                     "bs": [25, 50, 100, 200],
+                     "st": [(1, 64), (1, 128), (1, 256), (1, 512)]}
+
 
 def measured_traffic(workload: str, kind: str):
     """DRAM bytes per launch of the dominant prefill launch, or None when no
@@ -79,40 +88,6 @@ def measured_traffic(workload: str, kind: str):
     except OSError:
         return None
     return t["bytes"] if h.hexdigest() == t["sha256"] else None
-
-
-def vs_pairs(tile_dist_words, vertical, N: int) -> int:
-    """Admitted (i, j) pairs, j <= i, of one vertical-slash head: active 64x64
-    tiles (the diagonal one triangular) plus the uncovered vertical columns."""
-    NB = N // 64
-    words = np.asarray(tile_dist_words, dtype=np.int64) & 0xFFFFFFFF
-    t = np.arange(NB)
-    bits = ((words[t >> 5] >> (t & 31)) & 1).astype(np.int64)
-    cum = np.cumsum(bits)  # cum[m] = #{t in D, t <= m}
-    diag = int(bits[0])
-    total = int(((cum - diag) * 4096).sum()) + diag * 2080 * NB
-    V = np.asarray(vertical, dtype=np.int64)
-    mj = V // 64
-    # row blocks m > mj whose distance m - mj is not in D contribute 64 rows
-    upto = NB - 1 - mj
-    in_d = np.where(upto >= 1, cum[np.maximum(upto, 0)] - diag, 0)
-    total += int((64 * (upto - in_d)).sum())
-    if not diag:  # the key's own row block: rows j..64*mj+63
-        total += int((64 * (mj + 1) - V).sum())
-    return total
-
-
-def bs_pairs(block_count) -> int:
-    c = np.asarray(block_count, dtype=np.int64)
-    return int(((c - 1) * 4096 + 2080).sum())
-
-
-def st_pairs(N: int, init_num: int, local: int) -> int:
-    total = 0
-    for m in range(N // 64):
-        blocks = set(range(min(init_num, m + 1))) | set(range(max(0, m - local + 1), m + 1))
-        total += 2080 + 4096 * (len(blocks) - 1)
-    return total
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -288,6 +263,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=24, help="oracle rows per head (reference arm)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
+    ap.add_argument("--no-search", action="store_true",
+                    help="skip the kernel-aware pattern search measurement")
     ap.add_argument("--no-kv-select", action="store_true",
                     help="skip the KV-selection measurement (window score + keep set)")
     args = ap.parse_args()
@@ -503,6 +480,24 @@ def main():
                  / (sum(kv_ms.values()) * 1e-3) / 1e12}
         del kvb
 
+    # ---- kernel-aware pattern search (a separate measurement, not part of the step)
+    psearch = None
+    if not args.no_search and rank == 0:
+        from dynamic_sparse_attention_slash_gb300 import search as msearch
+        budget = SEARCH_BUDGET_FRAC * 4 * D * N * (N + 1) / 2
+        res = msearch.search(q, k, v, SEARCH_CANDIDATES, budget, last_q=w.last_q)
+        chosen = {p: 0 for p in msearch.PATTERNS}
+        recalls = []
+        for (b_, h_), (p_, _) in res["assignment"].items():
+            chosen[p_] += 1
+            r = res["records"][(b_, h_)][p_]
+            recalls.append(r["recall"][r["setting"]])
+        n_calls = 1 + sum(len(c) for c in SEARCH_CANDIDATES.values())
+        psearch = {"ms": res["ms"], "calls": n_calls, "heads": len(res["assignment"]),
+                   "budget_frac_of_dense": SEARCH_BUDGET_FRAC, "candidates": SEARCH_CANDIDATES,
+                   "chosen": chosen, "mean_recall_of_choice": float(np.mean(recalls)),
+                   "min_recall_of_choice": float(np.min(recalls))}
+
     # ---- CPU oracle on the host cores (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -534,6 +529,7 @@ def main():
             "dense_causal": dense,
             "device_status": status,
             "kv_select": kvsel,
+            "pattern_search": psearch,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

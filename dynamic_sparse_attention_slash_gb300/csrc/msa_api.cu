@@ -330,6 +330,9 @@ KvMask base_mask(const Call& c, int kind) {
 }
 
 }  // namespace
+
+void note_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n)); }
+
 }  // namespace msa
 
 using namespace msa;

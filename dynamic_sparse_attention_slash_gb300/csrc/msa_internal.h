@@ -88,6 +88,9 @@ struct KvMask {
   int init_num, local_num;
 };
 
+// Adds n to the library's kernel-launch counter (msa_kernel_launches).
+void note_launches(int n);
+
 // ---------------------------------------------------------------- launches
 cudaError_t launch_vs_estimate(const Geometry& g, const UnitMap& u, TensorView q, TensorView k,
                                int last_q, float* partial, int n_split, float* row_stats,

@@ -41,7 +41,7 @@ MSA_STAGE_COUNT = 5
 
 EXPORTED_SYMBOLS = (
     "msa_vertical_slash", "msa_block_sparse", "msa_streaming", "msa_workspace_bytes",
-    "msa_device_status", "msa_status_string", "msa_kernel_launches",
+    "msa_device_status", "msa_status_string", "msa_kernel_launches", "msa_mass_recall",
 )
 
 
@@ -107,6 +107,11 @@ def load_library():
     lib.msa_status_string.restype = ctypes.c_char_p
     lib.msa_kernel_launches.argtypes = []
     lib.msa_kernel_launches.restype = ctypes.c_uint64
+    F = ctypes.c_void_p
+    lib.msa_mass_recall.argtypes = [F, F, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                    ctypes.c_int64, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32,
+                                    F, ctypes.c_void_p]
+    lib.msa_mass_recall.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -287,3 +292,30 @@ def msa_streaming(q, k, v, init_num: int, local_window_num: int, out=None, *,
     return _run("msa_streaming", MSA_KIND_STREAMING, q, k, v,
                 (ctypes.c_int64(init_num), ctypes.c_int64(local_window_num)), out, 0, 0, 0, scale,
                 heads, workspace, None, stage_events, stream, kv_select)
+
+
+def mass_recall(lse, ref_lse, recall=None, *, row0: int = 0, heads: Optional[Sequence[int]] = None,
+                stream=None):
+    """Mean kept dense-attention mass per head over rows [row0, N) (MInference 1.0
+    overview, section 2.1): lse / ref_lse are f32 [B,Hq,N] normalisers of a sparse
+    and a dense call; writes the selected heads of recall f32 [B,Hq]."""
+    lib = load_library()
+    B, Hq, N = lse.shape
+    for name, t in (("lse", lse), ("ref_lse", ref_lse)):
+        if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous() and t.shape == lse.shape):
+            raise ValueError(f"{name} must be a contiguous CUDA float32 tensor of shape {tuple(lse.shape)}")
+    if recall is None:
+        recall = torch.zeros((B, Hq), dtype=torch.float32, device=lse.device)
+    if not (recall.is_cuda and recall.dtype == torch.float32 and recall.is_contiguous()
+            and tuple(recall.shape) == (B, Hq)):
+        raise ValueError("recall must be a contiguous CUDA float32 tensor [B, Hq]")
+    arr, n = None, 0
+    if heads is not None:
+        arr = (ctypes.c_int32 * len(heads))(*[int(h) for h in heads])
+        n = len(heads)
+    status = lib.msa_mass_recall(lse.data_ptr(), ref_lse.data_ptr(), B, Hq, N, int(row0),
+                                 ctypes.cast(arr, ctypes.POINTER(ctypes.c_int32)) if arr else None,
+                                 n, recall.data_ptr(), _stream_ptr(stream))
+    if status != MSA_OK:
+        raise MsaError(status, "msa_mass_recall")
+    return recall

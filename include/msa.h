@@ -240,6 +240,26 @@ int msa_vertical_slash_static(const msa_tensor* q, const msa_tensor* k, const ms
                               void* stream);
 
 /*
+ * Recall of the dense attention that a sparse mask keeps, per head (MInference
+ * 1.0 overview, section 2.1 "Kernel-Aware Optimal Sparse Pattern Search": the
+ * search compares candidate patterns at similar kernel FLOPs by the recall of
+ * the attention output).  For row i the kept mass is
+ *   sum_{j in J_i} softmax_dense(i)_j = exp(lse_i - ref_lse_i),
+ * lse from a sparse call and ref_lse from a dense call (msa_streaming with
+ * init_num 0 and local_window_num N/64), both through msa_kv_select.lse.
+ *   lse, ref_lse  float [B][H][N] device buffers (as msa_kv_select.lse)
+ *   recall        float [B][H] device buffer: entry (b, h) of every selected
+ *                 head receives the mean kept mass over rows [row0, N); other
+ *                 entries are left untouched.  Rows with lse = -inf keep 0.
+ *   heads         HOST array of n_heads query-head ids (no repeats); NULL = all.
+ * 0 <= row0 < N.  Enqueued on `stream` (cudaStream_t; NULL = legacy default);
+ * deterministic (fixed-order reduction in double).
+ */
+int msa_mass_recall(const float* lse, const float* ref_lse, int64_t B, int64_t H, int64_t N,
+                    int64_t row0, const int32_t* heads, int32_t n_heads, float* recall,
+                    void* stream);
+
+/*
  * Workspace bytes needed by one call.  kind is MSA_KIND_*; p0/p1 are
  * (vertical_topk, slash) for vertical-slash, (topk, unused) for block-sparse.
  * n_heads is the number of selected query heads (<= 0: all of q's heads).
