@@ -45,7 +45,10 @@ design notes with its reason):
   chosen indices in ascending order; k is clamped to the number of candidates;
 * the sparse format expands every selected diagonal to the 64x64 key tiles it
   crosses and keeps vertical columns that no active tile of the row block
-  already covers;
+  already covers; for N not a multiple of 64 it is built over the sequence
+  padded to the next multiple (MInference's block kernels work on padded
+  blocks), so every row block counts 64 rows; block-sparse pooling averages
+  the real rows of a partial block;
 * the block-sparse head keeps the diagonal block plus the top-(topk-1) earlier
   blocks by pooled score; streaming keeps blocks [0, init_num) and the
   ``local_window_num`` blocks ending at the query's own block;
@@ -197,6 +200,9 @@ def vs_active_tiles(slash_idx, N: int, row_blocks=None) -> np.ndarray:
     [64m - o, 64m + 63 - o] (cut at 0) meets [64n, 64n + 63].
     Returns a boolean [NB, NB] matrix (row block m, key block n); with
     `row_blocks`, a [len(row_blocks), NB] matrix for those row blocks only.
+    When N is not a multiple of 64 the format is built over the sequence
+    padded to the next multiple (the last row block counts as 64 rows); the
+    causal cut later removes the padded keys.
     """
     NB = (N + BLOCK - 1) // BLOCK
     S = np.asarray(slash_idx, dtype=np.int64)
@@ -204,7 +210,7 @@ def vs_active_tiles(slash_idx, N: int, row_blocks=None) -> np.ndarray:
     active = np.zeros((len(blocks), NB), dtype=bool)
     for r, m in enumerate(blocks):
         first_row = m * BLOCK
-        last_row = min(N, (m + 1) * BLOCK) - 1
+        last_row = (m + 1) * BLOCK - 1
         lo = first_row - S
         hi = last_row - S
         keep = hi >= 0

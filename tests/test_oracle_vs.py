@@ -116,11 +116,12 @@ def test_topk_ties_prefer_lower_index():
 # ----------------------------------------------------------------------------- sparse format
 def enumerate_tiles(S, N):
     """Every (row i, offset o) pair with i - o >= 0 marks key i - o; a tile is
-    active iff it holds a marked key of one of its rows."""
+    active iff it holds a marked key of one of its rows (rows of the sequence
+    padded to a multiple of 64)."""
     NB = (N + 63) // 64
     act = np.zeros((NB, NB), dtype=bool)
     for o in S:
-        for i in range(o, N):
+        for i in range(o, NB * 64):
             act[i // 64, (i - o) // 64] = True
     return act
 
@@ -140,10 +141,11 @@ def distance_set_tiles(S, N):
     return act
 
 
-@pytest.mark.parametrize("N,seed", [(256, 0), (256, 1), (192, 2), (320, 3), (128, 4)])
+@pytest.mark.parametrize("N,seed", [(256, 0), (256, 1), (192, 2), (320, 3), (128, 4),
+                                    (200, 5), (77, 6), (130, 7), (1, 8), (63, 9)])
 def test_tiles_three_derivations_agree(N, seed):
     rng = np.random.default_rng(seed)
-    S = np.sort(rng.choice(N, size=int(rng.integers(1, 12)), replace=False))
+    S = np.sort(rng.choice(N, size=min(N, int(rng.integers(1, 12))), replace=False))
     a = O.vs_active_tiles(S, N)
     np.testing.assert_array_equal(a, enumerate_tiles(S, N))
     np.testing.assert_array_equal(a, distance_set_tiles(S, N))
