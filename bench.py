@@ -203,7 +203,7 @@ def oracle_sample(w, q, k, v, heads, rows_per_head: int, seed: int = 0):
             sel, _ = O.block_sparse_blocks(qn, kn, w.block_topk, scale)
             mask = O.block_mask_from_blocks(sel, N)
         else:
-            sel = [O.streaming_blocks(m, w.init_num, w.local_window_num) for m in range(N // 64)]
+            sel = [O.streaming_blocks(m, w.init_num, w.local_window_num) for m in range((N + 63) // 64)]
             mask = O.block_mask_from_blocks(sel, N)
         _, counts = O.attend_rows(qn, kn, vn, rows, lambda i: mask(i // 64), scale)
         flops += 4 * D * int(counts.sum())
@@ -323,9 +323,9 @@ def main():
     export = {}
     if U_vs:
         export["vs"] = {"vertical": torch.empty(U_vs, min(w.vertical_topk, N), dtype=torch.int32, device=dev),
-                        "tile_dist": torch.empty(U_vs, (N // 64 + 32) // 32, dtype=torch.int32, device=dev)}
+                        "tile_dist": torch.empty(U_vs, ((N + 63) // 64 + 32) // 32, dtype=torch.int32, device=dev)}
     if U_bs:
-        export["bs"] = {"block_count": torch.empty(U_bs, N // 64, dtype=torch.int32, device=dev)}
+        export["bs"] = {"block_count": torch.empty(U_bs, (N + 63) // 64, dtype=torch.int32, device=dev)}
     step(export=export)
     torch.cuda.synchronize()
     pairs = {"vs": 0, "bs": 0, "st": 0}
@@ -333,7 +333,7 @@ def main():
         td, vt = export["vs"]["tile_dist"].cpu().numpy(), export["vs"]["vertical"].cpu().numpy()
         pairs["vs"] = sum(vs_pairs(td[u], vt[u], N) for u in range(U_vs))
     if U_bs:
-        pairs["bs"] = bs_pairs(export["bs"]["block_count"].cpu().numpy())
+        pairs["bs"] = bs_pairs(export["bs"]["block_count"].cpu().numpy(), N)
     if heads["st"]:
         pairs["st"] = B * len(heads["st"]) * st_pairs(N, w.init_num, w.local_window_num)
     flops = {kk_: 4 * D * vv_ for kk_, vv_ in pairs.items()}
@@ -429,9 +429,9 @@ def main():
     if not args.no_dense and rank == 0:
         dout = torch.empty_like(q)
         d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        msa.msa_streaming(q, k, v, 0, N // 64, dout)
+        msa.msa_streaming(q, k, v, 0, (N + 63) // 64, dout)
         d0.record(stream)
-        msa.msa_streaming(q, k, v, 0, N // 64, dout)
+        msa.msa_streaming(q, k, v, 0, (N + 63) // 64, dout)
         d1.record(stream)
         torch.cuda.synchronize()
         ours_ms = d0.elapsed_time(d1)

@@ -207,8 +207,8 @@ __global__ void __launch_bounds__(kThreads) vs_estimate_scores_kernel(const __gr
     }
   }
   // offsets o > N-64 start before key 0; chunk 0 owns them
-  if (chunk == 0 && t < 63) {
-    const int o = N - 63 + t;  // first key N-64-o = -(t+1)
+  if (chunk == 0 && t < 63 && N - 63 + t >= 0) {
+    const int o = N - 63 + t;  // first key N-64-o = -(t+1); o >= 0 when N < 64 too
     float s = 0.f;
     for (int r = t + 1; r < 64; ++r) s += sm_a[r * kAStride + (r - t - 1)];
     ss[o] = s;

@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kThreads) kv_score_kernel(const __grid_constan
   const int w0 = N - a.window;          // first window row
   const int m_first = w0 >> 6;          // first window row block
   const int m_lo = max(m_first, j0 >> 6);  // earlier row blocks end before key j0
-  const int NB = N >> 6;
+  const int NB = (N + 63) >> 6;          // a partial last block counts
   float acc_s = 0.f;                    // score of key j0 + tid
   for (int m = m_lo; m < NB; ++m) {
     const int r0 = m * 64;
@@ -101,8 +101,8 @@ __global__ void __launch_bounds__(kThreads) kv_score_kernel(const __grid_constan
     cp_async_commit();
     if (tid < 64) {
       const int i = r0 + tid;
-      const float l = a.lse[row_base + i];
-      // rows before the window, and rows without keys, contribute nothing
+      const float l = i < N ? a.lse[row_base + i] : -INFINITY;
+      // rows before the window, padded rows and rows without keys contribute nothing
       s_lse2[tid] = (i >= w0 && l != -INFINITY) ? l * kLog2e : INFINITY;
     }
     if (tid < 2) s_adm[tid] = block_admitted(a.mask, unit, m, (j0 >> 6) + tid) ? 1 : 0;

@@ -36,7 +36,6 @@ int check_tensor(const msa_tensor* t) {
   if (!t || !t->data) return MSA_ERR_INVALID;
   if (t->B <= 0 || t->H <= 0 || t->N <= 0 || t->D <= 0) return MSA_ERR_INVALID;
   if (t->D != kHeadDim) return MSA_ERR_UNSUPPORTED;
-  if (t->N % kBlock != 0) return MSA_ERR_UNSUPPORTED;
   if (t->N > (int64_t{1} << 21)) return MSA_ERR_UNSUPPORTED;
   if (!aligned(t->data, 16)) return MSA_ERR_INVALID;
   if (t->sn < t->D || t->sn % 8 || t->sh % 8 || t->sb % 8 || t->sh < 0 || t->sb < 0)
@@ -76,6 +75,7 @@ int prepare(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v, const
   c.st = opts ? static_cast<cudaStream_t>(opts->stream) : nullptr;
   c.last_q = (opts && opts->last_q) ? static_cast<int>(opts->last_q) : kLastQMax;
   if (opts && (opts->last_q < 0 || opts->last_q > kLastQMax)) return MSA_ERR_INVALID;
+  if (c.last_q > q->N) c.last_q = static_cast<int>(q->N);  // a sequence shorter than the window
   c.scale = (opts && opts->scale != 0.f) ? opts->scale : 1.0f / std::sqrt(static_cast<float>(q->D));
   if (!std::isfinite(c.scale) || c.scale <= 0.f) return MSA_ERR_INVALID;
   // head selection
@@ -105,7 +105,7 @@ int prepare(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v, const
   g.Hkv = static_cast<int>(k->H);
   g.G = g.Hq / g.Hkv;
   g.N = static_cast<int>(q->N);
-  g.NB = g.N / kBlock;
+  g.NB = (g.N + kBlock - 1) / kBlock;  // a partial last block counts as a padded block
   g.NQ = (g.N + kTileM - 1) / kTileM;
   g.n_units = static_cast<int>(units);
   g.scale = c.scale;
@@ -348,7 +348,7 @@ size_t msa_workspace_bytes(int kind, const msa_tensor* q, const msa_tensor* k, i
   g.Hkv = static_cast<int>(k->H);
   g.G = g.Hkv > 0 ? g.Hq / g.Hkv : 1;
   g.N = static_cast<int>(q->N);
-  g.NB = g.N / kBlock;
+  g.NB = (g.N + kBlock - 1) / kBlock;  // a partial last block counts as a padded block
   g.NQ = (g.N + kTileM - 1) / kTileM;
   g.n_units = static_cast<int>(q->B * (n_heads > 0 ? n_heads : q->H));
   if (kind == MSA_KIND_VERTICAL_SLASH) {

@@ -50,7 +50,14 @@ int scratch_address(void** out) {
 extern "C" int msa_vertical_slash_static(const msa_tensor* q, const msa_tensor* k,
                                          const msa_tensor* v, int64_t vertical_topk,
                                          int64_t slash, msa_tensor* out, void* stream) {
-  const int32_t n_heads = (q && q->H > 0) ? static_cast<int32_t>(q->H) : 0;
+  // Full host-side validation first, without touching the device: with no
+  // workspace the call checks every argument and then stops at the workspace
+  // check, so anything but MSA_ERR_WORKSPACE is the argument error.
+  msa_opts check = {};
+  check.stream = stream;
+  const int valid = msa_vertical_slash(q, k, v, vertical_topk, slash, out, &check);
+  if (valid != MSA_ERR_WORKSPACE) return valid;
+  const int32_t n_heads = static_cast<int32_t>(q->H);
   const size_t need =
       msa_workspace_bytes(MSA_KIND_VERTICAL_SLASH, q, k, vertical_topk, slash, n_heads);
   if (need == 0) return MSA_ERR_INVALID;

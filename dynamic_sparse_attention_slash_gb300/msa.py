@@ -189,8 +189,38 @@ class _Prepared:
         return self.host_out
 
 
+def _check_buffers(q, kind, p0, p1, heads, export, kv_select):
+    """Every device buffer the library will write must hold what it writes
+    (sizes from include/msa.h); a short buffer is refused here, before the call."""
+    B, Hq, N, _ = q.shape
+    NB = (N + 63) // 64
+    U = B * (len(heads) if heads is not None else Hq)
+    need = {}
+    if kind == MSA_KIND_VERTICAL_SLASH:
+        need = {"v_score": U * N, "s_score": U * N, "vertical": U * min(p0, N),
+                "slash": U * min(p1, N), "tile_dist": U * ((NB + 32) // 32)}
+    elif kind == MSA_KIND_BLOCK_SPARSE:
+        need = {"block_count": U * NB, "block_ids": U * NB * min(p0, NB)}
+    for name, t in (export or {}).items():
+        if t is None:
+            continue
+        if name not in need:
+            raise ValueError(f"export['{name}'] is not written by this call")
+        if not t.is_cuda or t.numel() * t.element_size() < 4 * need[name]:
+            raise ValueError(f"export['{name}'] must be a CUDA buffer of >= {need[name]} 4-byte entries")
+    if kv_select is not None:
+        kk = min(int(kv_select.get("keep_k", 0) or 0), N)
+        for name, n in (("lse", B * Hq * N), ("score", B * Hq * N), ("keep", B * Hq * kk)):
+            t = kv_select.get(name)
+            if t is not None and (not t.is_cuda or not t.is_contiguous()
+                                  or t.numel() * t.element_size() < 4 * n):
+                raise ValueError(f"kv_select['{name}'] must be a contiguous CUDA buffer of >= {n} "
+                                 "4-byte entries")
+
+
 def _opts(q, k, kind, p0, p1, last_q, scale, heads, workspace, export, stage_events, stream,
           keep, kv_select=None):
+    _check_buffers(q, kind, p0, p1, heads, export, kv_select)
     opts = MsaOpts()
     opts.stream = _stream_ptr(stream)
     opts.last_q = int(last_q)

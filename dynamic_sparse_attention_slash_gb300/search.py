@@ -57,7 +57,7 @@ def search(q, k, v, candidates: Dict[str, list], budget_flops: float, *,
     time of the GPU work}.
     """
     B, Hq, N, D = q.shape
-    NB = N // 64
+    NB = (N + 63) // 64
     heads_l = list(range(Hq)) if heads is None else [int(h) for h in heads]
     units = [(b, h) for b in range(B) for h in heads_l]
     order = [p for p in PATTERNS if candidates.get(p)]
@@ -98,7 +98,7 @@ def search(q, k, v, candidates: Dict[str, list], budget_flops: float, *,
                 pairs = [vs_pairs(td[u], vt[u], N) for u in range(U)]
             elif p == "bs":
                 bc = ex["block_count"].cpu().numpy()
-                pairs = [bs_pairs(bc[u]) for u in range(U)]
+                pairs = [bs_pairs(bc[u], N) for u in range(U)]
             else:
                 pairs = [st_pairs(N, setting[0], min(setting[1], NB))] * U
             for u, (b, h) in enumerate(units):

@@ -21,8 +21,11 @@
  *           device memory, innermost dimension contiguous, other strides given
  *           in elements and multiples of 8 (16 bytes), base addresses 16-byte
  *           aligned.  Query head h reads KV head h / (Hq / Hkv).
- * Supported D = 128, N a positive multiple of 64, Hq a multiple of Hkv.  Other
- *           shapes return MSA_ERR_UNSUPPORTED before anything is enqueued.
+ * Supported D = 128, 1 <= N <= 2^21, Hq a multiple of Hkv.  Other shapes return
+ *           MSA_ERR_UNSUPPORTED before anything is enqueued.  When N is not a
+ *           multiple of 64 the block formats treat the last block as a padded
+ *           64-token block (causality keeps padded keys out of every real
+ *           row; padded rows are never written).
  * Causal    Key j is admitted for query i only if j <= i.
  * Blocks    Block quantities count 64-token blocks.
  * Memory    The caller owns every buffer.  The library allocates no device
@@ -56,7 +59,7 @@ extern "C" {
 /* Status codes. */
 #define MSA_OK 0
 #define MSA_ERR_INVALID 1     /* bad pointer, shape, stride or parameter value */
-#define MSA_ERR_UNSUPPORTED 2 /* valid but outside what this build handles (D != 128, N % 64 != 0) */
+#define MSA_ERR_UNSUPPORTED 2 /* valid but outside what this build handles (D != 128, N > 2^21) */
 #define MSA_ERR_WORKSPACE 3   /* workspace missing, misaligned or too small */
 #define MSA_ERR_CUDA 4        /* a CUDA call or kernel launch failed */
 #define MSA_ERR_TIMEOUT 5     /* a bounded device-side wait gave up (read by msa_device_status) */

@@ -41,7 +41,7 @@ def run_vs(q, k, v, vertical_topk, slash, last_q=64, heads=None):
         "s_score": torch.empty(U, N, dtype=torch.float32, device=dev),
         "vertical": torch.empty(U, kv, dtype=torch.int32, device=dev),
         "slash": torch.empty(U, ks, dtype=torch.int32, device=dev),
-        "tile_dist": torch.empty(U, (N // 64 + 32) // 32, dtype=torch.int32, device=dev),
+        "tile_dist": torch.empty(U, ((N + 63) // 64 + 32) // 32, dtype=torch.int32, device=dev),
     }
     out = msa.msa_vertical_slash(q, k, v, vertical_topk, slash, last_q=last_q, heads=heads,
                                  export=ex)
@@ -53,7 +53,7 @@ def run_bs(q, k, v, topk, heads=None):
     B, Hq, N, _ = q.shape
     heads_l = list(range(Hq)) if heads is None else list(heads)
     U = B * len(heads_l)
-    NB = N // 64
+    NB = (N + 63) // 64
     kb = min(topk, NB)
     dev = q.device
     ex = {

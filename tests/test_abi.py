@@ -67,7 +67,7 @@ def test_workspace_bytes(lib):
 
 
 @pytest.mark.parametrize("case,expect", [
-    ("null_q", 1), ("d64", 2), ("n100", 2), ("misaligned", 1), ("gqa", 1), ("kv0", 1),
+    ("null_q", 1), ("d64", 2), ("n_huge", 2), ("misaligned", 1), ("gqa", 1), ("kv0", 1),
     ("flags", 1), ("lastq", 1), ("head_range", 1), ("head_dup", 1), ("no_ws", 3),
     ("small_ws", 3), ("ws_align", 3), ("odd_stride", 1), ("n_mismatch", 1),
 ])
@@ -79,8 +79,9 @@ def test_vertical_slash_rejects(lib, case, expect):
         q = T(ptr=0)
     elif case == "d64":
         q, out = T(D=64), T(D=64)
-    elif case == "n100":
-        q, k, v, out = T(N=100), T(H=2, N=100), T(H=2, N=100), T(N=100)
+    elif case == "n_huge":
+        n = (1 << 21) + 64
+        q, k, v, out = T(N=n), T(H=2, N=n), T(H=2, N=n), T(N=n)
     elif case == "misaligned":
         k = T(H=2, ptr=0x10008)
     elif case == "gqa":
@@ -166,3 +167,22 @@ def test_kv_select_rejected_on_host(lib):
     # a valid selection block passes validation and then fails on the missing workspace
     assert status(lse=ok_buf, score=ok_buf, window=64, keep=ok_buf, keep_k=8) == \
         msa.MSA_ERR_WORKSPACE
+
+
+def test_binding_refuses_buffers_the_library_would_overrun():
+    """The Python binding checks every export / KV buffer before the call."""
+    import torch
+    from dynamic_sparse_attention_slash_gb300 import msa
+
+    class Q:  # only the shape is read
+        shape = (1, 4, 1000, 128)
+
+    with pytest.raises(ValueError):  # not written by a block-sparse call
+        msa._check_buffers(Q, msa.MSA_KIND_BLOCK_SPARSE, 8, 0, None,
+                           {"slash": torch.zeros(4, dtype=torch.int32)}, None)
+    with pytest.raises(ValueError):  # host memory
+        msa._check_buffers(Q, msa.MSA_KIND_VERTICAL_SLASH, 10, 10, None,
+                           {"vertical": torch.zeros(40, dtype=torch.int32)}, None)
+    with pytest.raises(ValueError):
+        msa._check_buffers(Q, msa.MSA_KIND_STREAMING, 0, 0, None, None,
+                           {"lse": torch.zeros(4000), "window": 1, "keep_k": 0})

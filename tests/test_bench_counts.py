@@ -8,7 +8,7 @@ from oracle import msa_oracle as O
 
 
 def dist_words(S, N):
-    NB = N // 64
+    NB = (N + 63) // 64
     words = np.zeros((NB + 32) // 32, dtype=np.int64)
     for o in S:
         for t in ([o // 64] + ([o // 64 + 1] if o % 64 else [])):
@@ -16,10 +16,11 @@ def dist_words(S, N):
     return words
 
 
-@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("seed", range(12))
 def test_vs_pairs_match_mask_popcount(seed):
     rng = np.random.default_rng(seed)
-    N = 64 * int(rng.integers(1, 24))
+    # half the cases end on a partial block
+    N = 64 * int(rng.integers(1, 24)) - (int(rng.integers(1, 64)) if seed % 2 else 0)
     S = np.sort(rng.choice(N, size=int(rng.integers(1, 10)), replace=False))
     V = np.sort(rng.choice(N, size=int(rng.integers(1, 30)), replace=False))
     act = O.vs_active_tiles(S, N)
@@ -37,6 +38,17 @@ def test_bs_and_st_pairs():
     assert bench.bs_pairs([len(s) for s in sel]) == O.nnz_from_blocks(sel, N)
     st = [O.streaming_blocks(m, 2, 3) for m in range(N // 64)]
     assert bench.st_pairs(N, 2, 3) == O.nnz_from_blocks(st, N)
+
+
+@pytest.mark.parametrize("N", [1, 70, 1000, 1217])
+def test_bs_and_st_pairs_at_ragged_length(N):
+    rng = np.random.default_rng(N)
+    q, k = rng.standard_normal((N, 128)), rng.standard_normal((N, 128))
+    sel, _ = O.block_sparse_blocks(q, k, 3)
+    assert bench.bs_pairs([len(s) for s in sel], N) == O.nnz_from_blocks(sel, N)
+    NB = (N + 63) // 64
+    st = [O.streaming_blocks(m, 1, 2) for m in range(NB)]
+    assert bench.st_pairs(N, 1, 2) == O.nnz_from_blocks(st, N)
 
 
 def test_measured_traffic_is_tied_to_kernel_source(monkeypatch):

@@ -119,7 +119,7 @@ def run_vs_kv(q, k, v, vertical_topk, slash, kv, heads=None):
 def test_block_sparse_kv_select(N, topk, window):
     q, k, v = qkv(1, 2, 2, N, 22, vs=False, bs=True)
     kv = msa.kv_select_buffers(q, window, 128)
-    NB = N // 64
+    NB = (N + 63) // 64
     ex = {"block_count": torch.empty(2, NB, dtype=torch.int32, device=q.device),
           "block_ids": torch.empty(2, NB, min(topk, NB), dtype=torch.int32, device=q.device)}
     msa.msa_block_sparse(q, k, v, topk, export=ex, kv_select=kv)
@@ -142,7 +142,7 @@ def test_streaming_kv_select(N, init, local, window):
     kv = msa.kv_select_buffers(q, window, 40)
     msa.msa_streaming(q, k, v, init, local, kv_select=kv)
     torch.cuda.synchronize()
-    NB = N // 64
+    NB = (N + 63) // 64
     sel = [O.streaming_blocks(m, init, local) for m in range(NB)]
     mask = O.block_mask_from_blocks(sel, N)
     for h in range(2):
@@ -160,7 +160,7 @@ def test_dense_window_score_matches_gpu_vertical_estimate():
     N = 4096
     q, k, v = qkv(1, 1, 1, N, 24)
     kv = msa.kv_select_buffers(q, 64, 0)
-    msa.msa_streaming(q, k, v, 0, N // 64, kv_select=kv)
+    msa.msa_streaming(q, k, v, 0, (N + 63) // 64, kv_select=kv)
     v_score = torch.empty(1, N, dtype=torch.float32, device=q.device)
     msa.msa_vertical_slash(q, k, v, 100, 100, export={"v_score": v_score})
     torch.cuda.synchronize()
@@ -195,7 +195,7 @@ def test_lse_only_leaves_outputs_unchanged():
     b = msa.msa_streaming(q, k, v, 1, 3)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
-    mask = O.block_mask_from_blocks([O.streaming_blocks(m, 1, 3) for m in range(N // 64)], N)
+    mask = O.block_mask_from_blocks([O.streaming_blocks(m, 1, 3) for m in range((N + 63) // 64)], N)
     lse = O.row_lse(P.to_np(q[0, 1]), P.to_np(k[0, 0]), np.arange(N), mask, 1 / math.sqrt(D))
     check_lse(P.to_np(kv["lse"][0, 1]), lse, "lse only")
 
@@ -214,7 +214,7 @@ def test_kv_select_full_size(name):
           "slash": torch.empty(U, min(w.slash, N), dtype=torch.int32, device=q.device)}
     msa.msa_vertical_slash(q, k, v, w.vertical_topk, w.slash, out, heads=heads["vs"], export=ex,
                            kv_select=kv)
-    NB = N // 64
+    NB = (N + 63) // 64
     Ub = len(heads["bs"])
     exb = {"block_count": torch.empty(Ub, NB, dtype=torch.int32, device=q.device),
            "block_ids": torch.empty(Ub, NB, min(w.block_topk, NB), dtype=torch.int32,

@@ -32,7 +32,7 @@ def np64(t):
 @pytest.mark.parametrize("N,Hq,Hkv", [(640, 2, 1), (1024, 4, 2), (64, 1, 1)])
 def test_streaming_full_window_is_dense_causal(N, Hq, Hkv):
     q, k, v = qkv(1, Hq, Hkv, N, 11)
-    out = msa.msa_streaming(q, k, v, 0, N // 64)
+    out = msa.msa_streaming(q, k, v, 0, (N + 63) // 64)
     torch.cuda.synchronize()
     qn, kn, vn = np64(q), np64(k), np64(v)
     for h in range(Hq):
@@ -67,7 +67,7 @@ def test_block_sparse_matches_oracle(N, topk):
     q, k, v = qkv(1, 4, 2, N, 14, vs=False, bs=True)
     out, ex = P.run_bs(q, k, v, topk)
     qn, kn, vn = np64(q), np64(k), np64(v)
-    NB = N // 64
+    NB = (N + 63) // 64
     for h in range(4):
         g = h // 2
         sel, S = O.block_sparse_blocks(qn[0, h], kn[0, g], topk)
@@ -93,7 +93,7 @@ def check_vs_case(q, k, v, vertical_topk, slash, last_q=64, heads=None):
     heads_l = list(range(Hq)) if heads is None else list(heads)
     qn, kn, vn = np64(q), np64(k), np64(v)
     scale = 1 / math.sqrt(D)
-    NB = N // 64
+    NB = (N + 63) // 64
     for b in range(B):
         for t, h in enumerate(heads_l):
             u = b * len(heads_l) + t

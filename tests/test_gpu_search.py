@@ -35,7 +35,7 @@ def test_search_matches_oracle():
     budget = 0.25 * 4 * D * N * (N + 1) / 2
     res = search.search(q, k, v, cands, budget)
     scale = 1 / math.sqrt(D)
-    NB = N // 64
+    NB = (N + 63) // 64
     qn, kn = q[0].double().cpu().numpy(), k[0].double().cpu().numpy()
     # the GPU's index sets per candidate, for the oracle's masks
     for h in range(Hq):
@@ -87,7 +87,7 @@ def test_mass_recall_dense_is_one_and_subset_heads():
     q, k, v = inputs.make_qkv(2, 4, 2, N, 32, vs_planting=True, device="cpu")
     q, k, v = q.cuda(), k.cuda(), v.cuda()
     ref = {"lse": torch.zeros(2, 4, N, device="cuda"), "window": 0, "keep_k": 0}
-    msa.msa_streaming(q, k, v, 0, N // 64, kv_select=ref)
+    msa.msa_streaming(q, k, v, 0, (N + 63) // 64, kv_select=ref)
     recall = torch.full((2, 4), 9.0, device="cuda")
     msa.mass_recall(ref["lse"], ref["lse"], recall, heads=[2, 0])
     torch.cuda.synchronize()
@@ -100,7 +100,7 @@ def test_mass_recall_dense_is_one_and_subset_heads():
     msa.mass_recall(cur["lse"], ref["lse"], recall, row0=N - 64)
     torch.cuda.synchronize()
     qn, kn = q.double().cpu().numpy(), k.double().cpu().numpy()
-    mask = O.block_mask_from_blocks([O.streaming_blocks(m, 0, 2) for m in range(N // 64)], N)
+    mask = O.block_mask_from_blocks([O.streaming_blocks(m, 0, 2) for m in range((N + 63) // 64)], N)
     for b in range(2):
         for h in range(4):
             ref_r = O.mass_recall(qn[b, h], kn[b, h // 2], np.arange(N - 64, N), mask,

@@ -32,12 +32,12 @@ def run_step(w, q, k, v, heads):
             "s_score": torch.empty(U, N, dtype=torch.float32, device=q.device),
             "vertical": torch.empty(U, min(w.vertical_topk, N), dtype=torch.int32, device=q.device),
             "slash": torch.empty(U, min(w.slash, N), dtype=torch.int32, device=q.device),
-            "tile_dist": torch.empty(U, (N // 64 + 32) // 32, dtype=torch.int32, device=q.device)}
+            "tile_dist": torch.empty(U, ((N + 63) // 64 + 32) // 32, dtype=torch.int32, device=q.device)}
         msa.msa_vertical_slash(q, k, v, w.vertical_topk, w.slash, out, last_q=w.last_q,
                                heads=heads["vs"], export=ex["vs"])
     if heads["bs"]:
         U = B * len(heads["bs"])
-        NB = N // 64
+        NB = (N + 63) // 64
         ex["bs"] = {"block_count": torch.empty(U, NB, dtype=torch.int32, device=q.device),
                     "block_ids": torch.empty(U, NB, min(w.block_topk, NB), dtype=torch.int32,
                                              device=q.device)}
@@ -84,7 +84,7 @@ def test_workload_full_size(name):
                 near_ties += P.check_topk(e["slash"][u], ss_, w.slash, f"{name} h{h} slash")
                 S, V = e["slash"][u].astype(np.int64), e["vertical"][u].astype(np.int64)
                 blocks = sorted({i // 64 for i in rows})
-                bits = P.dist_bits_to_active(e["tile_dist"][u], N // 64) if N <= 131072 else None
+                bits = P.dist_bits_to_active(e["tile_dist"][u], (N + 63) // 64) if N <= 131072 else None
                 ref_act = O.vs_active_tiles(S, N, blocks)
                 words = np.asarray(e["tile_dist"][u], dtype=np.int64) & 0xFFFFFFFF
                 for r, m in enumerate(blocks):
@@ -101,7 +101,7 @@ def test_workload_full_size(name):
                 qn = P.to_np(q[0, h])
                 sel_ref, Sc = O.block_sparse_blocks(qn, kn, w.block_topk, scale)
                 sel = []
-                for m in range(N // 64):
+                for m in range((N + 63) // 64):
                     cnt = int(e["block_count"][u, m])
                     assert cnt == min(w.block_topk, m + 1)
                     got = e["block_ids"][u, m, :cnt].astype(np.int64)
@@ -112,7 +112,7 @@ def test_workload_full_size(name):
                     sel.append(got)
                 mask = O.block_mask_from_blocks(sel, N)
             else:
-                sel = [O.streaming_blocks(m, w.init_num, w.local_window_num) for m in range(N // 64)]
+                sel = [O.streaming_blocks(m, w.init_num, w.local_window_num) for m in range((N + 63) // 64)]
                 mask = O.block_mask_from_blocks(sel, N)
             ref, counts = O.attend_rows(qn, kn, vn, rows, lambda i: mask(i // 64), scale)
             assert (counts > 0).all(), "no sampled row may be empty under the planted inputs"
