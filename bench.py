@@ -258,7 +258,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="mixed_128k", choices=sorted(inputs.WORKLOADS))
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-rows", type=int, default=48, help="oracle rows per head (cpu_baseline)")
     ap.add_argument("--ref-rows", type=int, default=24, help="oracle rows per head (reference arm)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -396,33 +396,32 @@ def main():
                 "peak_source": peak_src,
                 "frac_of_burst": achieved / float(peaks.get("bf16_tflops", 1900.0))}
 
-    # ---- end to end: pinned host inputs, copies inside the timed region
+    # ---- end to end: pinned host inputs and outputs, every copy inside the timed
+    # region, through the package's host pipeline (pipeline.run_pipelined: inputs
+    # and outputs double-buffered, copies on two side streams while steps compute)
     e2e = None
     if args.e2e_steps > 0:
+        from dynamic_sparse_attention_slash_gb300.pipeline import run_pipelined
+        S = args.e2e_steps
         qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
-        oh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-        qd, kd, vd, od = (torch.empty_like(t) for t in (q, k, v, out))
-        od.zero_()
+        oh = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
         barrier(world)
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.e2e_steps):
-            qd.copy_(qh, non_blocking=True)
-            kd.copy_(kh, non_blocking=True)
-            vd.copy_(vh, non_blocking=True)
-            step(qq=qd, kk=kd, vv=vd, oo=od)
-            oh.copy_(od, non_blocking=True)
-        e1.record(stream)
+        evs = run_pipelined(lambda qq, kk, vv, oo: step(qq=qq, kk=kk, vv=vv, oo=oo),
+                            [(qh, kh, vh)] * S, [oh[i % 2] for i in range(S)], stream=stream,
+                            device=dev)
         torch.cuda.synchronize()
         barrier(world)
-        e_ms = max_over_ranks(e0.elapsed_time(e1), world)
-        e_val = sum_over_ranks(step_flops * args.e2e_steps, world) / (e_ms * 1e-3) / 1e12
+        e_ms = max_over_ranks(evs["start"].elapsed_time(evs["end"]), world)
+        compute_ms = sum(a_.elapsed_time(b_) for a_, b_ in evs["compute"]) / S
+        e_val = sum_over_ranks(step_flops * S, world) / (e_ms * 1e-3) / 1e12
         h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
         e2e = {"value": e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": oh.numel() * oh.element_size(),
-               "ms_per_step": e_ms / args.e2e_steps}
-        del qh, kh, vh, oh, qd, kd, vd, od
+               "d2h_bytes_per_step": oh[0].numel() * oh[0].element_size(),
+               "ms_per_step": e_ms / S, "compute_ms_per_step": compute_ms, "steps": S,
+               "pipelined": "pipeline.run_pipelined: double-buffered inputs/outputs, "
+                            "copies on two side streams"}
+        del qh, kh, vh, oh, evs
 
     # ---- dense causal attention on the same GPU (context)
     dense = None
