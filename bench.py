@@ -46,13 +46,14 @@ UNIT = "TFLOP/s"
 # dram__bytes_read.sum + dram__bytes_write.sum of the vertical-slash prefill
 # launch of the mixed 128K step, from one ncu capture (one pass, full size;
 # profiles/sparse_prefill_dram_mixed_128k.md).  The figure belongs to the kernel
-# source it was taken on: once either file changes, the bench reports null
+# source it was taken on: once any of its files changes, the bench reports null
 # until it is measured again.
 MEASURED_TRAFFIC = {
     "workload": "mixed_128k",
     "kind": "vs",
     "bytes": 2.53e9 + 0.654e9,
     "sources": ("dynamic_sparse_attention_slash_gb300/csrc/prefill.cu",
+                "dynamic_sparse_attention_slash_gb300/csrc/prefill_common.cuh",
                 "dynamic_sparse_attention_slash_gb300/csrc/sm103_ptx.cuh"),
     "sha256": "d941acb562cbaa8ab9b6ab4b3cc0728cf5f306cad4dbf12bc1b6aaa4bc0ccd23",
 }

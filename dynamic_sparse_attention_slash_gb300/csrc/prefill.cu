@@ -17,7 +17,8 @@
 // The item list is the union of the two query tiles' lists; a tile that does
 // not use an item sees it fully masked.  (Skipping such items per tile was
 // measured slower on GB300: it lengthens the single MMA thread's issue path,
-// which the tensor core waits on.)
+// which the tensor core waits on.)  Block-sparse heads, whose per-tile lists
+// are short and sparse, run the one-tile kernel of prefill_tile.cu instead.
 //
 // Warp roles (384 threads; the control warpgroup gives registers to the two
 // softmax warpgroups with setmaxnreg):
@@ -41,18 +42,16 @@
 // core works on the other tile.  Every mbarrier wait is bounded (see
 // sm103_ptx.cuh); a timeout sets the status word and the CTA drains its copies
 // and MMAs and exits.
-#include "msa_internal.h"
-#include "sm103_ptx.cuh"
+#include "prefill_common.cuh"
 
 namespace msa {
 namespace {
 
+using namespace prefill;
+
 constexpr int kThreads = 384;
 constexpr int kStagesK = 3;
 constexpr int kStagesV = 2;
-constexpr int kTileBytes = 128 * 128 * 2;  // one 128 x 128 16-bit tile (two 64-column halves)
-constexpr int kHalfBytes = kTileBytes / 2;
-constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O when the max grows by > 2^8
 // TMEM columns: S/P of tile t at kColS + 128 t, O of tile t at kColO + 128 t
 constexpr uint32_t kColS = 0, kColO = 256;
 // Register split: the control warpgroup drops to kCtrlRegs, the two softmax
@@ -86,28 +85,6 @@ __device__ __forceinline__ void setmaxnreg_inc() {
 }
 __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
-}
-
-__device__ __forceinline__ int unit_batch(const PrefillParams& P, int unit) {
-  return unit / P.units.n_heads;
-}
-__device__ __forceinline__ int unit_head(const PrefillParams& P, int unit) {
-  return P.units.heads[unit % P.units.n_heads];
-}
-
-__device__ __forceinline__ bool dist_bit(const uint32_t* dist, int t) {
-  return t >= 0 && ((dist[t >> 5] >> (t & 31)) & 1u);
-}
-
-// Number of union distances <= pB (the pair list is ascending).
-__device__ __forceinline__ int vs_tiles_upto(const PrefillParams& P, int unit, int pB) {
-  const int32_t* qd = P.qdelta + static_cast<int64_t>(unit) * (P.g.NQ + 1);  // (D << 5) | bits
-  int lo = 0, hi = P.qdelta_count[unit];
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if ((qd[mid] >> 5) <= pB) lo = mid + 1; else hi = mid;
-  }
-  return lo;
 }
 
 // Column-chunk word x of the pair: chunks needed by query tile pA or pB.
@@ -157,21 +134,6 @@ __device__ __forceinline__ int n_items(const PrefillParams& P, int unit, int c, 
   int sink_hi, loc_lo;
   st_ranges(P, pA, sink_hi, loc_lo);
   return sink_hi + (pair_qmax(P, pA) - loc_lo + 1);
-}
-
-// Quadrant mask of key tile q for query tile p (bit a*2 + b), streaming head.
-__device__ __forceinline__ uint32_t quad_mask_st(const PrefillParams& P, int p, int q) {
-  uint32_t mask = 0;
-#pragma unroll
-  for (int a = 0; a < 2; ++a) {
-#pragma unroll
-    for (int b = 0; b < 2; ++b) {
-      const int m = 2 * p + a, n = 2 * q + b;
-      if (m < P.g.NB && n <= m && (n < P.init_num || n >= m - P.local_num + 1))
-        mask |= 1u << (a * 2 + b);
-    }
-  }
-  return mask;
 }
 
 // Item i of pair c.  Vertical-slash: column chunks first (ascending), then key
@@ -228,11 +190,6 @@ __device__ __forceinline__ Item get_item(const PrefillParams& P, int unit, int c
     it.qmask[1] = quad_mask_st(P, pB, it.idx);
   }
   return it;
-}
-
-__device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity) {
-  int never = 0;
-  return mbar_wait(bar, parity, &never);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -622,6 +579,11 @@ cudaError_t launch_v_to_f16(TensorView v, int B, int Hkv, int N, __half* dst, ui
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                            const CUtensorMap& mv, const CUtensorMap& mkc, const CUtensorMap& mvc,
                            cudaStream_t st, int* n_launch) {
+  // Block-sparse heads run the one-tile kernel (prefill_tile.cu): their short,
+  // sparse per-tile item lists favour skipping items per query tile and a
+  // shorter softmax chain; the two-tile kernel keeps the tensor core busier on
+  // the long lists of vertical-slash and streaming heads.
+  if (p.kind == kPrefillBS) return launch_prefill_tile(p, mq, mk, mv, mkc, mvc, st, n_launch);
   // The register split above needs the launch to provide kMinLaunchRegs per
   // thread; refuse to launch (rather than wait forever) if the build differs.
   static int launch_regs = -1;

@@ -1,0 +1,565 @@
+// Sparse prefill attention (MInference 1.0 overview, section 2.2: "block-sparse
+// computation of the attention weights and output" over the sparse index, shared
+// by the vertical-slash, block-sparse and streaming heads), with the one-pass
+// online softmax of FlashAttention-2 (the Novita vLLM article, "Attention
+// modification", Fig. 7: keep a running row max and row sum, rescale the output,
+// divide by the row sum at the end).
+//
+// This kernel serves the block-sparse heads: one CTA computes one 128-row
+// query tile p of one (batch, head) unit (row blocks 2p and 2p + 1).  It walks
+// the pair lists of prefill.cu's index structures but keeps only the entries
+// whose quadrant mask is non-empty for its own tile, so a tile never loads or
+// multiplies a key tile only its neighbour needs.  Work items are 128 keys wide:
+//   * a key tile q: keys [128q, 128q+128) of the KV head, with a 4-bit quadrant
+//     mask (bit a*2+b: row half a may see key half b) and the causal cut on the
+//     tile's diagonal;
+//   * a column chunk c (vertical-slash only): gathered K/V rows of chosen keys
+//     [128c, 128c+128) of the unit's ascending vertical list, each admitted for
+//     a row iff the key is <= the row and outside the row block's active tiles.
+// (The kernel runs every head kind; the library routes only block-sparse heads
+// here.)
+//
+// Warp roles (384 threads):
+//   warp 0     TMA producer for Q and K (one thread)
+//   warp 1     TMEM allocator and tcgen05.mma issuer (one thread)
+//   warp 2     TMA producer for V (one thread)
+//   warp 3     idle
+//   warps 4-11 softmax: warps 4 + w and 8 + w own query rows 32w .. 32w + 31
+//              (TMEM lanes) and split each row's 128 keys into two halves; the
+//              halves exchange their maxima once per item through shared
+//              memory, run the online softmax in fp32 (exp2 with log2(e) folded
+//              into the scale), write P as f16 back over S, rescale their half
+//              of O in TMEM when the row max grows by more than 2^8, and write
+//              their half of the output row.
+//
+// TMEM (512 columns allocated): two S/P buffers at [0,128) and [128,256) for
+// even and odd items, the output accumulator O at [256,384).  S = Q K^T reads Q
+// and K from 128B-swizzled shared memory (K-major); O += P V reads P from TMEM
+// and V from shared memory (MN-major).  The MMA issue order is S(0), S(1),
+// PV(0), S(2), PV(1), ...: the tensor core computes S(i+1) while the softmax
+// works on S(i).  Every mbarrier wait is bounded (see sm103_ptx.cuh); a timeout
+// sets the status word and the CTA drains its copies and MMAs and exits.  The
+// named barriers between the two warps of a row group are reached by both on
+// every path (every wait before them is bounded and both leave together).
+#include "prefill_common.cuh"
+
+namespace msa {
+namespace {
+
+using namespace prefill;
+
+constexpr int kThreads = 384;
+constexpr int kStagesK = 3;
+constexpr int kStagesV = 2;
+// TMEM columns: S/P of item i at kColS + 128 (i & 1), O at kColO
+constexpr uint32_t kColS = 0, kColO = 256;
+
+struct __align__(1024) TileSmem {
+  uint8_t q[kTileBytes];
+  uint8_t k[kStagesK][kTileBytes];
+  uint8_t v[kStagesV][kTileBytes];
+  uint64_t q_full;
+  uint64_t k_full[kStagesK], k_empty[kStagesK];
+  uint64_t v_full[kStagesV], v_empty[kStagesV];
+  uint64_t s_full[2], p_full[2];
+  uint64_t final_bar;
+  float xmax[2][2][128];  // half-row maxima [item parity][column half][row]
+  float xsum[2][128];     // half-row sums at the end
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct Item {
+  bool cols;    // column chunk (true) or key tile (false)
+  int idx;      // key tile q or chunk c
+  uint32_t qm;  // quadrant mask of a key tile for this query tile (bit a*2 + b)
+};
+
+// The query tile of a CTA and the slots its items are drawn from.  The index
+// structures describe pairs of query tiles (2c, 2c + 1); a tile takes the
+// pair's entries whose quadrant mask for it is not empty.
+struct Tile {
+  int unit, p, t, pB;    // tile p = 2c + t, pB = 2c + 1
+  int n_chunk_slots;     // vertical-slash: 32 * chunk_words column-chunk slots first
+  int n_slots;
+  int n_hi;              // vertical-slash: pair distances <= pB
+  int sink_hi, loc_lo;   // streaming: key tiles [0, sink_hi) and [loc_lo, p]
+};
+
+__device__ __forceinline__ Tile make_tile(const PrefillParams& P, int unit, int p) {
+  Tile T;
+  T.unit = unit;
+  T.p = p;
+  T.t = p & 1;
+  T.pB = p | 1;
+  T.n_chunk_slots = 0;
+  T.n_hi = 0;
+  T.sink_hi = 0;
+  T.loc_lo = 0;
+  if (P.kind == kPrefillVS) {
+    T.n_chunk_slots = 32 * P.chunk_words;
+    T.n_hi = vs_tiles_upto(P, unit, T.pB);
+    T.n_slots = T.n_chunk_slots + T.n_hi;
+  } else if (P.kind == kPrefillBS) {
+    T.n_slots = P.bs_tile_count[static_cast<int64_t>(unit) * P.npair + (p >> 1)];
+  } else {
+    T.sink_hi = min((P.init_num + 1) >> 1, p + 1);
+    T.loc_lo = max(0, 2 * p - P.local_num + 1) >> 1;
+    if (T.sink_hi >= T.loc_lo) {  // the two ranges meet: one range [0, p]
+      T.sink_hi = 0;
+      T.loc_lo = 0;
+    }
+    T.n_slots = T.sink_hi + (p - T.loc_lo + 1);
+  }
+  return T;
+}
+
+// Vertical-slash pair entry (D << 5) | bits: key tile pB - D; quadrant (a, b)
+// sits at 64-block distance 2D + a - b for tile pB (bit a - b + 3) and
+// 2D - 2 + a - b for tile pA (bit a - b + 1).  Row blocks past the sequence
+// take nothing.
+__device__ __forceinline__ uint32_t vs_qmask(const PrefillParams& P, const Tile& T, int32_t e) {
+  const int sh = T.t ? 3 : 1;
+  uint32_t m = 0;
+#pragma unroll
+  for (int a = 0; a < 2; ++a) {
+#pragma unroll
+    for (int b = 0; b < 2; ++b)
+      if (2 * T.p + a < P.g.NB) m |= ((e >> (a - b + sh)) & 1u) << (a * 2 + b);
+  }
+  return m;
+}
+
+__device__ __forceinline__ uint32_t bs_qmask(const Tile& T, int32_t e) {
+  return static_cast<uint32_t>(T.t ? (e >> 4) & 15 : e & 15);
+}
+
+__device__ __forceinline__ int st_key(const Tile& T, int s) {
+  return s < T.sink_hi ? s : T.loc_lo + (s - T.sink_hi);
+}
+
+// Items of the tile (warp-collective: every lane returns the count).
+__device__ int count_items(const PrefillParams& P, const Tile& T, int lane) {
+  int cnt = 0;
+  if (P.kind == kPrefillVS) {
+    const uint32_t* w = P.col_chunks + (static_cast<int64_t>(T.unit) * P.g.NQ + T.p) * P.chunk_words;
+    for (int x = lane; x < P.chunk_words; x += 32) cnt += __popc(w[x]);
+    const int32_t* qd = P.qdelta + static_cast<int64_t>(T.unit) * (P.g.NQ + 1);
+    for (int j = lane; j < T.n_hi; j += 32) cnt += vs_qmask(P, T, qd[j]) != 0u ? 1 : 0;
+  } else if (P.kind == kPrefillBS) {
+    const int32_t* L = P.bs_tiles + (static_cast<int64_t>(T.unit) * P.npair + (T.p >> 1)) * P.bs_tile_cap;
+    for (int j = lane; j < T.n_slots; j += 32) cnt += bs_qmask(T, L[j]) != 0u ? 1 : 0;
+  } else {
+    for (int s = lane; s < T.n_slots; s += 32) cnt += quad_mask_st(P, T.p, st_key(T, s)) != 0u ? 1 : 0;
+  }
+  return __reduce_add_sync(0xffffffffu, cnt);
+}
+
+// The next item at or after slot s (s moves past it); false when none is left.
+// Vertical-slash: column chunks ascending, then key tiles ascending (largest
+// pair distance first).
+__device__ __forceinline__ bool next_item(const PrefillParams& P, const Tile& T, int& s, Item& it) {
+  if (P.kind == kPrefillVS) {
+    if (s < T.n_chunk_slots) {
+      const uint32_t* w = P.col_chunks + (static_cast<int64_t>(T.unit) * P.g.NQ + T.p) * P.chunk_words;
+      while (s < T.n_chunk_slots) {
+        const uint32_t word = w[s >> 5] >> (s & 31);
+        if (word == 0u) {
+          s = (s | 31) + 1;
+          continue;
+        }
+        s += __ffs(static_cast<int>(word)) - 1;
+        it.cols = true;
+        it.idx = s++;
+        it.qm = 0xFu;
+        return true;
+      }
+    }
+    const int32_t* qd = P.qdelta + static_cast<int64_t>(T.unit) * (P.g.NQ + 1);
+    while (s < T.n_slots) {
+      const int32_t e = qd[T.n_hi - 1 - (s - T.n_chunk_slots)];
+      ++s;
+      const uint32_t m = vs_qmask(P, T, e);
+      if (m) {
+        it.cols = false;
+        it.idx = T.pB - (e >> 5);
+        it.qm = m;
+        return true;
+      }
+    }
+    return false;
+  }
+  if (P.kind == kPrefillBS) {
+    const int32_t* L = P.bs_tiles + (static_cast<int64_t>(T.unit) * P.npair + (T.p >> 1)) * P.bs_tile_cap;
+    while (s < T.n_slots) {
+      const int32_t e = L[s++];
+      const uint32_t m = bs_qmask(T, e);
+      if (m) {
+        it.cols = false;
+        it.idx = e >> 8;
+        it.qm = m;
+        return true;
+      }
+    }
+    return false;
+  }
+  while (s < T.n_slots) {
+    const int q = st_key(T, s++);
+    const uint32_t m = quad_mask_st(P, T.p, q);
+    if (m) {
+      it.cols = false;
+      it.idx = q;
+      it.qm = m;
+      return true;
+    }
+  }
+  return false;
+}
+
+// TMA of item it's K (or V) tile into dst, completion on bar.
+__device__ __forceinline__ void load_item(const PrefillParams& P, const Item& it, uint8_t* dst,
+                                          const CUtensorMap* map, const CUtensorMap* map_cols,
+                                          uint64_t* bar, int unit, int hkv, int b) {
+  mbar_arrive_expect_tx(bar, kTileBytes);
+  if (it.cols) {
+    const int row = unit * P.kv_pad + 128 * it.idx;
+    tma_load_2d(dst, map_cols, bar, 0, row);
+    tma_load_2d(dst + kHalfBytes, map_cols, bar, 64, row);
+  } else {
+    tma_load_4d(dst, map, bar, 0, 128 * it.idx, hkv, b);
+    tma_load_4d(dst + kHalfBytes, map, bar, 64, 128 * it.idx, hkv, b);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ CUtensorMap mq,
+                      const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+                      const __grid_constant__ CUtensorMap mkc,
+                      const __grid_constant__ CUtensorMap mvc) {
+  extern __shared__ uint8_t smem_raw[];
+  TileSmem& sm = *reinterpret_cast<TileSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                      ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int unit = blockIdx.y;
+  const int p = P.g.NQ - 1 - static_cast<int>(blockIdx.x);  // heavy (late) tiles first
+  const Tile T = make_tile(P, unit, p);
+  const int b = unit_batch(P, unit), h = unit_head(P, unit), hkv = h / P.g.G;
+  volatile int* abort = &sm.abort;
+
+  if (tid == 0) {
+    mbar_init(&sm.q_full, 1);
+    for (int s = 0; s < kStagesK; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.k_empty[s], 1);
+    }
+    for (int s = 0; s < kStagesV; ++s) {
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.v_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&sm.s_full[t], 1);
+      mbar_init(&sm.p_full[t], 8);  // one arrival per softmax warp
+    }
+    mbar_init(&sm.final_bar, 1);
+    sm.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ Q + K producer
+    if (lane == 0) {
+      tma_prefetch_desc(&mq);
+      tma_prefetch_desc(&mk);
+      mbar_arrive_expect_tx(&sm.q_full, kTileBytes);
+      tma_load_4d(sm.q, &mq, &sm.q_full, 0, 128 * p, h, b);
+      tma_load_4d(sm.q + kHalfBytes, &mq, &sm.q_full, 64, 128 * p, h, b);
+      int issued = 0, s = 0;
+      Item it;
+      for (int i = 0; next_item(P, T, s, it); ++i) {
+        const int st = i % kStagesK;
+        if (!mbar_wait(&sm.k_empty[st], ((i / kStagesK) & 1) ^ 1, abort)) break;
+        load_item(P, it, sm.k[st], &mk, &mkc, &sm.k_full[st], unit, hkv, b);
+        issued = i + 1;
+      }
+      // drain: the latest load of every stage, and Q, must land before exit
+      wait_drain(&sm.q_full, 0);
+      for (int i = max(0, issued - kStagesK); i < issued; ++i)
+        wait_drain(&sm.k_full[i % kStagesK], (i / kStagesK) & 1);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ V producer
+    if (lane == 0) {
+      tma_prefetch_desc(&mv);
+      int issued = 0, s = 0;
+      Item it;
+      for (int i = 0; next_item(P, T, s, it); ++i) {
+        const int st = i % kStagesV;
+        if (!mbar_wait(&sm.v_empty[st], ((i / kStagesV) & 1) ^ 1, abort)) break;
+        load_item(P, it, sm.v[st], &mv, &mvc, &sm.v_full[st], unit, hkv, b);
+        issued = i + 1;
+      }
+      for (int i = max(0, issued - kStagesV); i < issued; ++i)
+        wait_drain(&sm.v_full[i % kStagesV], (i / kStagesV) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    const int n = count_items(P, T, lane);
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idO = idesc_f32acc(128, 128, /*bf16=*/false, false, true);  // f16 P, f16 V
+      bool ok = n == 0 || mbar_wait(&sm.q_full, 0, abort);
+      tc_fence_after();
+      // Operand descriptors are built once; a K-step only adds a constant to the
+      // start-address field (16-byte units), which cannot carry out of it.
+      const uint64_t q_desc = sdesc_sw128(smem_u32(sm.q), 16, 1024);
+      const uint64_t k_desc0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
+      const uint64_t v_desc0 = sdesc_sw128(smem_u32(sm.v[0]), kHalfBytes, 1024);
+      constexpr uint64_t kStageStep = kTileBytes >> 4;
+      // S(i) = Q K(i)^T into S buffer i & 1; its completion releases the K stage
+      auto issue_s = [&](int i) -> bool {
+        const int sk = i % kStagesK;
+        if (!mbar_wait(&sm.k_full[sk], (i / kStagesK) & 1, abort)) return false;
+        tc_fence_after();
+        const uint64_t kd = k_desc0 + sk * kStageStep;
+        const uint32_t s_tm = tmem + kColS + 128 * (i & 1);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+          mma_ss(s_tm, q_desc + off, kd + off, idS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&sm.s_full[i & 1]);
+        mma_commit(&sm.k_empty[sk]);
+        return true;
+      };
+      // O += P(i) V(i); its completion releases the V stage (and tells the
+      // softmax that O holds items 0..i)
+      auto issue_pv = [&](int i) -> bool {
+        const int sv = i % kStagesV;
+        if (!mbar_wait(&sm.v_full[sv], (i / kStagesV) & 1, abort)) return false;
+        if (!mbar_wait(&sm.p_full[i & 1], (i >> 1) & 1, abort)) return false;
+        tc_fence_after();
+        const uint64_t vd = v_desc0 + sv * kStageStep;
+        const uint32_t p_tm = tmem + kColS + 128 * (i & 1);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + kColO, p_tm + kk * 8, vd + ((kk * 2048) >> 4), idO,
+                 (i > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&sm.v_empty[sv]);
+        return true;
+      };
+      // S(i + 1) is computed while the softmax works on S(i)
+      if (ok && n > 0) ok = issue_s(0);
+      for (int i = 0; ok && i < n; ++i) {
+        if (i + 1 < n && !issue_s(i + 1)) ok = false;
+        else if (!issue_pv(i)) ok = false;
+      }
+      // every MMA issued above must complete before TMEM is released
+      mma_commit(&sm.final_bar);
+      wait_drain(&sm.final_bar, 0);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    // Warps 4 + w and 8 + w share TMEM lanes 32w .. 32w + 31 (query rows) and
+    // split the columns: warpgroup g takes keys [64g, 64g + 64) of each item and
+    // output dimensions [64g, 64g + 64).  The two halves of a row exchange their
+    // maxima through shared memory once per item, so both keep the same
+    // running max; their row sums are added at the end.
+    const int g = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;        // query row within the tile == TMEM lane
+    const uint32_t pair_bar = 1 + quarter;    // named barrier of the two warps of these rows
+    const int half = r >> 6;                  // row block 2p + half
+    const int row = 128 * p + r;              // query index i
+    const int mblk = 2 * p + half;
+    const uint32_t* dist = P.kind == kPrefillVS
+                               ? P.tile_dist + static_cast<int64_t>(unit) * P.dist_words
+                               : nullptr;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t o_col = lane_base + kColO + 64 * g;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    int k = 0;  // items processed so far
+    int slot = 0;
+    Item it;
+    while (next_item(P, T, slot, it)) {
+      const uint32_t s_col = lane_base + kColS + 128 * (k & 1);
+      // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
+      const bool waited = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[k & 1], (k >> 1) & 1, abort));
+      tc_fence_after();
+      // raw logits (unscaled) of this row's half; scale * log2(e) is folded in below
+      float x[64];
+      {
+        uint32_t raw[64];
+        tmem_ld64(s_col + 64 * g, raw);
+#pragma unroll
+        for (int e = 0; e < 64; ++e) x[e] = __uint_as_float(raw[e]);
+      }
+      // ---- mask
+      if (it.cols) {
+        const int base = 128 * it.idx + 64 * g;
+        const int32_t* V = P.vertical + static_cast<int64_t>(unit) * P.kv + base;
+        const int valid = P.kv - base;
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+          bool keep = false;
+          if (e < valid) {
+            const int j = V[e];
+            keep = j <= row && !dist_bit(dist, mblk - (j >> 6));
+          }
+          if (!keep) x[e] = -INFINITY;
+        }
+      } else {
+        const bool in_q = (it.qm >> (half * 2 + g)) & 1u;
+        if (!in_q) {
+#pragma unroll
+          for (int e = 0; e < 64; ++e) x[e] = -INFINITY;
+        } else if (it.idx == p) {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (64 * g + e > r) x[e] = -INFINITY;
+        }
+      }
+      // ---- online softmax (8 independent chains of 3-input max, paired sums)
+      float mx8[8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) {
+        float m = fmax3(x[a], x[8 + a], x[16 + a]);
+#pragma unroll
+        for (int e = 24; e < 56; e += 16) m = fmax3(m, x[e + a], x[e + 8 + a]);
+        mx8[a] = fmaxf(m, x[56 + a]);
+      }
+      const float mxh = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                              fmaxf(mx8[6], mx8[7]));
+      sm.xmax[k & 1][g][r] = mxh;
+      // both warps pass this barrier on every item (every wait above is bounded),
+      // and leave together when either one's wait failed
+      if (!bar_red_and(pair_bar, 64, waited)) {
+        ok = false;
+        break;
+      }
+      const float mx = fmaxf(mxh, sm.xmax[k & 1][g ^ 1][r]);
+      const float m_new = fmaxf(m_run, mx * P.scale_log2);
+      const bool grow = m_new > m_run + kRescaleThreshold;  // false when both are -inf
+      const float m_use = grow ? m_new : m_run;
+      const float neg_base = m_use == -INFINITY ? 0.f : -m_use;
+      const float2 scale2 = make_float2(P.scale_log2, P.scale_log2);
+      const float2 nb2 = make_float2(neg_base, neg_base);
+      float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                       make_float2(0.f, 0.f)};
+      uint32_t pk[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const float2 a = ffma2(make_float2(x[2 * e], x[2 * e + 1]), scale2, nb2);
+        const float2 pe = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+        rs2[e & 3] = fadd2(rs2[e & 3], pe);
+        pk[e] = pack_f16x2(pe.x, pe.y);
+      }
+      const float2 rsa = fadd2(fadd2(rs2[0], rs2[1]), fadd2(rs2[2], rs2[3]));
+      const float rs = rsa.x + rsa.y;
+      const bool correct = grow && m_run != -INFINITY;  // O holds earlier items' weight
+      const float alpha = correct ? ex2_approx(m_run - m_new) : 1.f;
+      l_run = (m_run == -INFINITY ? 0.f : l_run * alpha) + rs;
+      m_run = m_use;
+      // both warps of these rows take this branch together (same maxima)
+      if (__any_sync(0xffffffffu, correct)) {
+        // O must hold P(k-1) V(k-1) before it is rescaled: that product's
+        // completion released its V stage
+        const int j = k - 1;
+        const bool got = __all_sync(
+            0xffffffffu, mbar_wait(&sm.v_empty[j % kStagesV], (j / kStagesV) & 1, abort));
+        if (!bar_red_and(pair_bar, 64, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+          uint32_t o[32];
+          tmem_ld32(o_col + 32 * q2, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(o_col + 32 * q2, o);
+        }
+      }
+      tmem_st32(s_col + 32 * g, pk);  // f16 pairs of keys [64g, 64g + 64)
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.p_full[k & 1]);
+      ++k;
+    }
+    // ---- epilogue: add the two halves' row sums (both warps arrive here)
+    sm.xsum[g][r] = l_run;
+    ok = bar_red_and(pair_bar, 64, ok);
+    const float l_row = l_run + sm.xsum[g ^ 1][r];
+    uint4 outv[8];
+    const bool have = ok && k > 0 && l_row > 0.f;
+    if (ok && k > 0) {
+      const int j = k - 1;  // the last product's completion released its V stage
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.v_empty[j % kStagesV], (j / kStagesV) & 1, abort)))
+        ok = false;
+      tc_fence_after();
+    }
+    if (ok && k > 0) {
+      const float inv = have ? 1.f / l_row : 0.f;
+      uint32_t o[64];
+      tmem_ld64(o_col, o);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        uint4 w;
+        w.x = pack_bf16x2(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv);
+        w.y = pack_bf16x2(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
+        w.z = pack_bf16x2(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
+        w.w = pack_bf16x2(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
+        outv[e] = w;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) outv[e] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (row < P.g.N && ok) {
+      uint4* dst = reinterpret_cast<uint4*>(P.out + b * P.out_sb + h * P.out_sh +
+                                            static_cast<int64_t>(row) * P.out_sn + 64 * g);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) dst[e] = outv[e];
+      if (P.lse && g == 0) {
+        // ln sum_j exp(z_ij) = (m + log2 l) ln 2: m is the (lazily updated) row
+        // max in log2 units, l the row sum relative to it
+        const float lse = have ? (m_run + log2f(l_row)) * 0.69314718055994531f : -INFINITY;
+        P.lse[(static_cast<int64_t>(b) * P.g.Hq + h) * P.g.N + row] = lse;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+  if (tid == 0 && sm.abort && P.status) atomicOr(P.status, kStatusTimeout);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tile(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                                const CUtensorMap& mv, const CUtensorMap& mkc,
+                                const CUtensorMap& mvc, cudaStream_t st, int* n_launch) {
+  const int smem = static_cast<int>(sizeof(TileSmem)) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(sparse_prefill_tile_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  if (p.g.n_units == 0 || p.g.NQ == 0) return cudaSuccess;
+  sparse_prefill_tile_kernel<<<dim3(p.g.NQ, p.g.n_units), kThreads, smem, st>>>(p, mq, mk, mv, mkc,
+                                                                                mvc);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) ++*n_launch;
+  return e;
+}
+
+}  // namespace msa
