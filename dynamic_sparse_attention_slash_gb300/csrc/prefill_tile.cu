@@ -394,50 +394,50 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
       // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
       const bool waited = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[k & 1], (k >> 1) & 1, abort));
       tc_fence_after();
+      // A key tile whose quadrant (row half, key half g) is not admitted leaves
+      // this warp nothing to do: its half of P is zero, its maximum -inf.
+      const bool idle = !it.cols && !((it.qm >> (half * 2 + g)) & 1u);
       // raw logits (unscaled) of this row's half; scale * log2(e) is folded in below
       float x[64];
-      {
-        uint32_t raw[64];
-        tmem_ld64(s_col + 64 * g, raw);
+      float mxh = -INFINITY;
+      if (!idle) {
+        {
+          uint32_t raw[64];
+          tmem_ld64(s_col + 64 * g, raw);
 #pragma unroll
-        for (int e = 0; e < 64; ++e) x[e] = __uint_as_float(raw[e]);
-      }
-      // ---- mask
-      if (it.cols) {
-        const int base = 128 * it.idx + 64 * g;
-        const int32_t* V = P.vertical + static_cast<int64_t>(unit) * P.kv + base;
-        const int valid = P.kv - base;
-#pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          bool keep = false;
-          if (e < valid) {
-            const int j = V[e];
-            keep = j <= row && !dist_bit(dist, mblk - (j >> 6));
-          }
-          if (!keep) x[e] = -INFINITY;
+          for (int e = 0; e < 64; ++e) x[e] = __uint_as_float(raw[e]);
         }
-      } else {
-        const bool in_q = (it.qm >> (half * 2 + g)) & 1u;
-        if (!in_q) {
+        // ---- mask
+        if (it.cols) {
+          const int base = 128 * it.idx + 64 * g;
+          const int32_t* V = P.vertical + static_cast<int64_t>(unit) * P.kv + base;
+          const int valid = P.kv - base;
 #pragma unroll
-          for (int e = 0; e < 64; ++e) x[e] = -INFINITY;
+          for (int e = 0; e < 64; ++e) {
+            bool keep = false;
+            if (e < valid) {
+              const int j = V[e];
+              keep = j <= row && !dist_bit(dist, mblk - (j >> 6));
+            }
+            if (!keep) x[e] = -INFINITY;
+          }
         } else if (it.idx == p) {
 #pragma unroll
           for (int e = 0; e < 64; ++e)
             if (64 * g + e > r) x[e] = -INFINITY;
         }
-      }
-      // ---- online softmax (8 independent chains of 3-input max, paired sums)
-      float mx8[8];
+        // ---- online softmax (8 independent chains of 3-input max, paired sums)
+        float mx8[8];
 #pragma unroll
-      for (int a = 0; a < 8; ++a) {
-        float m = fmax3(x[a], x[8 + a], x[16 + a]);
+        for (int a = 0; a < 8; ++a) {
+          float m = fmax3(x[a], x[8 + a], x[16 + a]);
 #pragma unroll
-        for (int e = 24; e < 56; e += 16) m = fmax3(m, x[e + a], x[e + 8 + a]);
-        mx8[a] = fmaxf(m, x[56 + a]);
+          for (int e = 24; e < 56; e += 16) m = fmax3(m, x[e + a], x[e + 8 + a]);
+          mx8[a] = fmaxf(m, x[56 + a]);
+        }
+        mxh = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                    fmaxf(mx8[6], mx8[7]));
       }
-      const float mxh = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                              fmaxf(mx8[6], mx8[7]));
       sm.xmax[k & 1][g][r] = mxh;
       // both warps pass this barrier on every item (every wait above is bounded),
       // and leave together when either one's wait failed
@@ -450,24 +450,31 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
       const bool grow = m_new > m_run + kRescaleThreshold;  // false when both are -inf
       const float m_use = grow ? m_new : m_run;
       const float neg_base = m_use == -INFINITY ? 0.f : -m_use;
-      const float2 scale2 = make_float2(P.scale_log2, P.scale_log2);
-      const float2 nb2 = make_float2(neg_base, neg_base);
-      float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                       make_float2(0.f, 0.f)};
       uint32_t pk[32];
+      float rs = 0.f;
+      if (idle) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const float2 a = ffma2(make_float2(x[2 * e], x[2 * e + 1]), scale2, nb2);
-        const float2 pe = make_float2(ex2_approx(a.x), ex2_approx(a.y));
-        rs2[e & 3] = fadd2(rs2[e & 3], pe);
-        pk[e] = pack_f16x2(pe.x, pe.y);
+        for (int e = 0; e < 32; ++e) pk[e] = 0u;
+      } else {
+        const float2 scale2 = make_float2(P.scale_log2, P.scale_log2);
+        const float2 nb2 = make_float2(neg_base, neg_base);
+        float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float2 a = ffma2(make_float2(x[2 * e], x[2 * e + 1]), scale2, nb2);
+          const float2 pe = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+          rs2[e & 3] = fadd2(rs2[e & 3], pe);
+          pk[e] = pack_f16x2(pe.x, pe.y);
+        }
+        const float2 rsa = fadd2(fadd2(rs2[0], rs2[1]), fadd2(rs2[2], rs2[3]));
+        rs = rsa.x + rsa.y;
       }
-      const float2 rsa = fadd2(fadd2(rs2[0], rs2[1]), fadd2(rs2[2], rs2[3]));
-      const float rs = rsa.x + rsa.y;
       const bool correct = grow && m_run != -INFINITY;  // O holds earlier items' weight
       const float alpha = correct ? ex2_approx(m_run - m_new) : 1.f;
       l_run = (m_run == -INFINITY ? 0.f : l_run * alpha) + rs;
       m_run = m_use;
+      tmem_st32(s_col + 32 * g, pk);  // f16 pairs of keys [64g, 64g + 64)
       // both warps of these rows take this branch together (same maxima)
       if (__any_sync(0xffffffffu, correct)) {
         // O must hold P(k-1) V(k-1) before it is rescaled: that product's
@@ -476,6 +483,7 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
         const bool got = __all_sync(
             0xffffffffu, mbar_wait(&sm.v_empty[j % kStagesV], (j / kStagesV) & 1, abort));
         if (!bar_red_and(pair_bar, 64, got)) {
+          tmem_st_wait();
           ok = false;
           break;
         }
@@ -489,7 +497,6 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
           tmem_st32(o_col + 32 * q2, o);
         }
       }
-      tmem_st32(s_col + 32 * g, pk);  // f16 pairs of keys [64g, 64g + 64)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
