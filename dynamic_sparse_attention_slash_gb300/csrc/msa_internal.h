@@ -119,7 +119,8 @@ cudaError_t launch_v_to_f16(TensorView v, int B, int Hkv, int N, __half* dst, ui
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                            const CUtensorMap& mv, const CUtensorMap& mkc, const CUtensorMap& mvc,
                            cudaStream_t st, int* n_launch);
-// One query tile per CTA (same contract as launch_prefill; used for block-sparse heads).
+// One query tile per CTA, for block-sparse plans (launch_prefill routes them
+// here); any other kind returns cudaErrorInvalidValue.
 cudaError_t launch_prefill_tile(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                                 const CUtensorMap& mv, const CUtensorMap& mkc,
                                 const CUtensorMap& mvc, cudaStream_t st, int* n_launch);

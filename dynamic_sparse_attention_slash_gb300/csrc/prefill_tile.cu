@@ -7,17 +7,12 @@
 //
 // This kernel serves the block-sparse heads: one CTA computes one 128-row
 // query tile p of one (batch, head) unit (row blocks 2p and 2p + 1).  It walks
-// the pair lists of prefill.cu's index structures but keeps only the entries
-// whose quadrant mask is non-empty for its own tile, so a tile never loads or
-// multiplies a key tile only its neighbour needs.  Work items are 128 keys wide:
-//   * a key tile q: keys [128q, 128q+128) of the KV head, with a 4-bit quadrant
-//     mask (bit a*2+b: row half a may see key half b) and the causal cut on the
-//     tile's diagonal;
-//   * a column chunk c (vertical-slash only): gathered K/V rows of chosen keys
-//     [128c, 128c+128) of the unit's ascending vertical list, each admitted for
-//     a row iff the key is <= the row and outside the row block's active tiles.
-// (The kernel runs every head kind; the library routes only block-sparse heads
-// here.)
+// the pair tile list that bs_index.cu builds for the pair of query tiles
+// (2c, 2c + 1) and keeps only the entries whose quadrant mask is non-empty for
+// its own tile, so a tile never loads or multiplies a key tile only its
+// neighbour needs.  An item is a key tile q: keys [128q, 128q+128) of the KV
+// head, with a 4-bit quadrant mask (bit a*2+b: row half a may see key half b)
+// and the causal cut on the tile's diagonal.
 //
 // Warp roles (384 threads):
 //   warp 0     TMA producer for Q and K (one thread)
@@ -70,20 +65,17 @@ struct __align__(1024) TileSmem {
 };
 
 struct Item {
-  bool cols;    // column chunk (true) or key tile (false)
-  int idx;      // key tile q or chunk c
-  uint32_t qm;  // quadrant mask of a key tile for this query tile (bit a*2 + b)
+  int idx;      // key tile q
+  uint32_t qm;  // quadrant mask for this query tile (bit a*2 + b: row half a sees key half b)
 };
 
-// The query tile of a CTA and the slots its items are drawn from.  The index
-// structures describe pairs of query tiles (2c, 2c + 1); a tile takes the
-// pair's entries whose quadrant mask for it is not empty.
+// The query tile of a CTA and its pair's block-sparse tile list.  The list
+// describes the pair of query tiles (2c, 2c + 1), each entry (q << 8) | maskB
+// << 4 | maskA; the tile keeps the entries whose own mask is not empty.
 struct Tile {
-  int unit, p, t, pB;    // tile p = 2c + t, pB = 2c + 1
-  int n_chunk_slots;     // vertical-slash: 32 * chunk_words column-chunk slots first
-  int n_slots;
-  int n_hi;              // vertical-slash: pair distances <= pB
-  int sink_hi, loc_lo;   // streaming: key tiles [0, sink_hi) and [loc_lo, p]
+  int unit, p, t;  // tile p = 2c + t
+  int n_slots;     // entries of the pair list
+  const int32_t* list;
 };
 
 __device__ __forceinline__ Tile make_tile(const PrefillParams& P, int unit, int p) {
@@ -91,124 +83,31 @@ __device__ __forceinline__ Tile make_tile(const PrefillParams& P, int unit, int 
   T.unit = unit;
   T.p = p;
   T.t = p & 1;
-  T.pB = p | 1;
-  T.n_chunk_slots = 0;
-  T.n_hi = 0;
-  T.sink_hi = 0;
-  T.loc_lo = 0;
-  if (P.kind == kPrefillVS) {
-    T.n_chunk_slots = 32 * P.chunk_words;
-    T.n_hi = vs_tiles_upto(P, unit, T.pB);
-    T.n_slots = T.n_chunk_slots + T.n_hi;
-  } else if (P.kind == kPrefillBS) {
-    T.n_slots = P.bs_tile_count[static_cast<int64_t>(unit) * P.npair + (p >> 1)];
-  } else {
-    T.sink_hi = min((P.init_num + 1) >> 1, p + 1);
-    T.loc_lo = max(0, 2 * p - P.local_num + 1) >> 1;
-    if (T.sink_hi >= T.loc_lo) {  // the two ranges meet: one range [0, p]
-      T.sink_hi = 0;
-      T.loc_lo = 0;
-    }
-    T.n_slots = T.sink_hi + (p - T.loc_lo + 1);
-  }
+  const int64_t pair = static_cast<int64_t>(unit) * P.npair + (p >> 1);
+  T.n_slots = P.bs_tile_count[pair];
+  T.list = P.bs_tiles + pair * P.bs_tile_cap;
   return T;
 }
 
-// Vertical-slash pair entry (D << 5) | bits: key tile pB - D; quadrant (a, b)
-// sits at 64-block distance 2D + a - b for tile pB (bit a - b + 3) and
-// 2D - 2 + a - b for tile pA (bit a - b + 1).  Row blocks past the sequence
-// take nothing.
-__device__ __forceinline__ uint32_t vs_qmask(const PrefillParams& P, const Tile& T, int32_t e) {
-  const int sh = T.t ? 3 : 1;
-  uint32_t m = 0;
-#pragma unroll
-  for (int a = 0; a < 2; ++a) {
-#pragma unroll
-    for (int b = 0; b < 2; ++b)
-      if (2 * T.p + a < P.g.NB) m |= ((e >> (a - b + sh)) & 1u) << (a * 2 + b);
-  }
-  return m;
-}
-
-__device__ __forceinline__ uint32_t bs_qmask(const Tile& T, int32_t e) {
+__device__ __forceinline__ uint32_t tile_qmask(const Tile& T, int32_t e) {
   return static_cast<uint32_t>(T.t ? (e >> 4) & 15 : e & 15);
 }
 
-__device__ __forceinline__ int st_key(const Tile& T, int s) {
-  return s < T.sink_hi ? s : T.loc_lo + (s - T.sink_hi);
-}
-
 // Items of the tile (warp-collective: every lane returns the count).
-__device__ int count_items(const PrefillParams& P, const Tile& T, int lane) {
+__device__ int count_items(const Tile& T, int lane) {
   int cnt = 0;
-  if (P.kind == kPrefillVS) {
-    const uint32_t* w = P.col_chunks + (static_cast<int64_t>(T.unit) * P.g.NQ + T.p) * P.chunk_words;
-    for (int x = lane; x < P.chunk_words; x += 32) cnt += __popc(w[x]);
-    const int32_t* qd = P.qdelta + static_cast<int64_t>(T.unit) * (P.g.NQ + 1);
-    for (int j = lane; j < T.n_hi; j += 32) cnt += vs_qmask(P, T, qd[j]) != 0u ? 1 : 0;
-  } else if (P.kind == kPrefillBS) {
-    const int32_t* L = P.bs_tiles + (static_cast<int64_t>(T.unit) * P.npair + (T.p >> 1)) * P.bs_tile_cap;
-    for (int j = lane; j < T.n_slots; j += 32) cnt += bs_qmask(T, L[j]) != 0u ? 1 : 0;
-  } else {
-    for (int s = lane; s < T.n_slots; s += 32) cnt += quad_mask_st(P, T.p, st_key(T, s)) != 0u ? 1 : 0;
-  }
+  for (int j = lane; j < T.n_slots; j += 32) cnt += tile_qmask(T, T.list[j]) != 0u ? 1 : 0;
   return __reduce_add_sync(0xffffffffu, cnt);
 }
 
 // The next item at or after slot s (s moves past it); false when none is left.
-// Vertical-slash: column chunks ascending, then key tiles ascending (largest
-// pair distance first).
-__device__ __forceinline__ bool next_item(const PrefillParams& P, const Tile& T, int& s, Item& it) {
-  if (P.kind == kPrefillVS) {
-    if (s < T.n_chunk_slots) {
-      const uint32_t* w = P.col_chunks + (static_cast<int64_t>(T.unit) * P.g.NQ + T.p) * P.chunk_words;
-      while (s < T.n_chunk_slots) {
-        const uint32_t word = w[s >> 5] >> (s & 31);
-        if (word == 0u) {
-          s = (s | 31) + 1;
-          continue;
-        }
-        s += __ffs(static_cast<int>(word)) - 1;
-        it.cols = true;
-        it.idx = s++;
-        it.qm = 0xFu;
-        return true;
-      }
-    }
-    const int32_t* qd = P.qdelta + static_cast<int64_t>(T.unit) * (P.g.NQ + 1);
-    while (s < T.n_slots) {
-      const int32_t e = qd[T.n_hi - 1 - (s - T.n_chunk_slots)];
-      ++s;
-      const uint32_t m = vs_qmask(P, T, e);
-      if (m) {
-        it.cols = false;
-        it.idx = T.pB - (e >> 5);
-        it.qm = m;
-        return true;
-      }
-    }
-    return false;
-  }
-  if (P.kind == kPrefillBS) {
-    const int32_t* L = P.bs_tiles + (static_cast<int64_t>(T.unit) * P.npair + (T.p >> 1)) * P.bs_tile_cap;
-    while (s < T.n_slots) {
-      const int32_t e = L[s++];
-      const uint32_t m = bs_qmask(T, e);
-      if (m) {
-        it.cols = false;
-        it.idx = e >> 8;
-        it.qm = m;
-        return true;
-      }
-    }
-    return false;
-  }
+// Key tiles come in the list's ascending order.
+__device__ __forceinline__ bool next_item(const Tile& T, int& s, Item& it) {
   while (s < T.n_slots) {
-    const int q = st_key(T, s++);
-    const uint32_t m = quad_mask_st(P, T.p, q);
+    const int32_t e = T.list[s++];
+    const uint32_t m = tile_qmask(T, e);
     if (m) {
-      it.cols = false;
-      it.idx = q;
+      it.idx = e >> 8;
       it.qm = m;
       return true;
     }
@@ -216,26 +115,18 @@ __device__ __forceinline__ bool next_item(const PrefillParams& P, const Tile& T,
   return false;
 }
 
-// TMA of item it's K (or V) tile into dst, completion on bar.
-__device__ __forceinline__ void load_item(const PrefillParams& P, const Item& it, uint8_t* dst,
-                                          const CUtensorMap* map, const CUtensorMap* map_cols,
-                                          uint64_t* bar, int unit, int hkv, int b) {
+// TMA of key tile it.idx's K (or V) rows into dst, completion on bar.
+__device__ __forceinline__ void load_item(const Item& it, uint8_t* dst, const CUtensorMap* map,
+                                          uint64_t* bar, int hkv, int b) {
   mbar_arrive_expect_tx(bar, kTileBytes);
-  if (it.cols) {
-    const int row = unit * P.kv_pad + 128 * it.idx;
-    tma_load_2d(dst, map_cols, bar, 0, row);
-    tma_load_2d(dst + kHalfBytes, map_cols, bar, 64, row);
-  } else {
-    tma_load_4d(dst, map, bar, 0, 128 * it.idx, hkv, b);
-    tma_load_4d(dst + kHalfBytes, map, bar, 64, 128 * it.idx, hkv, b);
-  }
+  tma_load_4d(dst, map, bar, 0, 128 * it.idx, hkv, b);
+  tma_load_4d(dst + kHalfBytes, map, bar, 64, 128 * it.idx, hkv, b);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
 sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ CUtensorMap mq,
-                      const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
-                      const __grid_constant__ CUtensorMap mkc,
-                      const __grid_constant__ CUtensorMap mvc) {
+                           const __grid_constant__ CUtensorMap mk,
+                           const __grid_constant__ CUtensorMap mv) {
   extern __shared__ uint8_t smem_raw[];
   TileSmem& sm = *reinterpret_cast<TileSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~static_cast<uintptr_t>(1023));
@@ -283,10 +174,10 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
       tma_load_4d(sm.q + kHalfBytes, &mq, &sm.q_full, 64, 128 * p, h, b);
       int issued = 0, s = 0;
       Item it;
-      for (int i = 0; next_item(P, T, s, it); ++i) {
+      for (int i = 0; next_item(T, s, it); ++i) {
         const int st = i % kStagesK;
         if (!mbar_wait(&sm.k_empty[st], ((i / kStagesK) & 1) ^ 1, abort)) break;
-        load_item(P, it, sm.k[st], &mk, &mkc, &sm.k_full[st], unit, hkv, b);
+        load_item(it, sm.k[st], &mk, &sm.k_full[st], hkv, b);
         issued = i + 1;
       }
       // drain: the latest load of every stage, and Q, must land before exit
@@ -300,10 +191,10 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
       tma_prefetch_desc(&mv);
       int issued = 0, s = 0;
       Item it;
-      for (int i = 0; next_item(P, T, s, it); ++i) {
+      for (int i = 0; next_item(T, s, it); ++i) {
         const int st = i % kStagesV;
         if (!mbar_wait(&sm.v_empty[st], ((i / kStagesV) & 1) ^ 1, abort)) break;
-        load_item(P, it, sm.v[st], &mv, &mvc, &sm.v_full[st], unit, hkv, b);
+        load_item(it, sm.v[st], &mv, &sm.v_full[st], hkv, b);
         issued = i + 1;
       }
       for (int i = max(0, issued - kStagesV); i < issued; ++i)
@@ -311,7 +202,7 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    const int n = count_items(P, T, lane);
+    const int n = count_items(T, lane);
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idO = idesc_f32acc(128, 128, /*bf16=*/false, false, true);  // f16 P, f16 V
@@ -378,10 +269,6 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
     const uint32_t pair_bar = 1 + quarter;    // named barrier of the two warps of these rows
     const int half = r >> 6;                  // row block 2p + half
     const int row = 128 * p + r;              // query index i
-    const int mblk = 2 * p + half;
-    const uint32_t* dist = P.kind == kPrefillVS
-                               ? P.tile_dist + static_cast<int64_t>(unit) * P.dist_words
-                               : nullptr;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t o_col = lane_base + kColO + 64 * g;
     float m_run = -INFINITY, l_run = 0.f;
@@ -389,14 +276,14 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
     int k = 0;  // items processed so far
     int slot = 0;
     Item it;
-    while (next_item(P, T, slot, it)) {
+    while (next_item(T, slot, it)) {
       const uint32_t s_col = lane_base + kColS + 128 * (k & 1);
       // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
       const bool waited = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[k & 1], (k >> 1) & 1, abort));
       tc_fence_after();
       // A key tile whose quadrant (row half, key half g) is not admitted leaves
       // this warp nothing to do: its half of P is zero, its maximum -inf.
-      const bool idle = !it.cols && !((it.qm >> (half * 2 + g)) & 1u);
+      const bool idle = !((it.qm >> (half * 2 + g)) & 1u);
       // raw logits (unscaled) of this row's half; scale * log2(e) is folded in below
       float x[64];
       float mxh = -INFINITY;
@@ -407,21 +294,8 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
 #pragma unroll
           for (int e = 0; e < 64; ++e) x[e] = __uint_as_float(raw[e]);
         }
-        // ---- mask
-        if (it.cols) {
-          const int base = 128 * it.idx + 64 * g;
-          const int32_t* V = P.vertical + static_cast<int64_t>(unit) * P.kv + base;
-          const int valid = P.kv - base;
-#pragma unroll
-          for (int e = 0; e < 64; ++e) {
-            bool keep = false;
-            if (e < valid) {
-              const int j = V[e];
-              keep = j <= row && !dist_bit(dist, mblk - (j >> 6));
-            }
-            if (!keep) x[e] = -INFINITY;
-          }
-        } else if (it.idx == p) {
+        // ---- causal cut on the diagonal tile
+        if (it.idx == p) {
 #pragma unroll
           for (int e = 0; e < 64; ++e)
             if (64 * g + e > r) x[e] = -INFINITY;
@@ -561,9 +435,9 @@ cudaError_t launch_prefill_tile(const PrefillParams& p, const CUtensorMap& mq, c
   cudaError_t e = cudaFuncSetAttribute(sparse_prefill_tile_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  if (p.kind != kPrefillBS) return cudaErrorInvalidValue;  // block-sparse tile lists only
   if (p.g.n_units == 0 || p.g.NQ == 0) return cudaSuccess;
-  sparse_prefill_tile_kernel<<<dim3(p.g.NQ, p.g.n_units), kThreads, smem, st>>>(p, mq, mk, mv, mkc,
-                                                                                mvc);
+  sparse_prefill_tile_kernel<<<dim3(p.g.NQ, p.g.n_units), kThreads, smem, st>>>(p, mq, mk, mv);
   e = cudaGetLastError();
   if (e == cudaSuccess) ++*n_launch;
   return e;
