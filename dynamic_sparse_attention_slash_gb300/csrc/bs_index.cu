@@ -17,6 +17,14 @@ namespace {
 constexpr int kPoolWarps = 4;
 constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
+// Selection with shared key chunks: kSelWarps row blocks per CTA (one warp
+// each) score against pooled key blocks staged kKeyChunk at a time in shared
+// memory (row stride kHeadDim + 1 floats, so the 32 lanes, one key each, read
+// 32 different banks).  Used while the CTA's scores fit: NB <= kRowsMaxNB.
+constexpr int kKeyChunk = 32;
+constexpr int kKStride = kHeadDim + 1;
+constexpr int kRowsMaxNB = 4096;
+constexpr int kTilesWarps = 4;
 
 struct PoolArgs {
   UnitMap u;
@@ -159,50 +167,187 @@ __global__ void __launch_bounds__(kSelThreads) bs_select_kernel(const __grid_con
   if (tid == 0) ids[k_earlier] = m;  // the diagonal block, largest id
 }
 
+// One CTA per kSelWarps consecutive row blocks of a unit; warp w owns row
+// block m0 + w: its scores against every earlier block (one lane per key,
+// pooled keys staged in shared memory and shared by the CTA's rows), then the
+// same radix select and ascending compaction as bs_select_kernel, run by the
+// warp alone.
+__global__ void __launch_bounds__(kSelThreads) bs_select_rows_kernel(const __grid_constant__ SelArgs a) {
+  extern __shared__ float dyn[];
+  float* sc = dyn;                              // [kSelWarps][NB] scores
+  float* kc = sc + kSelWarps * a.NB;            // [kKeyChunk][kKStride] pooled keys
+  float* qs = kc + kKeyChunk * kKStride;        // [kSelWarps][kHeadDim] pooled queries
+  __shared__ int hist[kSelWarps][256];
+  const int unit = blockIdx.y, m0 = blockIdx.x * kSelWarps;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = unit / a.u.n_heads;
+  const int hkv = a.u.heads[unit % a.u.n_heads] / a.G;
+  const int rows = min(kSelWarps, a.NB - m0);
+  for (int i = tid; i < kSelWarps * kHeadDim; i += kSelThreads) {
+    const int r = i / kHeadDim;
+    qs[i] = r < rows
+                ? a.qpool[(static_cast<int64_t>(unit) * a.NB + m0 + r) * kHeadDim + i % kHeadDim]
+                : 0.f;
+  }
+  const float* kp = a.kpool + static_cast<int64_t>(b * a.Hkv + hkv) * a.NB * kHeadDim;
+  const int n_end = m0 + rows - 1;  // the CTA's last row block scores keys n < n_end
+  const int m = m0 + warp;
+  for (int n0 = 0; n0 < n_end; n0 += kKeyChunk) {
+    __syncthreads();  // the previous chunk is consumed (and qs is written)
+    for (int i = tid; i < kKeyChunk * kHeadDim; i += kSelThreads) {
+      const int j = i / kHeadDim, c = i % kHeadDim;
+      kc[j * kKStride + c] = n0 + j < n_end ? kp[static_cast<int64_t>(n0 + j) * kHeadDim + c] : 0.f;
+    }
+    __syncthreads();
+    const int n = n0 + lane;
+    if (warp < rows && n < m) {
+      const float* qr = qs + warp * kHeadDim;
+      const float* kr = kc + lane * kKStride;
+      float d = 0.f;
+#pragma unroll 16
+      for (int c = 0; c < kHeadDim; ++c) d = fmaf(qr[c], kr[c], d);
+      sc[warp * a.NB + n] = d * a.scale;
+    }
+  }
+  if (warp >= rows) return;  // no CTA-wide barrier follows
+  __syncwarp();
+  int32_t* ids = a.block_ids + (static_cast<int64_t>(unit) * a.NB + m) * a.kb;
+  const int k_earlier = min(a.topk - 1, m);  // earlier blocks to keep
+  if (lane == 0) a.block_count[static_cast<int64_t>(unit) * a.NB + m] = k_earlier + 1;
+  if (k_earlier == m) {  // every earlier block is kept
+    for (int n = lane; n <= m; n += 32) ids[n] = n;
+    return;
+  }
+  const float* s = sc + warp * a.NB;
+  int* h = hist[warp];
+  uint32_t prefix = 0u, mask = 0u;
+  int need = k_earlier;
+  if (k_earlier > 0) {
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      for (int i = lane; i < 256; i += 32) h[i] = 0;
+      __syncwarp();
+      for (int n = lane; n < m; n += 32) {
+        const uint32_t key = ordered_key(s[n]);
+        if ((key & mask) == prefix) atomicAdd(&h[(key >> shift) & 255u], 1);
+      }
+      __syncwarp();
+      // lane l holds bins 255 - 8l down to 248 - 8l; the bucket is the one in
+      // which the count from the top reaches `need`
+      int cnt[8], tot = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        cnt[j] = h[255 - 8 * lane - j];
+        tot += cnt[j];
+      }
+      int incl = tot;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      const int excl = incl - tot;
+      const bool mine = excl < need && incl >= need;
+      const int src = __ffs(static_cast<int>(__ballot_sync(0xffffffffu, mine))) - 1;
+      int bucket = 0, above = excl;
+      if (mine) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (above + cnt[j] >= need) {
+            bucket = 255 - 8 * lane - j;
+            break;
+          }
+          above += cnt[j];
+        }
+      }
+      bucket = __shfl_sync(0xffffffffu, bucket, src);
+      above = __shfl_sync(0xffffffffu, above, src);
+      need -= above;
+      prefix |= static_cast<uint32_t>(bucket) << shift;
+      mask |= 255u << shift;
+      __syncwarp();  // every lane has read the histogram before it is cleared
+    }
+    // keys above the threshold, and the first `need` keys equal to it (lower
+    // blocks first), in ascending block order
+    const uint32_t lt = (1u << lane) - 1u;
+    int kept = 0, eq_seen = 0;
+    for (int base = 0; base < m; base += 32) {
+      const int n = base + lane;
+      const uint32_t key = n < m ? ordered_key(s[n]) : 0u;
+      const bool eq = n < m && key == prefix;
+      const uint32_t eqb = __ballot_sync(0xffffffffu, eq);
+      const bool keep = n < m && (key > prefix || (eq && eq_seen + __popc(eqb & lt) < need));
+      const uint32_t kb = __ballot_sync(0xffffffffu, keep);
+      if (keep) ids[kept + __popc(kb & lt)] = n;
+      kept += __popc(kb);
+      eq_seen += __popc(eqb);
+    }
+  }
+  if (lane == 0) ids[k_earlier] = m;  // the diagonal block, largest id
+}
+
 struct TileArgs {
   int NB, npair, kb, tile_cap, n_units;
+  int words_per_warp;   // shared words per warp: ceil(key tiles / 4)
   const int32_t* block_count;
   const int32_t* block_ids;
   int32_t* tiles;       // [units][npair][tile_cap] (q << 8) | maskB << 4 | maskA
   int32_t* tile_count;  // [units][npair]
 };
 
-// One thread per (unit, pair c of 128-row query tiles): merge the ascending
-// block lists of row blocks 4c .. 4c+3 into 128-key tiles with one 4-bit
-// quadrant mask per query tile (bit a*2 + b: row half a sees key half b).
-__global__ void bs_tiles_kernel(TileArgs a) {
-  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (gid >= static_cast<int64_t>(a.n_units) * a.npair) return;
+// One warp per (unit, pair c of 128-row query tiles): the blocks kept by row
+// blocks 4c .. 4c+3 set bits of a per-key-tile byte in shared memory (key tile
+// q = block >> 1; bit tile * 4 + row half * 2 + key half, i.e. maskA in the low
+// and maskB in the high nibble), and the non-empty bytes are written out in
+// ascending q as (q << 8) | maskB << 4 | maskA.
+__global__ void __launch_bounds__(32 * kTilesWarps) bs_tiles_kernel(TileArgs a) {
+  extern __shared__ uint32_t tile_bytes[];  // [kTilesWarps][words_per_warp], 4 key tiles a word
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * kTilesWarps + warp;
+  if (gid >= static_cast<int64_t>(a.n_units) * a.npair) return;  // no CTA-wide barrier follows
   const int unit = static_cast<int>(gid / a.npair), c = static_cast<int>(gid % a.npair);
-  const int32_t* lists[4];
-  int cnt[4], pos[4] = {0, 0, 0, 0};
+  const int nq = min(2 * c + 2, (a.NB + 1) >> 1);  // key tiles q <= 2c + 1 within the sequence
+  const int words = (nq + 3) >> 2;
+  uint32_t* w = tile_bytes + warp * a.words_per_warp;
+  for (int i = lane; i < words; i += 32) w[i] = 0u;
+  __syncwarp();
   for (int j = 0; j < 4; ++j) {
     const int m = 4 * c + j;
-    lists[j] = a.block_ids + (static_cast<int64_t>(unit) * a.NB + m) * a.kb;
-    cnt[j] = m < a.NB ? a.block_count[static_cast<int64_t>(unit) * a.NB + m] : 0;
-  }
-  int32_t* out = a.tiles + gid * a.tile_cap;
-  int n = 0, cur_q = -1, cur_mask = 0;
-  for (;;) {
-    int best = -1, blk = 0;
-    for (int j = 0; j < 4; ++j)
-      if (pos[j] < cnt[j] && (best < 0 || lists[j][pos[j]] < blk)) {
-        best = j;
-        blk = lists[j][pos[j]];
-      }
-    if (best < 0) break;
-    ++pos[best];
-    const int q = blk >> 1;
-    const int bit = (best >> 1) * 4 + (best & 1) * 2 + (blk & 1);  // tile, row half, key half
-    if (q != cur_q) {
-      if (cur_q >= 0) out[n++] = (cur_q << 8) | cur_mask;
-      cur_q = q;
-      cur_mask = 0;
+    if (m >= a.NB) break;
+    const int64_t rb = static_cast<int64_t>(unit) * a.NB + m;
+    const int cnt = a.block_count[rb];
+    const int32_t* L = a.block_ids + rb * a.kb;
+    const int bit = (j >> 1) * 4 + (j & 1) * 2;  // tile, row half
+    for (int i = lane; i < cnt; i += 32) {
+      const int blk = L[i];
+      const int q = blk >> 1;
+      atomicOr(&w[q >> 2], (1u << (bit + (blk & 1))) << (8 * (q & 3)));
     }
-    cur_mask |= 1 << bit;
   }
-  if (cur_q >= 0) out[n++] = (cur_q << 8) | cur_mask;
-  a.tile_count[gid] = n;
+  __syncwarp();
+  int32_t* out = a.tiles + gid * a.tile_cap;
+  int n = 0;
+  for (int base = 0; base < words; base += 32) {
+    const int i = base + lane;
+    const uint32_t word = i < words ? w[i] : 0u;
+    int cw = 0;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) cw += ((word >> (8 * t)) & 255u) != 0u ? 1 : 0;
+    int incl = cw;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    int pos = n + incl - cw;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const uint32_t mk = (word >> (8 * t)) & 255u;
+      if (mk) out[pos++] = ((4 * i + t) << 8) | static_cast<int>(mk);
+    }
+    n += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) a.tile_count[gid] = n;
 }
 
 }  // namespace
@@ -243,12 +388,23 @@ cudaError_t launch_bs_index(const Geometry& g, const UnitMap& u, TensorView q, T
   sa.block_count = block_count;
   sa.block_ids = block_ids;
   sa.kb = min(topk, g.NB);
-  const int smem = g.NB * 4;
-  if (smem > 48 * 1024) {
-    e = cudaFuncSetAttribute(bs_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
+  if (g.NB <= kRowsMaxNB) {
+    const int smem = (kSelWarps * g.NB + kKeyChunk * kKStride + kSelWarps * kHeadDim) * 4;
+    if (smem > 48 * 1024) {
+      e = cudaFuncSetAttribute(bs_select_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               smem);
+      if (e != cudaSuccess) return e;
+    }
+    bs_select_rows_kernel<<<dim3((g.NB + kSelWarps - 1) / kSelWarps, g.n_units), kSelThreads, smem,
+                            st>>>(sa);
+  } else {
+    const int smem = g.NB * 4;
+    if (smem > 48 * 1024) {
+      e = cudaFuncSetAttribute(bs_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+    }
+    bs_select_kernel<<<dim3(g.NB, g.n_units), kSelThreads, smem, st>>>(sa);
   }
-  bs_select_kernel<<<dim3(g.NB, g.n_units), kSelThreads, smem, st>>>(sa);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   ++*n_launch;
   TileArgs ta;
@@ -261,8 +417,15 @@ cudaError_t launch_bs_index(const Geometry& g, const UnitMap& u, TensorView q, T
   ta.block_ids = block_ids;
   ta.tiles = tiles;
   ta.tile_count = tile_count;
-  const int64_t threads = static_cast<int64_t>(g.n_units) * ta.npair;
-  bs_tiles_kernel<<<static_cast<unsigned>((threads + 127) / 128), 128, 0, st>>>(ta);
+  ta.words_per_warp = (((g.NB + 1) >> 1) + 3) >> 2;
+  const int tsmem = kTilesWarps * ta.words_per_warp * 4;
+  if (tsmem > 48 * 1024) {
+    e = cudaFuncSetAttribute(bs_tiles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tsmem);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t warps = static_cast<int64_t>(g.n_units) * ta.npair;
+  bs_tiles_kernel<<<static_cast<unsigned>((warps + kTilesWarps - 1) / kTilesWarps),
+                    32 * kTilesWarps, tsmem, st>>>(ta);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   ++*n_launch;
   return cudaSuccess;

@@ -85,6 +85,33 @@ def test_block_sparse_matches_oracle(N, topk):
         P.compare_out(np64(out[0, h]), ref, f"bs h{h}")
 
 
+@pytest.mark.parametrize("NB", [4096, 4097])
+def test_block_sparse_selection_at_long_lengths(NB):
+    """The block selection runs as CTAs of eight row blocks sharing staged key
+    chunks up to 4096 row blocks and as one CTA per row block beyond: every row
+    block's kept set against the oracle on both sides of that bound, outputs on
+    sampled rows (including the first and last rows and the rows at the bound)."""
+    N, topk = 64 * NB, 100
+    q, k, v = qkv(1, 1, 1, N, 15, vs=False, bs=True)
+    out, ex = P.run_bs(q, k, v, topk)
+    qn, kn, vn = np64(q)[0, 0], np64(k)[0, 0], np64(v)[0, 0]
+    _, S = O.block_sparse_blocks(qn, kn, topk)
+    gpu_sel = []
+    for m in range(NB):
+        cnt = int(ex["block_count"][0, m])
+        assert cnt == min(topk, m + 1)
+        got = ex["block_ids"][0, m, :cnt]
+        assert got[-1] == m, "diagonal block must be kept"
+        if m > 0:
+            P.check_topk(got[:-1], S[m, :m], topk - 1, f"m{m}")
+        gpu_sel.append(got.astype(np.int64))
+    rng = np.random.default_rng(NB)
+    rows = np.unique(np.concatenate([rng.integers(0, N, 40), [0, 64 * 4095, 64 * 4096 - 1, N - 1]]))
+    mask = O.block_mask_from_blocks(gpu_sel, N)
+    ref, _ = O.attend_rows(qn, kn, vn, rows, lambda i: mask(i // 64), 1 / math.sqrt(D))
+    P.compare_out(np64(out[0, 0, rows]), ref, f"bs NB={NB}")
+
+
 # ----------------------------------------------------------------------------- vertical-slash
 def check_vs_case(q, k, v, vertical_topk, slash, last_q=64, heads=None):
     out, ex = P.run_vs(q, k, v, vertical_topk, slash, last_q=last_q, heads=heads)
