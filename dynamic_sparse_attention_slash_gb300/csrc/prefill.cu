@@ -29,8 +29,10 @@
 //   warps 4-7 softmax of query tile A, warps 8-11 of query tile B: thread r owns
 //            query row r of its tile (TMEM lane r): reads S from TMEM, masks,
 //            runs the online softmax in fp32 (exp2 with log2(e) folded into the
-//            scale), writes P as f16 back over S, rescales O in TMEM when the
-//            row max grows by more than 2^8, and writes the output row.
+//            scale) against the row's running max, takes the row max (and
+//            rescales O in TMEM) only when the item's row sum would let a P
+//            value leave the f16 range, writes P as f16 back over S, and writes
+//            the output row.
 //
 // TMEM (512 columns): S/P of tile A at [0,128), of tile B at [128,256); the
 // output accumulators O_A at [256,384) and O_B at [384,512).  S = Q K^T reads Q
@@ -52,6 +54,8 @@ using namespace prefill;
 constexpr int kThreads = 384;
 constexpr int kStagesK = 3;
 constexpr int kStagesV = 2;
+// A row sum of at most 2^15 bounds every p of the item by it: P fits f16.
+constexpr float kSumLimit = 32768.f;
 // TMEM columns: S/P of tile t at kColS + 128 t, O of tile t at kColO + 128 t
 constexpr uint32_t kColS = 0, kColO = 256;
 // Register split: the control warpgroup drops to kCtrlRegs, the two softmax
@@ -393,73 +397,99 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
       // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[t], k & 1, abort))) { ok = false; break; }
       tc_fence_after();
-      // raw logits (unscaled) of this row; scale * log2(e) is folded in below
-      float x[128];
-      {
-        uint32_t raw[128];
-        tmem_ld128(s_col, raw);
+      // raw logits (unscaled) of this row, masked; scale * log2(e) is folded in
+      // below.  S stays in TMEM until P is written over it, so this may run twice.
+      auto logits = [&](float (&x)[128]) {
+        {
+          uint32_t raw[128];
+          tmem_ld128(s_col, raw);
 #pragma unroll
-        for (int e = 0; e < 128; ++e) x[e] = __uint_as_float(raw[e]);
-      }
-      // ---- mask
-      if (it.cols) {
-        const int32_t* V = P.vertical + static_cast<int64_t>(unit) * P.kv + 128 * it.idx;
-        const int valid = min(128, P.kv - 128 * it.idx);
-#pragma unroll
-        for (int e = 0; e < 128; ++e) {
-          bool keep = false;
-          if (e < valid) {
-            const int j = V[e];
-            keep = j <= row && !dist_bit(dist, mblk - (j >> 6));
-          }
-          if (!keep) x[e] = -INFINITY;
+          for (int e = 0; e < 128; ++e) x[e] = __uint_as_float(raw[e]);
         }
-      } else {
-        const uint32_t qm = t ? it.qmask[1] : it.qmask[0];
-        const bool lo_ok = (qm >> (half * 2)) & 1u;
-        const bool hi_ok = (qm >> (half * 2 + 1)) & 1u;
-        const bool diag = it.idx == p;
-        if (!lo_ok || !hi_ok || diag) {
+        if (it.cols) {
+          const int32_t* V = P.vertical + static_cast<int64_t>(unit) * P.kv + 128 * it.idx;
+          const int valid = min(128, P.kv - 128 * it.idx);
 #pragma unroll
           for (int e = 0; e < 128; ++e) {
-            const bool in_q = e < 64 ? lo_ok : hi_ok;
-            if (!in_q || (diag && e > r)) x[e] = -INFINITY;
+            bool keep = false;
+            if (e < valid) {
+              const int j = V[e];
+              keep = j <= row && !dist_bit(dist, mblk - (j >> 6));
+            }
+            if (!keep) x[e] = -INFINITY;
+          }
+        } else {
+          const uint32_t qm = t ? it.qmask[1] : it.qmask[0];
+          const bool lo_ok = (qm >> (half * 2)) & 1u;
+          const bool hi_ok = (qm >> (half * 2 + 1)) & 1u;
+          const bool diag = it.idx == p;
+          if (!lo_ok || !hi_ok || diag) {
+#pragma unroll
+            for (int e = 0; e < 128; ++e) {
+              const bool in_q = e < 64 ? lo_ok : hi_ok;
+              if (!in_q || (diag && e > r)) x[e] = -INFINITY;
+            }
           }
         }
-      }
-      // ---- online softmax (8 independent chains of 3-input max, paired sums)
-      float mx8[8];
+      };
+      // p = 2^(z log2(e) - m) as f16 pairs (paired exponent arguments and sums);
+      // returns the row sum
+      auto exps = [&](const float (&x)[128], float m, uint32_t (&pk)[64]) -> float {
+        const float2 scale2 = make_float2(P.scale_log2, P.scale_log2);
+        const float nb = m == -INFINITY ? 0.f : -m;
+        const float2 nb2 = make_float2(nb, nb);
+        float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
 #pragma unroll
-      for (int a = 0; a < 8; ++a) {
-        float m = fmax3(x[a], x[8 + a], x[16 + a]);
-#pragma unroll
-        for (int e = 24; e < 120; e += 16) m = fmax3(m, x[e + a], x[e + 8 + a]);
-        mx8[a] = fmaxf(m, x[120 + a]);
-      }
-      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                             fmaxf(mx8[6], mx8[7]));
-      const float m_new = fmaxf(m_run, mx * P.scale_log2);
-      const bool grow = m_new > m_run + kRescaleThreshold;  // false when both are -inf
-      const float m_use = grow ? m_new : m_run;
-      const float neg_base = m_use == -INFINITY ? 0.f : -m_use;
-      const float2 scale2 = make_float2(P.scale_log2, P.scale_log2);
-      const float2 nb2 = make_float2(neg_base, neg_base);
-      float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                       make_float2(0.f, 0.f)};
+        for (int e = 0; e < 64; ++e) {
+          const float2 a = ffma2(make_float2(x[2 * e], x[2 * e + 1]), scale2, nb2);
+          const float2 pe = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+          rs2[e & 3] = fadd2(rs2[e & 3], pe);
+          pk[e] = pack_f16x2(pe.x, pe.y);
+        }
+        const float2 rsa = fadd2(fadd2(rs2[0], rs2[1]), fadd2(rs2[2], rs2[3]));
+        return rsa.x + rsa.y;
+      };
+      // ---- online softmax.  The exponentials use the running max m_run as
+      // they are: while the row sum stays <= kSumLimit, no p exceeds it, so P
+      // fits f16 and the row max is not needed.  A row's first item with keys
+      // (m_run = -inf), or a sum above the limit (some logit more than
+      // log2(kSumLimit / 128) above m_run), takes the row max: S is loaded again,
+      // m_run moves to the max, O and l are rescaled, and the warp recomputes its
+      // exponentials (rows that did not move get the same values again).
       uint32_t pk[64];
-#pragma unroll
-      for (int e = 0; e < 64; ++e) {
-        const float2 a = ffma2(make_float2(x[2 * e], x[2 * e + 1]), scale2, nb2);
-        const float2 pe = make_float2(ex2_approx(a.x), ex2_approx(a.y));
-        rs2[e & 3] = fadd2(rs2[e & 3], pe);
-        pk[e] = pack_f16x2(pe.x, pe.y);
+      float rs;
+      {
+        float x[128];
+        logits(x);
+        rs = exps(x, m_run, pk);
       }
-      const float2 rsa = fadd2(fadd2(rs2[0], rs2[1]), fadd2(rs2[2], rs2[3]));
-      const float rs = rsa.x + rsa.y;
-      const bool correct = grow && m_run != -INFINITY;  // O holds earlier items' weight
-      const float alpha = correct ? ex2_approx(m_run - m_new) : 1.f;
-      l_run = (m_run == -INFINITY ? 0.f : l_run * alpha) + rs;
-      m_run = m_use;
+      const bool redo = m_run == -INFINITY || !(rs <= kSumLimit);
+      bool correct = false;
+      float alpha = 1.f;
+      if (__any_sync(0xffffffffu, redo)) {
+        float x[128];
+        logits(x);
+        float mx8[8];  // 8 independent chains of 3-input max
+#pragma unroll
+        for (int a = 0; a < 8; ++a) {
+          float m = fmax3(x[a], x[8 + a], x[16 + a]);
+#pragma unroll
+          for (int e = 24; e < 120; e += 16) m = fmax3(m, x[e + a], x[e + 8 + a]);
+          mx8[a] = fmaxf(m, x[120 + a]);
+        }
+        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                               fmaxf(mx8[6], mx8[7]));
+        if (redo) {
+          const float m_new = fmaxf(m_run, mx * P.scale_log2);
+          correct = m_run != -INFINITY && m_new > m_run;  // O holds earlier items' weight
+          alpha = correct ? ex2_approx(m_run - m_new) : 1.f;
+          l_run *= alpha;
+          m_run = m_new;
+        }
+        rs = exps(x, m_run, pk);
+      }
+      l_run += rs;
       // PV_t(i-1) completed before S_t(i) did (in-order tcgen05), so O_t is ready
       if (__any_sync(0xffffffffu, correct)) {
 #pragma unroll
