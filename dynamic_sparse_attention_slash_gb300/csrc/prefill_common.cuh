@@ -9,7 +9,6 @@ namespace prefill {
 
 constexpr int kTileBytes = 128 * 128 * 2;  // one 128 x 128 16-bit tile (two 64-column halves)
 constexpr int kHalfBytes = kTileBytes / 2;
-constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O when the max grows by > 2^8
 
 __device__ __forceinline__ int unit_batch(const PrefillParams& P, int unit) {
   return unit / P.units.n_heads;

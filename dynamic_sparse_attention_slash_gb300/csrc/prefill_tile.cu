@@ -20,12 +20,13 @@
 //   warp 2     TMA producer for V (one thread)
 //   warp 3     idle
 //   warps 4-11 softmax: warps 4 + w and 8 + w own query rows 32w .. 32w + 31
-//              (TMEM lanes) and split each row's 128 keys into two halves; the
-//              halves exchange their maxima once per item through shared
-//              memory, run the online softmax in fp32 (exp2 with log2(e) folded
-//              into the scale), write P as f16 back over S, rescale their half
-//              of O in TMEM when the row max grows by more than 2^8, and write
-//              their half of the output row.
+//              (TMEM lanes) and split each row's 128 keys into two halves.
+//              They run the online softmax in fp32 (exp2 with log2(e) folded
+//              into the scale) against the row's running max, decide together
+//              once per item (one named barrier) whether a row needs its max
+//              and only then exchange half-row maxima through shared memory,
+//              write P as f16 back over S, rescale their half of O in TMEM when
+//              the running max moves, and write their half of the output row.
 //
 // TMEM (512 columns allocated): two S/P buffers at [0,128) and [128,256) for
 // even and odd items, the output accumulator O at [256,384).  S = Q K^T reads Q
@@ -46,6 +47,8 @@ using namespace prefill;
 constexpr int kThreads = 384;
 constexpr int kStagesK = 3;
 constexpr int kStagesV = 2;
+// A sum of at most 2^15 over a half row bounds each of its p: P fits f16.
+constexpr float kSumLimit = 32768.f;
 // TMEM columns: S/P of item i at kColS + 128 (i & 1), O at kColO
 constexpr uint32_t kColS = 0, kColO = 256;
 
@@ -284,54 +287,26 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
       // A key tile whose quadrant (row half, key half g) is not admitted leaves
       // this warp nothing to do: its half of P is zero, its maximum -inf.
       const bool idle = !((it.qm >> (half * 2 + g)) & 1u);
-      // raw logits (unscaled) of this row's half; scale * log2(e) is folded in below
-      float x[64];
-      float mxh = -INFINITY;
-      if (!idle) {
+      // raw logits (unscaled) of this row's half with the diagonal tile's
+      // causal cut; scale * log2(e) is folded in below
+      auto logits = [&](float (&x)[64]) {
         {
           uint32_t raw[64];
           tmem_ld64(s_col + 64 * g, raw);
 #pragma unroll
           for (int e = 0; e < 64; ++e) x[e] = __uint_as_float(raw[e]);
         }
-        // ---- causal cut on the diagonal tile
         if (it.idx == p) {
 #pragma unroll
           for (int e = 0; e < 64; ++e)
             if (64 * g + e > r) x[e] = -INFINITY;
         }
-        // ---- online softmax (8 independent chains of 3-input max, paired sums)
-        float mx8[8];
-#pragma unroll
-        for (int a = 0; a < 8; ++a) {
-          float m = fmax3(x[a], x[8 + a], x[16 + a]);
-#pragma unroll
-          for (int e = 24; e < 56; e += 16) m = fmax3(m, x[e + a], x[e + 8 + a]);
-          mx8[a] = fmaxf(m, x[56 + a]);
-        }
-        mxh = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                    fmaxf(mx8[6], mx8[7]));
-      }
-      sm.xmax[k & 1][g][r] = mxh;
-      // both warps pass this barrier on every item (every wait above is bounded),
-      // and leave together when either one's wait failed
-      if (!bar_red_and(pair_bar, 64, waited)) {
-        ok = false;
-        break;
-      }
-      const float mx = fmaxf(mxh, sm.xmax[k & 1][g ^ 1][r]);
-      const float m_new = fmaxf(m_run, mx * P.scale_log2);
-      const bool grow = m_new > m_run + kRescaleThreshold;  // false when both are -inf
-      const float m_use = grow ? m_new : m_run;
-      const float neg_base = m_use == -INFINITY ? 0.f : -m_use;
-      uint32_t pk[32];
-      float rs = 0.f;
-      if (idle) {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) pk[e] = 0u;
-      } else {
+      };
+      // p = 2^(z log2(e) - m) as f16 pairs; returns this half's row sum
+      auto exps = [&](const float (&x)[64], float m, uint32_t (&pk)[32]) -> float {
         const float2 scale2 = make_float2(P.scale_log2, P.scale_log2);
-        const float2 nb2 = make_float2(neg_base, neg_base);
+        const float nb = m == -INFINITY ? 0.f : -m;
+        const float2 nb2 = make_float2(nb, nb);
         float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                          make_float2(0.f, 0.f)};
 #pragma unroll
@@ -342,12 +317,61 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
           pk[e] = pack_f16x2(pe.x, pe.y);
         }
         const float2 rsa = fadd2(fadd2(rs2[0], rs2[1]), fadd2(rs2[2], rs2[3]));
-        rs = rsa.x + rsa.y;
+        return rsa.x + rsa.y;
+      };
+      // ---- online softmax.  Both halves of a row exponentiate against the
+      // row's running max m_run as it stands: while each half's sum stays <=
+      // kSumLimit no p exceeds it, so P fits f16 and no row max is needed.  The
+      // two warps of the rows decide together, in the one barrier every item
+      // passes, whether a row needs its max (its first item with keys, or a sum
+      // above the limit) or a wait failed; only then do they load S again,
+      // exchange half-row maxima and move m_run.
+      uint32_t pk[32];
+      float rs = 0.f;
+      bool want = false;
+      if (idle) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pk[e] = 0u;
+      } else {
+        float x[64];
+        logits(x);
+        rs = exps(x, m_run, pk);
+        want = m_run == -INFINITY || !(rs <= kSumLimit);
       }
-      const bool correct = grow && m_run != -INFINITY;  // O holds earlier items' weight
-      const float alpha = correct ? ex2_approx(m_run - m_new) : 1.f;
-      l_run = (m_run == -INFINITY ? 0.f : l_run * alpha) + rs;
-      m_run = m_use;
+      // both warps pass this barrier on every item (every wait above is bounded)
+      bool correct = false;
+      float alpha = 1.f;
+      if (bar_red_or(pair_bar, 64, want || !waited)) {
+        if (!bar_red_and(pair_bar, 64, waited)) {  // both leave when either wait failed
+          ok = false;
+          break;
+        }
+        float x[64];
+        float mxh = -INFINITY;
+        if (!idle) {
+          logits(x);
+          float mx8[8];  // 8 independent chains of 3-input max
+#pragma unroll
+          for (int a = 0; a < 8; ++a) {
+            float m = fmax3(x[a], x[8 + a], x[16 + a]);
+#pragma unroll
+            for (int e = 24; e < 56; e += 16) m = fmax3(m, x[e + a], x[e + 8 + a]);
+            mx8[a] = fmaxf(m, x[56 + a]);
+          }
+          mxh = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                      fmaxf(mx8[6], mx8[7]));
+        }
+        sm.xmax[k & 1][g][r] = mxh;
+        named_bar_sync(pair_bar, 64);
+        const float mx = fmaxf(mxh, sm.xmax[k & 1][g ^ 1][r]);
+        const float m_new = fmaxf(m_run, mx * P.scale_log2);
+        correct = m_run != -INFINITY && m_new > m_run;  // O holds earlier items' weight
+        alpha = correct ? ex2_approx(m_run - m_new) : 1.f;
+        l_run *= alpha;
+        m_run = m_new;
+        if (!idle) rs = exps(x, m_run, pk);
+      }
+      l_run += rs;
       tmem_st32(s_col + 32 * g, pk);  // f16 pairs of keys [64g, 64g + 64)
       // both warps of these rows take this branch together (same maxima)
       if (__any_sync(0xffffffffu, correct)) {

@@ -278,6 +278,17 @@ __device__ __forceinline__ bool bar_red_and(uint32_t id, uint32_t nthreads, bool
       : "memory");
   return out != 0;
 }
+// Named barrier over nthreads threads that also returns the OR of `v` over them.
+__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t nthreads, bool v) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, %2, %3, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(out)
+      : "r"(v ? 1u : 0u), "r"(id), "r"(nthreads)
+      : "memory");
+  return out != 0;
+}
 __device__ __forceinline__ bool elect_one_sync() {
   uint32_t pred = 0;
   asm volatile(
