@@ -51,11 +51,11 @@ UNIT = "TFLOP/s"
 MEASURED_TRAFFIC = {
     "workload": "mixed_128k",
     "kind": "vs",
-    "bytes": 2.519e9 + 0.654e9,
+    "bytes": 2.539e9 + 0.655e9,
     "sources": ("dynamic_sparse_attention_slash_gb300/csrc/prefill.cu",
                 "dynamic_sparse_attention_slash_gb300/csrc/prefill_common.cuh",
                 "dynamic_sparse_attention_slash_gb300/csrc/sm103_ptx.cuh"),
-    "sha256": "764de9d63c2beb9c248ec95cfcb02a0d1eeff721ab1b634ebdc83518d789f5d9",
+    "sha256": "c24b9c26900891013be870e300ca177924726f56a4f190bc2f6059407c104436",
 }
 
 
