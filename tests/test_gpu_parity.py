@@ -61,6 +61,57 @@ def test_streaming_head_subset_leaves_other_heads():
         assert (out[b, 1] == 7.0).all() and (out[b, 2] == 7.0).all()
 
 
+def growth_inputs(N, kind, seed):
+    """Rows whose running max rises far above its first value late in the row.
+
+    Every query shares a direction u (|u| = 8).  "jump": one key late in the
+    sequence gets 2u added, about 16 (log2 units) above every other logit of
+    the rows that see it, so without the row-sum check its p would overflow
+    f16.  "ramp": keys drift along u over the sequence, so a row's max grows
+    by about one log2 unit per 128-key tile (16 in all) and the softmax has to
+    move its running max and rescale O several times along each row.
+    """
+    g = torch.Generator().manual_seed(seed)
+    u = torch.randn(D, generator=g)
+    u = 8 * u / u.norm()
+    q = u + 0.5 * torch.randn(N, D, generator=g)
+    k = 0.3 * torch.randn(N, D, generator=g)
+    if kind == "jump":
+        k[3 * N // 4 + 5] += 2 * u
+    else:
+        k += torch.linspace(0, 2, N)[:, None] * u[None, :]
+    v = torch.randn(N, D, generator=g)
+    return [t.to(torch.bfloat16).reshape(1, 1, N, D).cuda() for t in (q, k, v)]
+
+
+@pytest.mark.parametrize("kind", ["jump", "ramp"])
+def test_softmax_running_max_growth(kind):
+    """Both attention kernels against dense causal attention when the row max
+    grows far after a row's first items: dense streaming and vertical-slash
+    covering every key (two query tiles per CTA), block-sparse keeping every
+    block (one query tile per CTA); row normalisers within the bound the
+    KV-selection tests derive (|d lse| <= 1e-4)."""
+    N = 2048
+    NB = N // 64
+    q, k, v = growth_inputs(N, kind, 40 if kind == "jump" else 41)
+    qn, kn, vn = np64(q)[0, 0], np64(k)[0, 0], np64(v)[0, 0]
+    scale = 1 / math.sqrt(D)
+    ref = O.dense_causal(qn, kn, vn, scale)
+    lse = torch.zeros(1, 1, N, device="cuda")
+    outs = {
+        "streaming": msa.msa_streaming(q, k, v, 0, NB,
+                                       kv_select={"lse": lse, "window": 0, "keep_k": 0}),
+        "vertical-slash": msa.msa_vertical_slash(q, k, v, N, N),
+        "block-sparse": msa.msa_block_sparse(q, k, v, NB),
+    }
+    torch.cuda.synchronize()
+    for name, out in outs.items():
+        P.compare_out(np64(out[0, 0]), ref, f"{kind} {name}")
+    ref_lse = O.row_lse(qn, kn, np.arange(N), lambda m: np.ones(N, dtype=bool), scale)
+    err = np.abs(lse[0, 0].double().cpu().numpy() - ref_lse)
+    assert err.max() <= 1e-4, f"{kind}: lse max err {err.max():.3e}"
+
+
 # ----------------------------------------------------------------------------- block-sparse
 @pytest.mark.parametrize("N,topk", [(2048, 5), (2112, 8), (1024, 100), (4096, 3), (640, 1)])
 def test_block_sparse_matches_oracle(N, topk):
