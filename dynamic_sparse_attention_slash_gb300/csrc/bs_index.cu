@@ -17,12 +17,15 @@ namespace {
 constexpr int kPoolWarps = 4;
 constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
-// Selection with shared key chunks: kSelWarps row blocks per CTA (one warp
-// each) score against pooled key blocks staged kKeyChunk at a time in shared
-// memory (row stride kHeadDim + 1 floats, so the 32 lanes, one key each, read
-// 32 different banks).  Used while the CTA's scores fit: NB <= kRowsMaxNB.
-constexpr int kKeyChunk = 32;
-constexpr int kKStride = kHeadDim + 1;
+// Selection with shared key chunks: kSelWarps row blocks per CTA score against
+// pooled key blocks staged kKeyChunk at a time in shared memory (row stride
+// kHeadDim + 4 floats: 16-byte rows whose float4 reads by eight consecutive
+// lanes cover all 32 banks); warp w takes keys 32 (w % 4) .. + 31 of a chunk
+// (one per lane) against row blocks 4 (w / 4) .. + 3, so each float4 of a key
+// is read once for four rows.  Used while the CTA's scores fit:
+// NB <= kRowsMaxNB.
+constexpr int kKeyChunk = 128;
+constexpr int kKStride = kHeadDim + 4;
 constexpr int kRowsMaxNB = 4096;
 constexpr int kTilesWarps = 4;
 
@@ -167,13 +170,12 @@ __global__ void __launch_bounds__(kSelThreads) bs_select_kernel(const __grid_con
   if (tid == 0) ids[k_earlier] = m;  // the diagonal block, largest id
 }
 
-// One CTA per kSelWarps consecutive row blocks of a unit; warp w owns row
-// block m0 + w: its scores against every earlier block (one lane per key,
-// pooled keys staged in shared memory and shared by the CTA's rows), then the
-// same radix select and ascending compaction as bs_select_kernel, run by the
-// warp alone.
+// One CTA per kSelWarps consecutive row blocks of a unit: the CTA scores its
+// rows against every earlier block (pooled keys staged in shared memory, each
+// lane one key against four rows), then warp w runs row block m0 + w's radix
+// select and ascending compaction alone, as bs_select_kernel does with a CTA.
 __global__ void __launch_bounds__(kSelThreads) bs_select_rows_kernel(const __grid_constant__ SelArgs a) {
-  extern __shared__ float dyn[];
+  extern __shared__ __align__(16) float dyn[];
   float* sc = dyn;                              // [kSelWarps][NB] scores
   float* kc = sc + kSelWarps * a.NB;            // [kKeyChunk][kKStride] pooled keys
   float* qs = kc + kKeyChunk * kKStride;        // [kSelWarps][kHeadDim] pooled queries
@@ -191,24 +193,41 @@ __global__ void __launch_bounds__(kSelThreads) bs_select_rows_kernel(const __gri
   }
   const float* kp = a.kpool + static_cast<int64_t>(b * a.Hkv + hkv) * a.NB * kHeadDim;
   const int n_end = m0 + rows - 1;  // the CTA's last row block scores keys n < n_end
-  const int m = m0 + warp;
+  const int m = m0 + warp;          // the row block this warp selects for
+  const int kg = warp & 3, rg = warp >> 2;  // score phase: key group, row group
   for (int n0 = 0; n0 < n_end; n0 += kKeyChunk) {
     __syncthreads();  // the previous chunk is consumed (and qs is written)
-    for (int i = tid; i < kKeyChunk * kHeadDim; i += kSelThreads) {
-      const int j = i / kHeadDim, c = i % kHeadDim;
-      kc[j * kKStride + c] = n0 + j < n_end ? kp[static_cast<int64_t>(n0 + j) * kHeadDim + c] : 0.f;
+    for (int i = tid; i < kKeyChunk * (kHeadDim / 4); i += kSelThreads) {
+      const int j = i / (kHeadDim / 4), c4 = i % (kHeadDim / 4);
+      const float4 val = n0 + j < n_end
+                             ? reinterpret_cast<const float4*>(kp + static_cast<int64_t>(n0 + j) * kHeadDim)[c4]
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4*>(kc + j * kKStride + 4 * c4) = val;
     }
     __syncthreads();
-    const int n = n0 + lane;
-    if (warp < rows && n < m) {
-      const float* qr = qs + warp * kHeadDim;
-      const float* kr = kc + lane * kKStride;
-      float d = 0.f;
-#pragma unroll 16
-      for (int c = 0; c < kHeadDim; ++c) d = fmaf(qr[c], kr[c], d);
-      sc[warp * a.NB + n] = d * a.scale;
+    const int j = 32 * kg + lane, n = n0 + j;
+    const float* kr = kc + j * kKStride;
+    const float* q0 = qs + 4 * rg * kHeadDim;
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+    for (int c = 0; c < kHeadDim; c += 4) {
+      const float4 kv = *reinterpret_cast<const float4*>(kr + c);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float4 qv = *reinterpret_cast<const float4*>(q0 + r * kHeadDim + c);
+        d[r] = fmaf(qv.x, kv.x, d[r]);
+        d[r] = fmaf(qv.y, kv.y, d[r]);
+        d[r] = fmaf(qv.z, kv.z, d[r]);
+        d[r] = fmaf(qv.w, kv.w, d[r]);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int row = 4 * rg + r;
+      if (row < rows && n < m0 + row) sc[row * a.NB + n] = d[r] * a.scale;
     }
   }
+  __syncthreads();  // every row's scores are written (by other warps)
   if (warp >= rows) return;  // no CTA-wide barrier follows
   __syncwarp();
   int32_t* ids = a.block_ids + (static_cast<int64_t>(unit) * a.NB + m) * a.kb;
