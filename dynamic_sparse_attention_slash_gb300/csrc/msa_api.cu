@@ -391,11 +391,11 @@ int msa_vertical_slash(const msa_tensor* q, const msa_tensor* k, const msa_tenso
   tm.end(MSA_STAGE_ESTIMATE);
   if (e != cudaSuccess) return finish(e, launches);
   tm.begin(MSA_STAGE_TOPK);
-  e = launch_topk(at<float>(ws, L.v_score), c.g.N, c.g.N, c.g.n_units, L.kv,
-                  at<int32_t>(ws, L.vertical), L.kv, c.st, &launches);
-  if (e == cudaSuccess)
-    e = launch_topk(at<float>(ws, L.s_score), c.g.N, c.g.N, c.g.n_units, L.ks,
-                    at<int32_t>(ws, L.slash), L.ks, c.st, &launches);
+  {  // vertical and slash lines in one launch
+    const TopkRows vert{at<float>(ws, L.v_score), c.g.N, L.kv, at<int32_t>(ws, L.vertical), L.kv};
+    const TopkRows slash{at<float>(ws, L.s_score), c.g.N, L.ks, at<int32_t>(ws, L.slash), L.ks};
+    e = launch_topk_pair(c.g.N, c.g.n_units, vert, slash, c.st, &launches);
+  }
   tm.end(MSA_STAGE_TOPK);
   if (e != cudaSuccess) return finish(e, launches);
   tm.begin(MSA_STAGE_INDEX);

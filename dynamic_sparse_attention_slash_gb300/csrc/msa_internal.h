@@ -95,8 +95,17 @@ void note_launches(int n);
 cudaError_t launch_vs_estimate(const Geometry& g, const UnitMap& u, TensorView q, TensorView k,
                                int last_q, float* partial, int n_split, float* row_stats,
                                float* v_score, float* s_score, cudaStream_t st, int* n_launch);
-cudaError_t launch_topk(const float* scores, int64_t n, int64_t row_stride, int rows, int k,
-                        int32_t* out_idx, int64_t out_stride, cudaStream_t st, int* n_launch);
+// Top-k of `rows` score rows of length n for two row sets at once (one launch,
+// one CTA per row of each set).
+struct TopkRows {
+  const float* scores;
+  int64_t row_stride;
+  int k;
+  int32_t* out;
+  int64_t out_stride;
+};
+cudaError_t launch_topk_pair(int64_t n, int rows, const TopkRows& job0, const TopkRows& job1,
+                             cudaStream_t st, int* n_launch);
 // Top-k of the rows of the selected units in [B][Hq][n] scores into [B][Hq][min(k, n)].
 cudaError_t launch_topk_units(const float* scores, int64_t n, int k, int Hq, const UnitMap& u,
                               int units, int32_t* out_idx, cudaStream_t st, int* n_launch);

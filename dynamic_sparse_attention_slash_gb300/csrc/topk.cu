@@ -109,12 +109,17 @@ __device__ __forceinline__ void topk_row(const float* __restrict__ s, int64_t n,
   }
 }
 
-// One CTA per row; row r at scores + r * row_stride.
-__global__ void __launch_bounds__(kThreads) topk_rows_kernel(const float* __restrict__ scores,
-                                                             int64_t n, int64_t row_stride, int k,
-                                                             int32_t* __restrict__ out,
-                                                             int64_t out_stride) {
-  topk_row(scores + static_cast<int64_t>(blockIdx.x) * row_stride, n, k,
+// One CTA per row of one of two row sets (blockIdx.y); row r of set s at
+// jobs[s].scores + r * row_stride.
+__global__ void __launch_bounds__(kThreads, 1) topk_rows_kernel(int64_t n,
+                                                             const __grid_constant__ TopkRows job0,
+                                                             const __grid_constant__ TopkRows job1) {
+  const bool second = blockIdx.y != 0;
+  const float* scores = second ? job1.scores : job0.scores;
+  const int64_t row_stride = second ? job1.row_stride : job0.row_stride;
+  int32_t* out = second ? job1.out : job0.out;
+  const int64_t out_stride = second ? job1.out_stride : job0.out_stride;
+  topk_row(scores + static_cast<int64_t>(blockIdx.x) * row_stride, n, second ? job1.k : job0.k,
            out + static_cast<int64_t>(blockIdx.x) * out_stride);
 }
 
@@ -141,10 +146,10 @@ cudaError_t launch_topk_units(const float* scores, int64_t n, int k, int Hq, con
   return e;
 }
 
-cudaError_t launch_topk(const float* scores, int64_t n, int64_t row_stride, int rows, int k,
-                        int32_t* out_idx, int64_t out_stride, cudaStream_t st, int* n_launch) {
+cudaError_t launch_topk_pair(int64_t n, int rows, const TopkRows& job0, const TopkRows& job1,
+                             cudaStream_t st, int* n_launch) {
   if (rows <= 0) return cudaSuccess;
-  topk_rows_kernel<<<rows, kThreads, 0, st>>>(scores, n, row_stride, k, out_idx, out_stride);
+  topk_rows_kernel<<<dim3(rows, 2), kThreads, 0, st>>>(n, job0, job1);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) ++*n_launch;
   return e;
