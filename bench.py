@@ -51,11 +51,11 @@ UNIT = "TFLOP/s"
 MEASURED_TRAFFIC = {
     "workload": "mixed_128k",
     "kind": "vs",
-    "bytes": 2.539e9 + 0.655e9,
+    "bytes": 2.534e9 + 0.655e9,
     "sources": ("dynamic_sparse_attention_slash_gb300/csrc/prefill.cu",
                 "dynamic_sparse_attention_slash_gb300/csrc/prefill_common.cuh",
                 "dynamic_sparse_attention_slash_gb300/csrc/sm103_ptx.cuh"),
-    "sha256": "c24b9c26900891013be870e300ca177924726f56a4f190bc2f6059407c104436",
+    "sha256": "ce2be635de23fb5e1a8d07fc0412a05202177a390750a8c2069af36ce7415fce",
 }
 
 

@@ -42,6 +42,7 @@ MSA_STAGE_COUNT = 5
 EXPORTED_SYMBOLS = (
     "msa_vertical_slash", "msa_block_sparse", "msa_streaming", "msa_workspace_bytes",
     "msa_device_status", "msa_status_string", "msa_kernel_launches", "msa_mass_recall",
+    "msa_selftest_wait_timeout",
 )
 
 
@@ -112,6 +113,8 @@ def load_library():
                                     ctypes.c_int64, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32,
                                     F, ctypes.c_void_p]
     lib.msa_mass_recall.restype = ctypes.c_int
+    lib.msa_selftest_wait_timeout.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+    lib.msa_selftest_wait_timeout.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -148,6 +151,23 @@ def workspace_bytes(kind: int, q: torch.Tensor, k: torch.Tensor, p0: int = 0, p1
     lib = load_library()
     qt, kt = describe(q), describe(k)
     return int(lib.msa_workspace_bytes(kind, ctypes.byref(qt), ctypes.byref(kt), p0, p1, n_heads))
+
+
+def selftest_wait_timeout(limit_us: int = 2000, stream=None, device=None) -> dict:
+    """Runs the library's bounded-wait self-test (msa_selftest_wait_timeout) and
+    reads its outcome: {"status": msa_device_status's code (MSA_ERR_TIMEOUT
+    expected), "control_ok": the control wait succeeded, "waited_us": how long
+    the abandoned wait lasted}."""
+    lib = load_library()
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    ws = torch.zeros(64, dtype=torch.int32, device=dev)  # 256 bytes; allocations are 256-byte aligned
+    rc = int(lib.msa_selftest_wait_timeout(ctypes.c_void_p(ws.data_ptr()), int(limit_us),
+                                           ctypes.c_void_p(_stream_ptr(stream))))
+    if rc != MSA_OK:
+        raise MsaError(rc, "msa_selftest_wait_timeout")
+    status = device_status(ws, stream)  # synchronises the stream, then clears word 0 only
+    words = ws[1:3].cpu()
+    return {"status": status, "control_ok": bool(int(words[0]) == 1), "waited_us": int(words[1])}
 
 
 def device_status(workspace: torch.Tensor, stream=None) -> int:

@@ -279,6 +279,22 @@ size_t msa_workspace_bytes(int kind, const msa_tensor* q, const msa_tensor* k, i
  */
 int msa_device_status(void* workspace, void* stream);
 
+/*
+ * Self-test of the bounded device-side waits behind MSA_ERR_TIMEOUT: enqueues
+ * on `stream` one 32-thread CTA that waits, with a limit of `limit_us`
+ * microseconds (1 .. 1000000), on an mbarrier nothing arrives at, and on a
+ * control mbarrier its own threads complete.  The first wait gives up and sets
+ * the timeout bit of the status word at `workspace`, so msa_device_status
+ * (workspace, stream) then returns MSA_ERR_TIMEOUT.  It also writes two 32-bit
+ * words after the status word: word 1 = 1 if the control wait succeeded, word
+ * 2 = microseconds the first wait lasted.  `workspace`: device memory of at
+ * least 256 bytes, 256-byte aligned, caller-owned (a call's workspace will do).
+ * Nothing faults or hangs: the waits are bounded and no copy or tensor-core
+ * work is in flight.  Returns MSA_OK when enqueued, MSA_ERR_INVALID for a bad
+ * pointer or limit, MSA_ERR_CUDA if the launch failed.
+ */
+int msa_selftest_wait_timeout(void* workspace, int64_t limit_us, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* msa_status_string(int status);
 

@@ -186,3 +186,14 @@ def test_binding_refuses_buffers_the_library_would_overrun():
     with pytest.raises(ValueError):
         msa._check_buffers(Q, msa.MSA_KIND_STREAMING, 0, 0, None, None,
                            {"lse": torch.zeros(4000), "window": 1, "keep_k": 0})
+
+
+def test_selftest_wait_timeout_rejects_on_host(lib):
+    """Bad arguments are refused before anything is launched."""
+    import ctypes
+    from dynamic_sparse_attention_slash_gb300 import msa
+    ok_ptr = ctypes.c_void_p(0x100000)  # never dereferenced: every case below is refused
+    assert lib.msa_selftest_wait_timeout(None, 1000, None) == msa.MSA_ERR_INVALID
+    assert lib.msa_selftest_wait_timeout(ctypes.c_void_p(0x100010), 1000, None) == msa.MSA_ERR_INVALID
+    assert lib.msa_selftest_wait_timeout(ok_ptr, 0, None) == msa.MSA_ERR_INVALID
+    assert lib.msa_selftest_wait_timeout(ok_ptr, 1000001, None) == msa.MSA_ERR_INVALID
