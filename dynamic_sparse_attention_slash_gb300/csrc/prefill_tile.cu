@@ -263,9 +263,9 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
     // ------------------------------------------------------------ softmax
     // Warps 4 + w and 8 + w share TMEM lanes 32w .. 32w + 31 (query rows) and
     // split the columns: warpgroup g takes keys [64g, 64g + 64) of each item and
-    // output dimensions [64g, 64g + 64).  The two halves of a row exchange their
-    // maxima through shared memory once per item, so both keep the same
-    // running max; their row sums are added at the end.
+    // output dimensions [64g, 64g + 64).  Both halves of a row keep the same
+    // running max (they move it together, exchanging half-row maxima through
+    // shared memory); their row sums are added at the end.
     const int g = (warp - 4) >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;        // query row within the tile == TMEM lane
