@@ -17,9 +17,11 @@ namespace msa {
 namespace {
 
 using namespace mma16;
-constexpr int kChunk = 128;       // keys (and diagonals) owned by one second-pass CTA
+constexpr int kChunk = 256;       // keys (and diagonals) owned by one second-pass CTA
 constexpr int kWindow = kChunk + kKeyTile;  // keys a second-pass CTA computes
+constexpr int kWinTiles = kWindow / kKeyTile;
 constexpr int kAStride = kWindow + 4;       // fp32 row stride of the probability tile
+constexpr int kScoreThreads = 256;          // two groups of four warps, alternate key tiles
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct EstArgs {
@@ -125,13 +127,14 @@ __global__ void __launch_bounds__(kThreads) vs_estimate_stats_kernel(const __gri
   }
 }
 
-// Pass 2: probabilities for keys [j0, j0 + 192), then column sums for the owned
-// keys [j0, j0 + 128) and diagonal sums for the owned offsets.
-__global__ void __launch_bounds__(kThreads) vs_estimate_scores_kernel(const __grid_constant__ EstArgs a) {
+// Pass 2: probabilities for keys [j0, j0 + 320) (the owned keys [j0, j0 + 256)
+// and the 64 after them, which the owned diagonals reach), then column sums for
+// the owned keys and diagonal sums for the owned offsets.
+__global__ void __launch_bounds__(kScoreThreads) vs_estimate_scores_kernel(const __grid_constant__ EstArgs a) {
   extern __shared__ __align__(1024) uint8_t dyn[];
   uint8_t* sm_q = dyn;                          // 16 KB
-  uint8_t* sm_k = dyn + 64 * 256;               // 2 x 16 KB
-  float* sm_a = reinterpret_cast<float*>(dyn + 64 * 256 + 2 * kKeyTile * 256);  // 64 x kAStride
+  uint8_t* sm_k = dyn + 64 * 256;               // 4 x 16 KB: two key tiles per step, two steps
+  float* sm_a = reinterpret_cast<float*>(dyn + 64 * 256 + 4 * kKeyTile * 256);  // 64 x kAStride
   __shared__ float s_m[64], s_linv[64];
   const int unit = blockIdx.y, chunk = blockIdx.x;
   const int N = a.g.N;
@@ -140,8 +143,10 @@ __global__ void __launch_bounds__(kThreads) vs_estimate_scores_kernel(const __gr
   unit_ptrs(a, unit, qb, kb);
   const int row0 = N - 64;
   const uint32_t q_s = smem_u32(sm_q);
+  auto k_buf = [&](int i) { return smem_u32(sm_k + i * kKeyTile * 256); };
   load_rows(q_s, qb, a.q_sn, row0, 64, N);
-  load_rows(smem_u32(sm_k), kb, a.k_sn, j0, kKeyTile, N);
+  load_rows(k_buf(0), kb, a.k_sn, j0, kKeyTile, N);
+  load_rows(k_buf(1), kb, a.k_sn, j0 + kKeyTile, kKeyTile, N);
   cp_async_commit();
   // combine the first pass: m = max_s m_s, l = sum_s l_s 2^(m_s - m)
   if (threadIdx.x < 64) {
@@ -157,32 +162,41 @@ __global__ void __launch_bounds__(kThreads) vs_estimate_scores_kernel(const __gr
   }
   cp_async_wait_all();
   __syncthreads();
-  uint32_t qa[8][4];
-  load_q_frags(q_s, qa);
+  // warp w: query rows 16 (w % 4) .. + 15 of key tiles w / 4, w / 4 + 2, ...
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int rA = warp * 16 + (lane >> 2), rB = rA + 8;
+  const int grp = warp >> 2, wq = warp & 3;
+  uint32_t qa[8][4];
+  load_q_frags(q_s, qa, wq);
+  const int rA = wq * 16 + (lane >> 2), rB = rA + 8;
   const int iA = row0 + rA, iB = row0 + rB;
   const bool vA = rA >= 64 - a.last_q, vB = rB >= 64 - a.last_q;
   const float mA = s_m[rA], mB = s_m[rB], liA = s_linv[rA], liB = s_linv[rB];
-  constexpr int kTiles = kWindow / kKeyTile;
-  for (int t = 0; t < kTiles; ++t) {
-    const int buf = t & 1;
-    if (t + 1 < kTiles)
-      load_rows(smem_u32(sm_k + (buf ^ 1) * kKeyTile * 256), kb, a.k_sn, j0 + (t + 1) * kKeyTile,
-                kKeyTile, N);
+  constexpr int kSteps = (kWinTiles + 1) / 2;
+  for (int step = 0; step < kSteps; ++step) {
+    const int buf = step & 1;
+    if (step + 1 < kSteps) {  // the next step's two tiles into the other buffer pair
+      for (int g2 = 0; g2 < 2; ++g2) {
+        const int tn = 2 * (step + 1) + g2;
+        if (tn < kWinTiles)
+          load_rows(k_buf((buf ^ 1) * 2 + g2), kb, a.k_sn, j0 + tn * kKeyTile, kKeyTile, N);
+      }
+    }
     cp_async_commit();
-    float acc[8][4];
-    tile_logits(qa, smem_u32(sm_k + buf * kKeyTile * 256), acc);
+    const int t = 2 * step + grp;
+    if (t < kWinTiles) {
+      float acc[8][4];
+      tile_logits(qa, k_buf(buf * 2 + grp), acc);
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+      for (int nt = 0; nt < 8; ++nt) {
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int col = t * kKeyTile + nt * 8 + 2 * (lane & 3) + e;
-        const int j = j0 + col;
-        const float pA = (vA && j <= iA) ? ex2_approx(acc[nt][e] * a.scale_log2 - mA) * liA : 0.f;
-        const float pB = (vB && j <= iB) ? ex2_approx(acc[nt][2 + e] * a.scale_log2 - mB) * liB : 0.f;
-        sm_a[rA * kAStride + col] = pA;
-        sm_a[rB * kAStride + col] = pB;
+        for (int e = 0; e < 2; ++e) {
+          const int col = t * kKeyTile + nt * 8 + 2 * (lane & 3) + e;
+          const int j = j0 + col;
+          const float pA = (vA && j <= iA) ? ex2_approx(acc[nt][e] * a.scale_log2 - mA) * liA : 0.f;
+          const float pB = (vB && j <= iB) ? ex2_approx(acc[nt][2 + e] * a.scale_log2 - mB) * liB : 0.f;
+          sm_a[rA * kAStride + col] = pA;
+          sm_a[rB * kAStride + col] = pB;
+        }
       }
     }
     cp_async_wait_all();
@@ -236,7 +250,7 @@ cudaError_t launch_vs_estimate(const Geometry& g, const UnitMap& u, TensorView q
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ++*n_launch;
-  const int smem = 64 * 256 + 2 * kKeyTile * 256 + 64 * kAStride * 4;
+  const int smem = 64 * 256 + 4 * kKeyTile * 256 + 64 * kAStride * 4;
   static bool attr_set = false;
   if (!attr_set) {
     e = cudaFuncSetAttribute(vs_estimate_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -244,7 +258,7 @@ cudaError_t launch_vs_estimate(const Geometry& g, const UnitMap& u, TensorView q
     attr_set = true;
   }
   const int n_chunks = (g.N + kChunk - 1) / kChunk;
-  vs_estimate_scores_kernel<<<dim3(n_chunks, g.n_units), kThreads, smem, st>>>(a);
+  vs_estimate_scores_kernel<<<dim3(n_chunks, g.n_units), kScoreThreads, smem, st>>>(a);
   e = cudaGetLastError();
   if (e == cudaSuccess) ++*n_launch;
   return e;

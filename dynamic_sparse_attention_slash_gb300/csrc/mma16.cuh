@@ -52,12 +52,17 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], 
 }
 
 // Q fragments of this warp's 16 estimate rows, all 8 k-steps.
-__device__ __forceinline__ void load_q_frags(uint32_t q_smem, uint32_t (&qa)[8][4]) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int row = warp * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+// A fragments of query rows 16 g .. 16 g + 15 (row group g) for all 128 dims.
+__device__ __forceinline__ void load_q_frags(uint32_t q_smem, uint32_t (&qa)[8][4], int g) {
+  const int lane = threadIdx.x & 31;
+  const int row = g * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)
     ldsm_x4(q_smem + swz(row, 2 * kk + (lane >> 4)), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+}
+// Row group = warp index (kThreads = 4 warps x 16 rows).
+__device__ __forceinline__ void load_q_frags(uint32_t q_smem, uint32_t (&qa)[8][4]) {
+  load_q_frags(q_smem, qa, static_cast<int>(threadIdx.x >> 5));
 }
 
 // acc[nt][*] = this warp's 16 rows x 64 keys of Q K^T (raw dot products).
