@@ -35,7 +35,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 from dynamic_sparse_attention_slash_gb300 import inputs  # noqa: E402
-from dynamic_sparse_attention_slash_gb300.flops import bs_pairs, st_pairs, vs_pairs  # noqa: E402,F401
+from dynamic_sparse_attention_slash_gb300.flops import (  # noqa: E402,F401
+    bs_pairs, st_pairs, vs_exact_line_pairs, vs_pairs)
 
 D = 128
 METRIC = "sparse prefill attention effective TFLOP/s at 128K tokens"
@@ -214,6 +215,24 @@ def oracle_sample(w, q, k, v, heads, rows_per_head: int, seed: int = 0):
     return flops, secs, label
 
 
+def cpu_description() -> dict:
+    """The host CPU the oracle ran on: architecture, model (as /proc/cpuinfo
+    names it, when it does) and the logical CPU count."""
+    import platform
+    model = None
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                key = line.split(":", 1)[0].strip().lower()
+                if key in ("model name", "cpu part", "hardware"):
+                    model = line.split(":", 1)[1].strip()
+                    if key == "model name":
+                        break
+    except OSError:
+        pass
+    return {"machine": platform.machine(), "model": model, "os_cpu_count": os.cpu_count()}
+
+
 def cpu_threads() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -260,7 +279,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="mixed_128k", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=10)
-    ap.add_argument("--cpu-rows", type=int, default=48, help="oracle rows per head (cpu_baseline)")
+    ap.add_argument("--cpu-rows", type=int, default=512, help="oracle rows per head (cpu_baseline)")
     ap.add_argument("--ref-rows", type=int, default=24, help="oracle rows per head (reference arm)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
@@ -324,15 +343,19 @@ def main():
     export = {}
     if U_vs:
         export["vs"] = {"vertical": torch.empty(U_vs, min(w.vertical_topk, N), dtype=torch.int32, device=dev),
+                        "slash": torch.empty(U_vs, min(w.slash, N), dtype=torch.int32, device=dev),
                         "tile_dist": torch.empty(U_vs, ((N + 63) // 64 + 32) // 32, dtype=torch.int32, device=dev)}
     if U_bs:
         export["bs"] = {"block_count": torch.empty(U_bs, (N + 63) // 64, dtype=torch.int32, device=dev)}
     step(export=export)
     torch.cuda.synchronize()
     pairs = {"vs": 0, "bs": 0, "st": 0}
+    exact_line = 0  # vertical-slash pairs on the chosen lines alone (diagnostic)
     if U_vs:
         td, vt = export["vs"]["tile_dist"].cpu().numpy(), export["vs"]["vertical"].cpu().numpy()
+        sl = export["vs"]["slash"].cpu().numpy()
         pairs["vs"] = sum(vs_pairs(td[u], vt[u], N) for u in range(U_vs))
+        exact_line = sum(vs_exact_line_pairs(vt[u], sl[u], N) for u in range(U_vs))
     if U_bs:
         pairs["bs"] = bs_pairs(export["bs"]["block_count"].cpu().numpy(), N)
     if heads["st"]:
@@ -504,7 +527,7 @@ def main():
         qc, kc, vc = q.cpu(), k.cpu(), v.cpu()
         f, secs, label = oracle_sample(w, qc, kc, vc, heads, args.cpu_rows)
         cpu = {"value": f / secs / 1e12, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-               "sample": label, "seconds": secs}
+               "sample": label, "seconds": secs, "cpu": cpu_description()}
 
     if rank == 0:
         line = {
@@ -526,6 +549,7 @@ def main():
             "stage_ms": stage_ms,
             "effective_tflop": {kk_: vv_ / 1e12 for kk_, vv_ in flops.items()},
             "density_vs_dense_causal": sum(pairs.values()) / dense_pairs,
+            "vs_exact_line_pairs_fraction": (exact_line / pairs["vs"]) if pairs["vs"] else None,
             "dense_causal": dense,
             "device_status": status,
             "kv_select": kvsel,

@@ -47,6 +47,19 @@ def vs_pairs(tile_dist_words, vertical, N: int) -> int:
     return total
 
 
+def vs_exact_line_pairs(vertical, slash, N: int) -> int:
+    """Pairs (i, j), j <= i < N, on the chosen lines themselves: j a chosen
+    vertical column or i - j a chosen slash offset, without the expansion to
+    64x64 tiles that the kernels compute (a diagnostic of the sparse format's
+    overhead).  Column j covers rows j .. N-1 (N - j pairs), offset o covers
+    rows o .. N-1 (N - o pairs), and a pair on both a column j and an offset o
+    (j + o <= N - 1) is counted once."""
+    V = np.sort(np.asarray(vertical, dtype=np.int64))
+    S = np.asarray(slash, dtype=np.int64)
+    both = int(np.searchsorted(V, N - S, side="left").sum())  # per o: columns j < N - o
+    return int((N - V).sum() + (N - S).sum() - both)
+
+
 def bs_pairs(block_count, N: int | None = None) -> int:
     """Pairs of a block-sparse head (or stacked heads) from its per-row-block
     kept-block counts [.., NB]: the diagonal block triangular, the others full.

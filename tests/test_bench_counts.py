@@ -60,3 +60,17 @@ def test_measured_traffic_is_tied_to_kernel_source(monkeypatch):
     stale = dict(bench.MEASURED_TRAFFIC, sha256="0" * 64)
     monkeypatch.setattr(bench, "MEASURED_TRAFFIC", stale)
     assert bench.measured_traffic("mixed_128k", "vs") is None
+
+
+@pytest.mark.parametrize("N,nv,ns,seed", [(300, 20, 30, 1), (130, 130, 5, 2), (64, 1, 64, 3), (1000, 0, 7, 4)])
+def test_exact_line_pairs_brute_force(N, nv, ns, seed):
+    """The exact-line count (chosen columns and offsets without tile expansion)
+    against the N x N causal mask built element by element."""
+    import bench
+    rng = np.random.default_rng(seed)
+    V = np.sort(rng.choice(N, size=nv, replace=False)) if nv else np.zeros(0, np.int64)
+    S = np.sort(rng.choice(N, size=ns, replace=False))
+    i = np.arange(N)[:, None]
+    j = np.arange(N)[None, :]
+    mask = (j <= i) & (np.isin(j, V) | np.isin(i - j, S))
+    assert bench.vs_exact_line_pairs(V, S, N) == int(mask.sum())
