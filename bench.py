@@ -279,7 +279,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="mixed_128k", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=10)
-    ap.add_argument("--cpu-rows", type=int, default=512, help="oracle rows per head (cpu_baseline)")
+    ap.add_argument("--cpu-rows", type=int, default=1536, help="oracle rows per head (cpu_baseline)")
     ap.add_argument("--ref-rows", type=int, default=24, help="oracle rows per head (reference arm)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
