@@ -404,7 +404,9 @@ def main():
             vals = [ev[kind][2 * si].elapsed_time(ev[kind][2 * si + 1]) for ev in ev_sets]
             stage_ms[f"{kind}_{nm}"] = sum(vals) / len(vals)
 
-    # ---- roofline of the dominant kernel (vertical-slash sparse prefill)
+    # ---- roofline of the dominant kernel: the first head kind present of
+    # vertical-slash, block-sparse, streaming (the block-sparse heads run the
+    # one-tile kernel, the others the two-tile kernel)
     peaks = {}
     try:
         peaks = _json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -416,7 +418,7 @@ def main():
     achieved = flops[dom] / (dom_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": measured_traffic(args.workload, dom),
-                "kernel": "sparse_prefill_kernel",
+                "kernel": "sparse_prefill_tile_kernel" if dom == "bs" else "sparse_prefill_kernel",
                 "peak_source": peak_src,
                 "frac_of_burst": achieved / float(peaks.get("bf16_tflops", 1900.0))}
 
