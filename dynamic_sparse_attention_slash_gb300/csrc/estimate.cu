@@ -251,12 +251,9 @@ cudaError_t launch_vs_estimate(const Geometry& g, const UnitMap& u, TensorView q
   if (e != cudaSuccess) return e;
   ++*n_launch;
   const int smem = 64 * 256 + 4 * kKeyTile * 256 + 64 * kAStride * 4;
-  static bool attr_set = false;
-  if (!attr_set) {
-    e = cudaFuncSetAttribute(vs_estimate_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // per call: the attribute belongs to the current device
+  e = cudaFuncSetAttribute(vs_estimate_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
   const int n_chunks = (g.N + kChunk - 1) / kChunk;
   vs_estimate_scores_kernel<<<dim3(n_chunks, g.n_units), kScoreThreads, smem, st>>>(a);
   e = cudaGetLastError();

@@ -158,16 +158,13 @@ cudaError_t launch_kv_score(const Geometry& g, const UnitMap& u, TensorView q, T
   a.scale_log2 = g.scale * kLog2e;
   a.mask = mask;
   const int smem = 64 * 256 + kChunk * 256 + 64 * kPStride * 4;
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(kv_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // per call: the attribute belongs to the current device
+  cudaError_t e =
+      cudaFuncSetAttribute(kv_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
   const int n_chunks = (g.N + kChunk - 1) / kChunk;
   kv_score_kernel<<<dim3(n_chunks, g.n_units), kThreads, smem, st>>>(a);
-  const cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e == cudaSuccess) ++*n_launch;
   return e;
 }
