@@ -136,6 +136,41 @@ def test_block_sparse_matches_oracle(N, topk):
         P.compare_out(np64(out[0, h]), ref, f"bs h{h}")
 
 
+def test_block_sparse_batch_and_head_subset():
+    """A batch of two with a head subset on a ragged length (an odd number of
+    128-row query tiles, the last one half real): the one-tile kernel's (batch,
+    head) units and their tile lists, every other head left untouched."""
+    N, topk, heads = 1088, 6, [3, 0]
+    q, k, v = qkv(2, 4, 2, N, 18, vs=False, bs=True)
+    out = torch.full_like(q, 7.0)
+    NB = (N + 63) // 64
+    U = 2 * len(heads)
+    ex = {"block_count": torch.empty(U, NB, dtype=torch.int32, device="cuda"),
+          "block_ids": torch.empty(U, NB, min(topk, NB), dtype=torch.int32, device="cuda")}
+    msa.msa_block_sparse(q, k, v, topk, out, heads=heads, export=ex)
+    torch.cuda.synchronize()
+    qn, kn, vn = np64(q), np64(k), np64(v)
+    counts, ids = ex["block_count"].cpu().numpy(), ex["block_ids"].cpu().numpy()
+    for b in range(2):
+        for t, h in enumerate(heads):
+            u, g = b * len(heads) + t, h // 2
+            _, S = O.block_sparse_blocks(qn[b, h], kn[b, g], topk)
+            sel = []
+            for m in range(NB):
+                cnt = int(counts[u, m])
+                assert cnt == min(topk, m + 1)
+                got = ids[u, m, :cnt]
+                assert got[-1] == m, "diagonal block must be kept"
+                if m > 0:
+                    P.check_topk(got[:-1], S[m, :m], topk - 1, f"b{b} h{h} m{m}")
+                sel.append(got.astype(np.int64))
+            ref, _ = O.attend_blocks(qn[b, h], kn[b, g], vn[b, g], O.block_mask_from_blocks(sel, N),
+                                     1 / math.sqrt(D))
+            P.compare_out(np64(out[b, h]), ref, f"bs b{b} h{h}")
+        for h in (1, 2):
+            assert (out[b, h] == 7.0).all(), f"head {h} outside the subset was written"
+
+
 @pytest.mark.parametrize("NB", [4096, 4097])
 def test_block_sparse_selection_at_long_lengths(NB):
     """The block selection runs as CTAs of eight row blocks sharing staged key
