@@ -59,7 +59,7 @@ extern "C" {
 /* Status codes. */
 #define MSA_OK 0
 #define MSA_ERR_INVALID 1     /* bad pointer, shape, stride or parameter value */
-#define MSA_ERR_UNSUPPORTED 2 /* valid but outside what this build handles (D != 128, N > 2^21) */
+#define MSA_ERR_UNSUPPORTED 2 /* valid but outside what the library handles (D != 128, N > 2^21) */
 #define MSA_ERR_WORKSPACE 3   /* workspace missing, misaligned or too small */
 #define MSA_ERR_CUDA 4        /* a CUDA call or kernel launch failed */
 #define MSA_ERR_TIMEOUT 5     /* a bounded device-side wait gave up (read by msa_device_status) */
