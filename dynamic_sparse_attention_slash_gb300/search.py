@@ -115,3 +115,42 @@ def search(q, k, v, candidates: Dict[str, list], budget_flops: float, *,
         p = order[choose_pattern(best)]
         assignment[u] = (p, candidates[p][records[u][p]["setting"]])
     return {"assignment": assignment, "records": records, "ms": ms}
+
+
+def assignment_groups(assignment: dict, n_heads: int) -> list:
+    """Groups a search assignment {(b, h): (pattern, setting)} into calls:
+    [(pattern, setting, [heads ascending])], one per distinct (pattern,
+    setting).  A head must have the same assignment in every batch entry (the
+    entry points select heads for the whole batch); every head in [0, n_heads)
+    must be assigned."""
+    per_head = {}
+    for (b, h), ps in assignment.items():
+        p, setting = ps
+        if p not in PATTERNS:
+            raise ValueError(f"unknown pattern {p!r}")
+        setting = tuple(setting) if isinstance(setting, (list, tuple)) else setting
+        if per_head.setdefault(h, (p, setting)) != (p, setting):
+            raise ValueError(f"head {h} has different assignments across the batch")
+    if sorted(per_head) != list(range(n_heads)):
+        raise ValueError("every query head must be assigned exactly once")
+    groups = {}
+    for h in sorted(per_head):
+        groups.setdefault(per_head[h], []).append(h)
+    return [(p, setting, heads) for (p, setting), heads in groups.items()]
+
+
+def apply_assignment(q, k, v, assignment: dict, out=None, *, last_q: int = 64, stream=None):
+    """Runs attention with each head's searched pattern (the output of search()
+    or any {(b, h): (pattern, setting)} map): one library call per distinct
+    (pattern, setting) on its heads, all writing into one output tensor."""
+    out = torch.empty_like(q) if out is None else out
+    for p, setting, heads in assignment_groups(assignment, q.shape[1]):
+        if p == "vs":
+            msa.msa_vertical_slash(q, k, v, setting[0], setting[1], out, last_q=last_q,
+                                   heads=heads, stream=stream)
+        elif p == "bs":
+            msa.msa_block_sparse(q, k, v, setting, out, heads=heads, stream=stream)
+        else:
+            msa.msa_streaming(q, k, v, setting[0], setting[1], out, heads=heads, stream=stream)
+    return out
+

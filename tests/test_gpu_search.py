@@ -106,3 +106,26 @@ def test_mass_recall_dense_is_one_and_subset_heads():
             ref_r = O.mass_recall(qn[b, h], kn[b, h // 2], np.arange(N - 64, N), mask,
                                   1 / math.sqrt(D)).mean()
             assert abs(float(recall[b, h]) - ref_r) <= R_REL * ref_r + R_ABS
+
+
+def test_apply_assignment_matches_individual_calls():
+    """The searched per-head patterns applied in one call give exactly the
+    outputs of the three entry points called on their head groups."""
+    N = 1024
+    q, k, v = inputs.make_qkv(1, 4, 2, N, 33, vs_planting=True, bs_planting=True, device="cpu")
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    a = {(0, 0): ("vs", (64, 96)), (0, 1): ("bs", 4), (0, 2): ("st", (1, 4)),
+         (0, 3): ("vs", (64, 96))}
+    out = search.apply_assignment(q, k, v, a)
+    ref = torch.empty_like(q)
+    msa.msa_vertical_slash(q, k, v, 64, 96, ref, heads=[0, 3])
+    msa.msa_block_sparse(q, k, v, 4, ref, heads=[1])
+    msa.msa_streaming(q, k, v, 1, 4, ref, heads=[2])
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    # and straight from a search result
+    res = search.search(q, k, v, {"vs": [(64, 32)], "bs": [2, 4], "st": [(1, 2)]},
+                        0.25 * 4 * D * N * (N + 1) / 2)
+    out2 = search.apply_assignment(q, k, v, res["assignment"])
+    torch.cuda.synchronize()
+    assert torch.isfinite(out2.float()).all()
