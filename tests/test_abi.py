@@ -197,3 +197,21 @@ def test_selftest_wait_timeout_rejects_on_host(lib):
     assert lib.msa_selftest_wait_timeout(ctypes.c_void_p(0x100010), 1000, None) == msa.MSA_ERR_INVALID
     assert lib.msa_selftest_wait_timeout(ok_ptr, 0, None) == msa.MSA_ERR_INVALID
     assert lib.msa_selftest_wait_timeout(ok_ptr, 1000001, None) == msa.MSA_ERR_INVALID
+
+
+def _build_c_example(out_path):
+    """Compiles include/msa_example.cu against the in-tree libmsa.so."""
+    import subprocess
+    from dynamic_sparse_attention_slash_gb300 import build
+    build.build()
+    pkg = os.path.dirname(build.LIB_PATH)
+    cmd = [build.nvcc(), "-std=c++17", *build.ARCH, "-I", os.path.join(ROOT, "include"),
+           os.path.join(ROOT, "include", "msa_example.cu"), "-L", pkg, "-l:libmsa.so",
+           "-Xlinker", f"-rpath={pkg}", "-o", str(out_path)]
+    return subprocess.run(cmd, capture_output=True, text=True)
+
+
+def test_c_example_compiles_and_links(tmp_path):
+    """The C ABI is usable from C++ alone: the example builds and links."""
+    r = _build_c_example(tmp_path / "msa_example")
+    assert r.returncode == 0, r.stderr[-2000:]
