@@ -44,6 +44,20 @@ int check_tensor(const msa_tensor* t) {
   return MSA_OK;
 }
 
+// Byte range [lo, hi) that a tensor view spans (validated views: non-negative
+// strides, so the last element is at the sum of the highest indices' offsets).
+struct Span {
+  uintptr_t lo, hi;
+};
+
+Span span(const msa_tensor* t) {
+  const int64_t last = (t->B - 1) * t->sb + (t->H - 1) * t->sh + (t->N - 1) * t->sn + t->D;
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(t->data);
+  return {lo, lo + static_cast<uintptr_t>(last) * 2};
+}
+
+bool overlap(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi; }
+
 struct Call {
   Geometry g;
   UnitMap u;
@@ -51,6 +65,7 @@ struct Call {
   int last_q;
   float scale;
   const msa_opts* opts;
+  Span tensors[4];  // q, k, v, out
 };
 
 int prepare(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v, const msa_tensor* out,
@@ -63,6 +78,9 @@ int prepare(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v, const
   if (k->N != q->N || v->N != q->N || out->N != q->N) return MSA_ERR_INVALID;
   if (v->H != k->H || out->H != q->H) return MSA_ERR_INVALID;
   if (q->H % k->H != 0) return MSA_ERR_INVALID;
+  // out is written while q, k and v are still read (and q again by KV selection)
+  const Span so = span(out);
+  if (overlap(so, span(q)) || overlap(so, span(k)) || overlap(so, span(v))) return MSA_ERR_INVALID;
   if (opts && opts->flags != 0) return MSA_ERR_INVALID;
   if (const msa_kv_select* kv = opts ? opts->kv_select : nullptr) {
     if (!kv->lse || !aligned(kv->lse, 4)) return MSA_ERR_INVALID;
@@ -72,6 +90,10 @@ int prepare(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v, const
     if (kv->keep && (!aligned(kv->keep, 4) || kv->keep_k < 1)) return MSA_ERR_INVALID;
   }
   c.opts = opts;
+  c.tensors[0] = span(q);
+  c.tensors[1] = span(k);
+  c.tensors[2] = span(v);
+  c.tensors[3] = so;
   c.st = opts ? static_cast<cudaStream_t>(opts->stream) : nullptr;
   c.last_q = (opts && opts->last_q) ? static_cast<int>(opts->last_q) : kLastQMax;
   if (opts && (opts->last_q < 0 || opts->last_q > kLastQMax)) return MSA_ERR_INVALID;
@@ -208,10 +230,14 @@ STLayout st_layout(const Geometry& g) {
   return L;
 }
 
-int check_workspace(const msa_opts* opts, size_t need) {
+int check_workspace(const Call& c, size_t need) {
+  const msa_opts* opts = c.opts;
   if (!opts || !opts->workspace) return MSA_ERR_WORKSPACE;
   if (!aligned(opts->workspace, 256)) return MSA_ERR_WORKSPACE;
   if (opts->workspace_bytes < need) return MSA_ERR_WORKSPACE;
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(opts->workspace);
+  for (const Span& t : c.tensors)
+    if (overlap({lo, lo + need}, t)) return MSA_ERR_WORKSPACE;
   return MSA_OK;
 }
 
@@ -371,7 +397,7 @@ int msa_vertical_slash(const msa_tensor* q, const msa_tensor* k, const msa_tenso
   if (s) return s;
   if (vertical_topk <= 0 || slash <= 0) return MSA_ERR_INVALID;
   const VSLayout L = vs_layout(c.g, vertical_topk, slash);
-  if ((s = check_workspace(opts, L.total))) return s;
+  if ((s = check_workspace(c, L.total))) return s;
   void* ws = opts->workspace;
   CUtensorMap mq, mk, mv, mkc, mvc;
   const int64_t crow = static_cast<int64_t>(c.g.n_units) * L.kv_pad;
@@ -455,7 +481,7 @@ int msa_block_sparse(const msa_tensor* q, const msa_tensor* k, const msa_tensor*
   if (s) return s;
   if (topk <= 0) return MSA_ERR_INVALID;
   const BSLayout L = bs_layout(c.g, topk);
-  if ((s = check_workspace(opts, L.total))) return s;
+  if ((s = check_workspace(c, L.total))) return s;
   void* ws = opts->workspace;
   CUtensorMap mq, mk, mv, mdummy;
   std::memset(&mdummy, 0, sizeof(mdummy));
@@ -512,7 +538,7 @@ int msa_streaming(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v,
   if (s) return s;
   if (init_num < 0 || local_window_num < 1) return MSA_ERR_INVALID;
   const STLayout L = st_layout(c.g);
-  if ((s = check_workspace(opts, L.total))) return s;
+  if ((s = check_workspace(c, L.total))) return s;
   void* ws = opts->workspace;
   CUtensorMap mq, mk, mv, mdummy;
   std::memset(&mdummy, 0, sizeof(mdummy));

@@ -31,7 +31,11 @@
  * Memory    The caller owns every buffer.  The library allocates no device
  *           memory; every entry point takes its scratch space from
  *           opts->workspace, sized by msa_workspace_bytes().  One workspace
- *           must not be shared by calls that may overlap on the GPU.
+ *           must not be shared by calls that may overlap on the GPU.  The
+ *           byte range out spans must not overlap those of q, k and v
+ *           (MSA_ERR_INVALID), nor the workspace's first
+ *           msa_workspace_bytes() bytes any of the four (MSA_ERR_WORKSPACE);
+ *           q, k and v may share memory with one another.
  * Precision S = Q K^T is a bf16 x bf16 product with f32 accumulation; the
  *           softmax runs in f32; P and a staged f16 copy of v (exact for
  *           |v| <= 65504, which is checked) form the P.V product with f32

@@ -31,8 +31,15 @@ def test_exports_every_declared_function(lib):
         assert hasattr(lib, name), name
 
 
-def T(B=1, H=4, N=1024, D=128, ptr=0x10000, sb=None, sh=None, sn=None):
+_next_ptr = [0]
+
+
+def T(B=1, H=4, N=1024, D=128, ptr=None, sb=None, sh=None, sn=None):
+    """A tensor descriptor; without ptr, a fresh fake address 4 GiB from the last."""
     from dynamic_sparse_attention_slash_gb300.msa import MsaTensor
+    if ptr is None:
+        _next_ptr[0] += 1
+        ptr = _next_ptr[0] << 32
     sn = D if sn is None else sn
     sh = N * sn if sh is None else sh
     sb = H * sh if sb is None else sb
@@ -70,6 +77,7 @@ def test_workspace_bytes(lib):
     ("null_q", 1), ("d64", 2), ("n_huge", 2), ("misaligned", 1), ("gqa", 1), ("kv0", 1),
     ("flags", 1), ("lastq", 1), ("head_range", 1), ("head_dup", 1), ("no_ws", 3),
     ("small_ws", 3), ("ws_align", 3), ("odd_stride", 1), ("n_mismatch", 1),
+    ("out_is_q", 1), ("out_overlaps_v", 1), ("ws_overlaps_k", 3),
 ])
 def test_vertical_slash_rejects(lib, case, expect):
     q, k, v, out = T(), T(H=2), T(H=2), T()
@@ -83,7 +91,7 @@ def test_vertical_slash_rejects(lib, case, expect):
         n = (1 << 21) + 64
         q, k, v, out = T(N=n), T(H=2, N=n), T(H=2, N=n), T(N=n)
     elif case == "misaligned":
-        k = T(H=2, ptr=0x10008)
+        k = T(H=2, ptr=(1 << 40) + 8)
     elif case == "gqa":
         k, v = T(H=3), T(H=3)
     elif case == "kv0":
@@ -106,6 +114,12 @@ def test_vertical_slash_rejects(lib, case, expect):
         q = T(sn=130)
     elif case == "n_mismatch":
         v = T(H=2, N=2048)
+    elif case == "out_is_q":
+        out = T(ptr=q.data)
+    elif case == "out_overlaps_v":  # out starts inside v's last head
+        out = T(ptr=v.data + (2 * 1024 * 128 - 64) * 2)
+    elif case == "ws_overlaps_k":
+        o.workspace = k.data + 0x1000
     assert call_vs(lib, q, k, v, out, kv=kv, o=o) == expect
 
 

@@ -31,7 +31,7 @@ def static_entry():
     return lib, fn
 
 
-def fake(B, H, N, ptr=0x10000):
+def fake(B, H, N, ptr):
     """A descriptor with a fake, never-dereferenced pointer (host-side checks only)."""
     return msa.MsaTensor(ptr, B, H, N, 128, H * N * 128, N * 128, 128)
 
@@ -41,20 +41,22 @@ def test_static_entry_rejects_on_host():
     from dynamic_sparse_attention_slash_gb300 import build
     build.build()
     lib, fn = static_entry()
-    q, k, out = fake(1, 32, 32768), fake(1, 8, 32768), fake(1, 32, 32768)
+    q, k, out = fake(1, 32, 32768, 1 << 32), fake(1, 8, 32768, 2 << 32), fake(1, 32, 32768, 3 << 32)
     need = lib.msa_workspace_bytes(msa.MSA_KIND_VERTICAL_SLASH, ctypes.byref(q), ctypes.byref(k),
                                    1000, 6096, 32)
     assert need > MSA_STATIC_SCRATCH_BYTES
     assert fn(ctypes.byref(q), ctypes.byref(k), ctypes.byref(k), 1000, 6096, ctypes.byref(out),
               None) == msa.MSA_ERR_WORKSPACE
-    q4, k2, out4 = fake(1, 4, 32768), fake(1, 2, 32768), fake(1, 4, 32768)
+    q4, k2, out4 = fake(1, 4, 32768, 1 << 32), fake(1, 2, 32768, 2 << 32), fake(1, 4, 32768, 3 << 32)
     assert lib.msa_workspace_bytes(msa.MSA_KIND_VERTICAL_SLASH, ctypes.byref(q4), ctypes.byref(k2),
                                    1000, 6096, 4) <= MSA_STATIC_SCRATCH_BYTES
     assert fn(ctypes.byref(q4), ctypes.byref(k2), ctypes.byref(k2), 0, 6096, ctypes.byref(out4),
               None) == msa.MSA_ERR_INVALID
-    bad = fake(1, 4, 100)
+    bad = fake(1, 4, 100, 4 << 32)
     assert fn(ctypes.byref(bad), ctypes.byref(k2), ctypes.byref(k2), 10, 10, ctypes.byref(out4),
               None) == msa.MSA_ERR_INVALID
+    assert fn(ctypes.byref(q4), ctypes.byref(k2), ctypes.byref(k2), 10, 10, ctypes.byref(q4),
+              None) == msa.MSA_ERR_INVALID  # out overlaps q
 
 
 @pytest.mark.gpu
