@@ -291,3 +291,37 @@ def test_value_outside_f16_range_is_reported():
     v[0, 0, 5, 3] = 60000.0
     msa.msa_streaming(q, k, v, 1, 2, workspace=ws)
     assert msa.device_status(ws) == msa.MSA_OK
+
+
+def test_golden_tiny_block_sparse_and_streaming():
+    """The hand-worked fixture through the CUDA path: its inputs are exact in
+    bf16, so the block choice must equal the fixture's and the output rows its
+    closed forms (within the output tolerance)."""
+    import json
+    import os
+    with open(os.path.join(os.path.dirname(__file__), "golden", "bs_st_tiny.json")) as f:
+        g = json.load(f)
+    bs = g["block_sparse"]
+    N = bs["N"]
+    q, k, v = (torch.zeros(1, 1, N, D, dtype=torch.bfloat16) for _ in range(3))
+    for m in range(N // 64):
+        q[0, 0, 64 * m:64 * (m + 1), :2] = torch.tensor(bs["a"][m], dtype=torch.bfloat16)
+        k[0, 0, 64 * m:64 * (m + 1), :2] = torch.tensor(bs["b"][m], dtype=torch.bfloat16)
+        v[0, 0, 64 * m:64 * (m + 1), :] = bs["c"][m]
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    for case in bs["cases"]:
+        out, ex = P.run_bs(q, k, v, case["topk"])
+        for m, blocks in enumerate(case["blocks"]):
+            cnt = int(ex["block_count"][0, m])
+            assert ex["block_ids"][0, m, :cnt].tolist() == blocks, f"topk {case['topk']} m {m}"
+        got = np64(out[0, 0])
+        for row, val in case["rows"].items():
+            P.compare_out(got[int(row)], np.full(D, val), f"topk {case['topk']} row {row}")
+    st = g["streaming"]
+    q, k, v = qkv(1, 1, 1, st["N"], 14)
+    for case in st["cases"]:
+        out = msa.msa_streaming(q, k, v, case["init_num"], case["local_window_num"])
+        torch.cuda.synchronize()
+        ref, info = O.streaming_forward(q.cpu(), k.cpu(), v.cpu(), case["init_num"],
+                                        case["local_window_num"])
+        P.compare_out(np64(out[0]), ref[0], f"streaming {case}")

@@ -126,3 +126,34 @@ def test_streaming_nnz_matches_mask_popcount():
         blocks = set([0]) | set(range(max(0, m - 2), m + 1))
         expect += 2080 + 4096 * (len(blocks) - 1)
     assert rec["nnz"] == expect
+
+
+def test_golden_tiny_block_sparse_and_streaming():
+    """Hand-worked cases (derivations in the fixture): block choice, admitted
+    pairs and closed-form output rows of the block-sparse head; block lists and
+    admitted pairs of the streaming head."""
+    import json
+    import os
+    with open(os.path.join(os.path.dirname(__file__), "golden", "bs_st_tiny.json")) as f:
+        g = json.load(f)
+    bs = g["block_sparse"]
+    N = bs["N"]
+    q, k, v = np.zeros((N, D)), np.zeros((N, D)), np.zeros((N, D))
+    for m in range(N // 64):
+        q[64 * m:64 * (m + 1), :2] = bs["a"][m]
+        k[64 * m:64 * (m + 1), :2] = bs["b"][m]
+        v[64 * m:64 * (m + 1), :] = bs["c"][m]
+    for case in bs["cases"]:
+        out, info = O.block_sparse_head(q, k, v, case["topk"])
+        assert [s.tolist() for s in info["blocks"]] == case["blocks"]
+        assert info["nnz"] == case["nnz"]
+        for row, val in case["rows"].items():
+            np.testing.assert_allclose(out[int(row)], val, rtol=0, atol=2e-9)
+    st = g["streaming"]
+    N = st["N"]
+    rng = np.random.default_rng(9)
+    q, k, v = (rng.standard_normal((N, D)) for _ in range(3))
+    for case in st["cases"]:
+        _, info = O.streaming_head(q, k, v, case["init_num"], case["local_window_num"])
+        assert [s.tolist() for s in info["blocks"]] == case["blocks"]
+        assert info["nnz"] == case["nnz"]
