@@ -52,11 +52,11 @@ UNIT = "TFLOP/s"
 MEASURED_TRAFFIC = {
     "workload": "mixed_128k",
     "kind": "vs",
-    "bytes": 2.534e9 + 0.655e9,
+    "bytes": 2.533e9 + 0.655e9,
     "sources": ("dynamic_sparse_attention_slash_gb300/csrc/prefill.cu",
                 "dynamic_sparse_attention_slash_gb300/csrc/prefill_common.cuh",
                 "dynamic_sparse_attention_slash_gb300/csrc/sm103_ptx.cuh"),
-    "sha256": "ce2be635de23fb5e1a8d07fc0412a05202177a390750a8c2069af36ce7415fce",
+    "sha256": "67c1573658491f117616900785e8dbce68549971a89dfc2a7c5c76f38e576408",
 }
 
 

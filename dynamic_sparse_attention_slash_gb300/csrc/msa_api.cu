@@ -431,7 +431,7 @@ int msa_vertical_slash(const msa_tensor* q, const msa_tensor* k, const msa_tenso
                       at<uint32_t>(ws, L.col_chunks), L.chunk_words, at<__nv_bfloat16>(ws, L.kc),
                       at<__half>(ws, L.vc), L.kv_pad, at<uint32_t>(ws, 0), c.st, &launches);
   if (e == cudaSuccess)
-    e = launch_v_to_f16(view(v), c.g.B, c.g.Hkv, c.g.N, at<__half>(ws, L.v16), at<uint32_t>(ws, 0),
+    e = launch_v_to_f16(view(v), c.g, c.u, at<__half>(ws, L.v16), at<uint32_t>(ws, 0),
                         c.st, &launches);
   tm.end(MSA_STAGE_INDEX);
   if (e != cudaSuccess) return finish(e, launches);
@@ -493,7 +493,7 @@ int msa_block_sparse(const msa_tensor* q, const msa_tensor* k, const msa_tensor*
   cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), c.st);
   if (e != cudaSuccess) return finish(e, launches);
   tm.begin(MSA_STAGE_INDEX);
-  e = launch_v_to_f16(view(v), c.g.B, c.g.Hkv, c.g.N, at<__half>(ws, L.v16), at<uint32_t>(ws, 0),
+  e = launch_v_to_f16(view(v), c.g, c.u, at<__half>(ws, L.v16), at<uint32_t>(ws, 0),
                       c.st, &launches);
   if (e != cudaSuccess) return finish(e, launches);
   e = launch_bs_index(c.g, c.u, view(q), view(k), static_cast<int>(L.kb < topk ? L.kb : topk),
@@ -550,7 +550,7 @@ int msa_streaming(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v,
   cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), c.st);
   if (e != cudaSuccess) return finish(e, launches);
   tm.begin(MSA_STAGE_INDEX);
-  e = launch_v_to_f16(view(v), c.g.B, c.g.Hkv, c.g.N, at<__half>(ws, L.v16), at<uint32_t>(ws, 0),
+  e = launch_v_to_f16(view(v), c.g, c.u, at<__half>(ws, L.v16), at<uint32_t>(ws, 0),
                       c.st, &launches);
   tm.end(MSA_STAGE_INDEX);
   if (e != cudaSuccess) return finish(e, launches);

@@ -123,8 +123,8 @@ cudaError_t launch_bs_index(const Geometry& g, const UnitMap& u, TensorView q, T
                             int topk, float* qpool, float* kpool, int32_t* block_count,
                             int32_t* block_ids, int32_t* tiles, int32_t* tile_count,
                             int tile_cap, cudaStream_t st, int* n_launch);
-cudaError_t launch_v_to_f16(TensorView v, int B, int Hkv, int N, __half* dst, uint32_t* status,
-                            cudaStream_t st, int* n_launch);
+cudaError_t launch_v_to_f16(TensorView v, const Geometry& g, const UnitMap& u, __half* dst,
+                            uint32_t* status, cudaStream_t st, int* n_launch);
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                            const CUtensorMap& mv, const CUtensorMap& mkc, const CUtensorMap& mvc,
                            cudaStream_t st, int* n_launch);

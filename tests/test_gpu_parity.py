@@ -315,8 +315,11 @@ def test_golden_tiny_block_sparse_and_streaming():
             cnt = int(ex["block_count"][0, m])
             assert ex["block_ids"][0, m, :cnt].tolist() == blocks, f"topk {case['topk']} m {m}"
         got = np64(out[0, 0])
-        for row, val in case["rows"].items():
-            P.compare_out(got[int(row)], np.full(D, val), f"topk {case['topk']} row {row}")
+        for row, val in case["rows"].items():  # a single row: the bf16 cast alone moves it
+            d = np.abs(got[int(row)] - val)    # up to half an ulp, so only the max bound applies
+            assert d.max() <= P.MAX_TOL + P.half_ulp_bf16(val), (case["topk"], row, got[int(row), 0])
+        ref, _ = O.block_sparse_attention(q.cpu(), k.cpu(), v.cpu(), case["topk"])
+        P.compare_out(got, ref[0, 0], f"topk {case['topk']}")
     st = g["streaming"]
     q, k, v = qkv(1, 1, 1, st["N"], 14)
     for case in st["cases"]:

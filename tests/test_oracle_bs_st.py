@@ -148,7 +148,7 @@ def test_golden_tiny_block_sparse_and_streaming():
         assert [s.tolist() for s in info["blocks"]] == case["blocks"]
         assert info["nnz"] == case["nnz"]
         for row, val in case["rows"].items():
-            np.testing.assert_allclose(out[int(row)], val, rtol=0, atol=2e-9)
+            np.testing.assert_allclose(out[int(row)], val, rtol=0, atol=2e-10)
     st = g["streaming"]
     N = st["N"]
     rng = np.random.default_rng(9)
