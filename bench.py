@@ -56,7 +56,7 @@ MEASURED_TRAFFIC = {
     "sources": ("dynamic_sparse_attention_slash_gb300/csrc/prefill.cu",
                 "dynamic_sparse_attention_slash_gb300/csrc/prefill_common.cuh",
                 "dynamic_sparse_attention_slash_gb300/csrc/sm103_ptx.cuh"),
-    "sha256": "67c1573658491f117616900785e8dbce68549971a89dfc2a7c5c76f38e576408",
+    "sha256": "0470a4bcfb3e50c906c3fbd6322c63a223f55238e12645a583b32c622a4f24fa",
 }
 
 

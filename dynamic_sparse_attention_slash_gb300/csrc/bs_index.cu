@@ -8,6 +8,7 @@
 // over the row's scores in shared memory followed by an order-preserving
 // compaction, so the kept blocks come out ascending.  Everything is fp32 and
 // deterministic (fixed reduction trees, no atomics on values).
+#include <algorithm>
 #include "block_scan.cuh"
 #include "msa_internal.h"
 
@@ -34,8 +35,10 @@ struct PoolArgs {
   int NB, N, G;
   const __nv_bfloat16* x;
   int64_t sb, sh, sn;
-  int n_heads_x;     // heads of x per batch entry (pool of every head when u is unused)
-  bool use_units;    // true: pool unit heads of q; false: pool every head of k
+  int n_heads_x;     // heads of x per batch entry
+  int h_lo, h_n;     // without units: pool heads [h_lo, h_lo + h_n) of every batch entry
+  bool use_units;    // true: pool unit heads of q (out row = unit); false: heads of k
+                     // (out row = b * n_heads_x + h)
   float* out;        // [rows of (b, head)][NB][128]
 };
 
@@ -44,14 +47,15 @@ __global__ void bs_pool_kernel(const __grid_constant__ PoolArgs a) {
   const int m = blockIdx.x * kPoolWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (m >= a.NB) return;
-  const int row = blockIdx.y;
+  int row = blockIdx.y;
   int b, h;
   if (a.use_units) {
     b = row / a.u.n_heads;
     h = a.u.heads[row % a.u.n_heads];
   } else {
-    b = row / a.n_heads_x;
-    h = row % a.n_heads_x;
+    b = row / a.h_n;
+    h = a.h_lo + row % a.h_n;
+    row = b * a.n_heads_x + h;
   }
   const __nv_bfloat16* base = a.x + b * a.sb + h * a.sh;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -306,67 +310,78 @@ __global__ void __launch_bounds__(kSelThreads) bs_select_rows_kernel(const __gri
 }
 
 struct TileArgs {
-  int NB, npair, kb, tile_cap, n_units;
-  int words_per_warp;   // shared words per warp: ceil(key tiles / 4)
+  int NB, NQ, kb, tile_cap, n_units;
+  int words_per_warp;   // shared words per warp: two bitmaps of ceil(NB / 32) words
   const int32_t* block_count;
   const int32_t* block_ids;
-  int32_t* tiles;       // [units][npair][tile_cap] (q << 8) | maskB << 4 | maskA
-  int32_t* tile_count;  // [units][npair]
+  int32_t* tiles;       // [units][NQ][tile_cap][2]: key-block slots, blk | flags << 16
+  int32_t* tile_count;  // [units][NQ]
 };
 
-// One warp per (unit, pair c of 128-row query tiles): the blocks kept by row
-// blocks 4c .. 4c+3 set bits of a per-key-tile byte in shared memory (key tile
-// q = block >> 1; bit tile * 4 + row half * 2 + key half, i.e. maskA in the low
-// and maskB in the high nibble), and the non-empty bytes are written out in
-// ascending q as (q << 8) | maskB << 4 | maskA.
+// One warp per (unit, 128-row query tile p): the union U of the blocks kept by
+// row blocks 2p and 2p + 1, ascending, packed two blocks to an item.  The kept
+// blocks set bits of two bitmaps in shared memory (one per row block); a scan
+// over the words of their OR gives each block of U its rank r, and the block
+// goes to item r >> 1, key half r & 1, as blk | flags << 16 with flag bit a
+// set when row block 2p + a kept it.  An odd |U| leaves the last item's second
+// half a copy of its first block with no flags (a valid load that the softmax
+// masks out).
 __global__ void __launch_bounds__(32 * kTilesWarps) bs_tiles_kernel(TileArgs a) {
-  extern __shared__ uint32_t tile_bytes[];  // [kTilesWarps][words_per_warp], 4 key tiles a word
+  extern __shared__ uint32_t tile_bits[];  // [kTilesWarps][2][words_per_warp / 2]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * kTilesWarps + warp;
-  if (gid >= static_cast<int64_t>(a.n_units) * a.npair) return;  // no CTA-wide barrier follows
-  const int unit = static_cast<int>(gid / a.npair), c = static_cast<int>(gid % a.npair);
-  const int nq = min(2 * c + 2, (a.NB + 1) >> 1);  // key tiles q <= 2c + 1 within the sequence
-  const int words = (nq + 3) >> 2;
-  uint32_t* w = tile_bytes + warp * a.words_per_warp;
-  for (int i = lane; i < words; i += 32) w[i] = 0u;
+  if (gid >= static_cast<int64_t>(a.n_units) * a.NQ) return;  // no CTA-wide barrier follows
+  const int unit = static_cast<int>(gid / a.NQ), p = static_cast<int>(gid % a.NQ);
+  const int nblk = min(2 * p + 2, a.NB);  // blocks <= 2p + 1 within the sequence
+  const int words = (nblk + 31) >> 5;
+  uint32_t* w0 = tile_bits + warp * a.words_per_warp;
+  uint32_t* w1 = w0 + (a.words_per_warp >> 1);
+  for (int i = lane; i < words; i += 32) w0[i] = w1[i] = 0u;
   __syncwarp();
-  for (int j = 0; j < 4; ++j) {
-    const int m = 4 * c + j;
-    if (m >= a.NB) break;
-    const int64_t rb = static_cast<int64_t>(unit) * a.NB + m;
+  for (int t = 0; t < 2 && 2 * p + t < a.NB; ++t) {
+    const int64_t rb = static_cast<int64_t>(unit) * a.NB + 2 * p + t;
     const int cnt = a.block_count[rb];
     const int32_t* L = a.block_ids + rb * a.kb;
-    const int bit = (j >> 1) * 4 + (j & 1) * 2;  // tile, row half
+    uint32_t* w = t ? w1 : w0;
     for (int i = lane; i < cnt; i += 32) {
       const int blk = L[i];
-      const int q = blk >> 1;
-      atomicOr(&w[q >> 2], (1u << (bit + (blk & 1))) << (8 * (q & 3)));
+      atomicOr(&w[blk >> 5], 1u << (blk & 31));
     }
   }
   __syncwarp();
-  int32_t* out = a.tiles + gid * a.tile_cap;
-  int n = 0;
+  int32_t* out = a.tiles + gid * a.tile_cap * 2;
+  int n = 0, last = 0;  // blocks of U placed so far; the largest of them
   for (int base = 0; base < words; base += 32) {
     const int i = base + lane;
-    const uint32_t word = i < words ? w[i] : 0u;
-    int cw = 0;
-#pragma unroll
-    for (int t = 0; t < 4; ++t) cw += ((word >> (8 * t)) & 255u) != 0u ? 1 : 0;
+    const uint32_t b0 = i < words ? w0[i] : 0u, b1 = i < words ? w1[i] : 0u;
+    uint32_t u = b0 | b1;
+    const int cw = __popc(u);
     int incl = cw;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int v = __shfl_up_sync(0xffffffffu, incl, off);
       if (lane >= off) incl += v;
     }
-    int pos = n + incl - cw;
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const uint32_t mk = (word >> (8 * t)) & 255u;
-      if (mk) out[pos++] = ((4 * i + t) << 8) | static_cast<int>(mk);
+    int r = n + incl - cw;
+    while (u) {
+      const int bit = __ffs(u) - 1;
+      u &= u - 1;
+      const int flags = static_cast<int>(((b0 >> bit) & 1u) | (((b1 >> bit) & 1u) << 1));
+      out[r++] = (32 * i + bit) | (flags << 16);
     }
-    n += __shfl_sync(0xffffffffu, incl, 31);
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (total > 0) {  // the highest lane with a block holds the largest so far
+      const uint32_t has = __ballot_sync(0xffffffffu, cw > 0);
+      const int src = 31 - __clz(static_cast<int>(has));
+      const int top = cw > 0 ? 32 * i + 31 - __clz(static_cast<int>(b0 | b1)) : 0;
+      last = __shfl_sync(0xffffffffu, top, src);
+    }
+    n += total;
   }
-  if (lane == 0) a.tile_count[gid] = n;
+  if (lane == 0) {
+    if (n & 1) out[n] = last;  // second half of the last item: the same block, no flags
+    a.tile_count[gid] = (n + 1) >> 1;
+  }
 }
 
 }  // namespace
@@ -383,6 +398,8 @@ cudaError_t launch_bs_index(const Geometry& g, const UnitMap& u, TensorView q, T
   pa.G = g.G;
   pa.x = q.data; pa.sb = q.sb; pa.sh = q.sh; pa.sn = q.sn;
   pa.n_heads_x = g.Hq;
+  pa.h_lo = 0;
+  pa.h_n = g.Hq;
   pa.use_units = true;
   pa.out = qpool;
   bs_pool_kernel<<<dim3((g.NB + kPoolWarps - 1) / kPoolWarps, g.n_units), 32 * kPoolWarps, 0, st>>>(pa);
@@ -390,9 +407,18 @@ cudaError_t launch_bs_index(const Geometry& g, const UnitMap& u, TensorView q, T
   ++*n_launch;
   pa.x = k.data; pa.sb = k.sb; pa.sh = k.sh; pa.sn = k.sn;
   pa.n_heads_x = g.Hkv;
+  pa.h_lo = g.Hkv;  // the KV heads the selected query heads read
+  int h_hi = -1;
+  for (int i = 0; i < u.n_heads; ++i) {
+    pa.h_lo = std::min(pa.h_lo, u.heads[i] / g.G);
+    h_hi = std::max(h_hi, u.heads[i] / g.G);
+  }
+  if (h_hi < pa.h_lo) return cudaErrorInvalidValue;
+  pa.h_n = h_hi - pa.h_lo + 1;
   pa.use_units = false;
   pa.out = kpool;
-  bs_pool_kernel<<<dim3((g.NB + kPoolWarps - 1) / kPoolWarps, g.B * g.Hkv), 32 * kPoolWarps, 0, st>>>(pa);
+  bs_pool_kernel<<<dim3((g.NB + kPoolWarps - 1) / kPoolWarps, g.B * pa.h_n), 32 * kPoolWarps, 0,
+                   st>>>(pa);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   ++*n_launch;
   SelArgs sa;
@@ -428,7 +454,7 @@ cudaError_t launch_bs_index(const Geometry& g, const UnitMap& u, TensorView q, T
   ++*n_launch;
   TileArgs ta;
   ta.NB = g.NB;
-  ta.npair = (g.NQ + 1) / 2;
+  ta.NQ = g.NQ;
   ta.kb = sa.kb;
   ta.tile_cap = tile_cap;
   ta.n_units = g.n_units;
@@ -436,13 +462,13 @@ cudaError_t launch_bs_index(const Geometry& g, const UnitMap& u, TensorView q, T
   ta.block_ids = block_ids;
   ta.tiles = tiles;
   ta.tile_count = tile_count;
-  ta.words_per_warp = (((g.NB + 1) >> 1) + 3) >> 2;
+  ta.words_per_warp = 2 * ((g.NB + 31) >> 5);
   const int tsmem = kTilesWarps * ta.words_per_warp * 4;
   if (tsmem > 48 * 1024) {
     e = cudaFuncSetAttribute(bs_tiles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tsmem);
     if (e != cudaSuccess) return e;
   }
-  const int64_t warps = static_cast<int64_t>(g.n_units) * ta.npair;
+  const int64_t warps = static_cast<int64_t>(g.n_units) * g.NQ;
   bs_tiles_kernel<<<static_cast<unsigned>((warps + kTilesWarps - 1) / kTilesWarps),
                     32 * kTilesWarps, tsmem, st>>>(ta);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

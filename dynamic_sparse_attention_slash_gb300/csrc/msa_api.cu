@@ -201,7 +201,7 @@ struct BSLayout {
 BSLayout bs_layout(const Geometry& g, int64_t topk) {
   BSLayout L;
   L.kb = static_cast<int>(topk < g.NB ? topk : g.NB);
-  L.tile_cap = 4 * L.kb;  // a pair of query tiles spans four row blocks
+  L.tile_cap = L.kb;  // a query tile's two row blocks keep at most 2 kb blocks, two per item
   const size_t U = static_cast<size_t>(g.n_units);
   Carver c;
   c.off = kStatusBytes;
@@ -209,9 +209,8 @@ BSLayout bs_layout(const Geometry& g, int64_t topk) {
   L.kpool = c.take<float>(static_cast<size_t>(g.B) * g.Hkv * g.NB * kHeadDim);
   L.block_count = c.take<int32_t>(U * g.NB);
   L.block_ids = c.take<int32_t>(U * g.NB * L.kb);
-  const size_t npair = static_cast<size_t>(g.NQ + 1) / 2;
-  L.tiles = c.take<int32_t>(U * npair * L.tile_cap);
-  L.tile_count = c.take<int32_t>(U * npair);
+  L.tiles = c.take<int32_t>(U * g.NQ * L.tile_cap * 2);
+  L.tile_count = c.take<int32_t>(U * g.NQ);
   L.v16 = c.take<__half>(v16_elems(g));
   L.total = (c.off + 255) & ~size_t{255};
   return L;
@@ -248,7 +247,8 @@ T* at(void* ws, size_t off) {
 
 // ------------------------------------------------------------------ TMA maps
 int make_map_4d(CUtensorMap* m, const msa_tensor* t,
-                CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+                CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                cuuint32_t box_rows = 128) {
   auto fn = encode_fn();
   if (!fn) return MSA_ERR_CUDA;
   const int64_t sh = t->H > 1 ? t->sh : t->N * t->sn;
@@ -257,7 +257,7 @@ int make_map_4d(CUtensorMap* m, const msa_tensor* t,
                         static_cast<cuuint64_t>(t->H), static_cast<cuuint64_t>(t->B)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(t->sn * 2), static_cast<cuuint64_t>(sh * 2),
                            static_cast<cuuint64_t>(sb * 2)};
-  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t box[4] = {64, box_rows, 1, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   const CUresult r = fn(m, dtype, 4, t->data, dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -266,7 +266,7 @@ int make_map_4d(CUtensorMap* m, const msa_tensor* t,
 }
 
 // Contiguous [B][H][N][128] f16 buffer (the staged copy of v).
-int make_map_f16(CUtensorMap* m, void* base, const Geometry& g) {
+int make_map_f16(CUtensorMap* m, void* base, const Geometry& g, cuuint32_t box_rows = 128) {
   msa_tensor t;
   t.data = base;
   t.B = g.B;
@@ -276,7 +276,7 @@ int make_map_f16(CUtensorMap* m, void* base, const Geometry& g) {
   t.sn = kHeadDim;
   t.sh = static_cast<int64_t>(g.N) * kHeadDim;
   t.sb = t.sh * g.Hkv;
-  return make_map_4d(m, &t, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+  return make_map_4d(m, &t, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, box_rows);
 }
 
 int make_map_rows(CUtensorMap* m, void* base, int64_t rows, CUtensorMapDataType dtype) {
@@ -483,10 +483,13 @@ int msa_block_sparse(const msa_tensor* q, const msa_tensor* k, const msa_tensor*
   const BSLayout L = bs_layout(c.g, topk);
   if ((s = check_workspace(c, L.total))) return s;
   void* ws = opts->workspace;
-  CUtensorMap mq, mk, mv, mdummy;
+  // K and the f16 copy of v are read as 64-key blocks: an item pairs two kept
+  // blocks that need not be adjacent
+  CUtensorMap mq, mk64, mv64, mdummy;
   std::memset(&mdummy, 0, sizeof(mdummy));
-  if ((s = make_map_4d(&mq, q)) || (s = make_map_4d(&mk, k)) ||
-      (s = make_map_f16(&mv, at<void>(ws, L.v16), c.g)))
+  if ((s = make_map_4d(&mq, q)) ||
+      (s = make_map_4d(&mk64, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 64)) ||
+      (s = make_map_f16(&mv64, at<void>(ws, L.v16), c.g, 64)))
     return s;
   const StageTimer tm{opts->stage_events, c.st};
   int launches = 0;
@@ -508,7 +511,7 @@ int msa_block_sparse(const msa_tensor* q, const msa_tensor* k, const msa_tensor*
   p.bs_tile_count = at<int32_t>(ws, L.tile_count);
   p.bs_tile_cap = L.tile_cap;
   tm.begin(MSA_STAGE_PREFILL);
-  e = launch_prefill(p, mq, mk, mv, mdummy, mdummy, c.st, &launches);
+  e = launch_prefill_tile(p, mq, mk64, mv64, c.st, &launches);
   tm.end(MSA_STAGE_PREFILL);
   if (e != cudaSuccess) return finish(e, launches);
   {

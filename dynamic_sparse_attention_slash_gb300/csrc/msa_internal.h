@@ -59,8 +59,8 @@ struct PrefillParams {
   int kv;                      // number of chosen columns
   int kv_pad;                  // rows per unit in the gathered K/V buffers (multiple of 128)
   // block-sparse plan
-  const int32_t* bs_tiles;       // [units][npair][bs_tile_cap] (q << 8) | maskB << 4 | maskA
-  const int32_t* bs_tile_count;  // [units][npair]
+  const int32_t* bs_tiles;       // [units][NQ][bs_tile_cap][2] 64-key block | flags << 16
+  const int32_t* bs_tile_count;  // [units][NQ] items per query tile
   int bs_tile_cap;
   // streaming plan
   int init_num, local_num;
@@ -130,8 +130,9 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& mq, const 
                            cudaStream_t st, int* n_launch);
 // One query tile per CTA, for block-sparse plans (launch_prefill routes them
 // here); any other kind returns cudaErrorInvalidValue.
-cudaError_t launch_prefill_tile(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
-                                const CUtensorMap& mv, const CUtensorMap& mkc,
-                                const CUtensorMap& mvc, cudaStream_t st, int* n_launch);
+// Block-sparse heads: mk64 / mv64 map K and the f16 copy of v in 64-key boxes.
+cudaError_t launch_prefill_tile(const PrefillParams& p, const CUtensorMap& mq,
+                                const CUtensorMap& mk64, const CUtensorMap& mv64, cudaStream_t st,
+                                int* n_launch);
 
 }  // namespace msa

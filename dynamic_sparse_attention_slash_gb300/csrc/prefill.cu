@@ -134,7 +134,7 @@ __device__ __forceinline__ int n_items(const PrefillParams& P, int unit, int c, 
                                        int n_tiles) {
   const int pA = 2 * c;
   if (P.kind == kPrefillVS) return n_chunks + n_tiles;
-  if (P.kind == kPrefillBS) return P.bs_tile_count[static_cast<int64_t>(unit) * P.npair + c];
+  if (P.kind == kPrefillBS) return P.bs_tile_count[static_cast<int64_t>(unit) * P.npair + c];  // never taken
   int sink_hi, loc_lo;
   st_ranges(P, pA, sink_hi, loc_lo);
   return sink_hi + (pair_qmax(P, pA) - loc_lo + 1);
@@ -182,6 +182,12 @@ __device__ __forceinline__ Item get_item(const PrefillParams& P, int unit, int c
     return it;
   }
   if (P.kind == kPrefillBS) {
+    // Never taken: launch_prefill refuses block-sparse plans, whose lists now
+    // pair 64-key blocks per query tile (prefill_tile.cu).  This branch reads
+    // the earlier pair format of 128-key tiles and stays compiled in because
+    // the kernel measured 0.6-1 % faster on vertical-slash heads with it
+    // (63.5-63.7 ms against 64.1-64.3 ms on the 128K step without it, and with
+    // the kernel specialised per head kind at compile time).
     const int32_t e = P.bs_tiles[(static_cast<int64_t>(unit) * P.npair + c) * P.bs_tile_cap + i];
     it.idx = e >> 8;
     it.qmask[0] = static_cast<uint32_t>(e & 15);
@@ -564,11 +570,11 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                            const CUtensorMap& mv, const CUtensorMap& mkc, const CUtensorMap& mvc,
                            cudaStream_t st, int* n_launch) {
-  // Block-sparse heads run the one-tile kernel (prefill_tile.cu): their short,
-  // sparse per-tile item lists favour skipping items per query tile and a
-  // shorter softmax chain; the two-tile kernel keeps the tensor core busier on
-  // the long lists of vertical-slash and streaming heads.
-  if (p.kind == kPrefillBS) return launch_prefill_tile(p, mq, mk, mv, mkc, mvc, st, n_launch);
+  // Block-sparse heads run the one-tile kernel (prefill_tile.cu, launched by
+  // the block-sparse entry point): their short, sparse per-tile lists favour
+  // items of two kept blocks per query tile; this kernel keeps the tensor core
+  // busier on the long lists of vertical-slash and streaming heads.
+  if (p.kind == kPrefillBS) return cudaErrorInvalidValue;
   // The register split above needs the launch to provide kMinLaunchRegs per
   // thread; refuse to launch (rather than wait forever) if the build differs.
   static int launch_regs = -1;

@@ -7,12 +7,14 @@
 //
 // This kernel serves the block-sparse heads: one CTA computes one 128-row
 // query tile p of one (batch, head) unit (row blocks 2p and 2p + 1).  It walks
-// the pair tile list that bs_index.cu builds for the pair of query tiles
-// (2c, 2c + 1) and keeps only the entries whose quadrant mask is non-empty for
-// its own tile, so a tile never loads or multiplies a key tile only its
-// neighbour needs.  An item is a key tile q: keys [128q, 128q+128) of the KV
-// head, with a 4-bit quadrant mask (bit a*2+b: row half a may see key half b)
-// and the causal cut on the tile's diagonal.
+// the tile's item list that bs_index.cu builds: the blocks kept by either row
+// block, ascending, two 64-key blocks to an item.  The two blocks of an item
+// need not be adjacent, so an item wastes at most the quadrants of a block that
+// only one row block kept (on synthetic top-100 heads at 128K: 56 % of the
+// computed 64 x 64 quadrants are kept blocks, against 32 % with items of
+// aligned 128-key tiles).  An item carries a 4-bit quadrant mask (bit a*2+b:
+// row half a may see key half b) and the causal cut where a block reaches
+// past a row.
 //
 // Warp roles (384 threads):
 //   warp 0     TMA producer for Q and K (one thread)
@@ -68,68 +70,53 @@ struct __align__(1024) TileSmem {
 };
 
 struct Item {
-  int idx;      // key tile q
-  uint32_t qm;  // quadrant mask for this query tile (bit a*2 + b: row half a sees key half b)
+  int blk[2];   // 64-key block of key half 0 and 1
+  uint32_t qm;  // quadrant mask (bit a*2 + b: row half a sees key half b)
 };
 
-// The query tile of a CTA and its pair's block-sparse tile list.  The list
-// describes the pair of query tiles (2c, 2c + 1), each entry (q << 8) | maskB
-// << 4 | maskA; the tile keeps the entries whose own mask is not empty.
+// The query tile of a CTA and its block-sparse item list: entry i is two
+// int32 slots, one per key half, each blk | flags << 16 (flag bit a: row
+// block 2p + a kept the block).
 struct Tile {
-  int unit, p, t;  // tile p = 2c + t
-  int n_slots;     // entries of the pair list
+  int n;  // items
   const int32_t* list;
 };
 
 __device__ __forceinline__ Tile make_tile(const PrefillParams& P, int unit, int p) {
+  const int64_t t = static_cast<int64_t>(unit) * P.g.NQ + p;
   Tile T;
-  T.unit = unit;
-  T.p = p;
-  T.t = p & 1;
-  const int64_t pair = static_cast<int64_t>(unit) * P.npair + (p >> 1);
-  T.n_slots = P.bs_tile_count[pair];
-  T.list = P.bs_tiles + pair * P.bs_tile_cap;
+  T.n = P.bs_tile_count[t];
+  T.list = P.bs_tiles + t * P.bs_tile_cap * 2;
   return T;
 }
 
-__device__ __forceinline__ uint32_t tile_qmask(const Tile& T, int32_t e) {
-  return static_cast<uint32_t>(T.t ? (e >> 4) & 15 : e & 15);
+__device__ __forceinline__ Item get_item(const Tile& T, int i) {
+  const int32_t s0 = T.list[2 * i], s1 = T.list[2 * i + 1];
+  const uint32_t f0 = static_cast<uint32_t>(s0 >> 16) & 3u, f1 = static_cast<uint32_t>(s1 >> 16) & 3u;
+  Item it;
+  it.blk[0] = s0 & 0xffff;
+  it.blk[1] = s1 & 0xffff;
+  it.qm = (f0 & 1u) | ((f1 & 1u) << 1) | ((f0 >> 1) << 2) | ((f1 >> 1) << 3);
+  return it;
 }
 
-// Items of the tile (warp-collective: every lane returns the count).
-__device__ int count_items(const Tile& T, int lane) {
-  int cnt = 0;
-  for (int j = lane; j < T.n_slots; j += 32) cnt += tile_qmask(T, T.list[j]) != 0u ? 1 : 0;
-  return __reduce_add_sync(0xffffffffu, cnt);
-}
-
-// The next item at or after slot s (s moves past it); false when none is left.
-// Key tiles come in the list's ascending order.
-__device__ __forceinline__ bool next_item(const Tile& T, int& s, Item& it) {
-  while (s < T.n_slots) {
-    const int32_t e = T.list[s++];
-    const uint32_t m = tile_qmask(T, e);
-    if (m) {
-      it.idx = e >> 8;
-      it.qm = m;
-      return true;
-    }
-  }
-  return false;
-}
-
-// TMA of key tile it.idx's K (or V) rows into dst, completion on bar.
-__device__ __forceinline__ void load_item(const Item& it, uint8_t* dst, const CUtensorMap* map,
+// TMA of the item's K (or V) rows into dst, completion on bar: keys of block
+// blk[h] are rows [64h, 64h + 64) of the 128-row tile (both 64-column halves).
+__device__ __forceinline__ void load_item(const Item& it, uint8_t* dst, const CUtensorMap* map64,
                                           uint64_t* bar, int hkv, int b) {
   mbar_arrive_expect_tx(bar, kTileBytes);
-  tma_load_4d(dst, map, bar, 0, 128 * it.idx, hkv, b);
-  tma_load_4d(dst + kHalfBytes, map, bar, 64, 128 * it.idx, hkv, b);
+#pragma unroll
+  for (int hd = 0; hd < 2; ++hd)
+#pragma unroll
+    for (int kh = 0; kh < 2; ++kh)
+      tma_load_4d(dst + hd * kHalfBytes + kh * (kHalfBytes / 2), map64, bar, 64 * hd,
+                  64 * it.blk[kh], hkv, b);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
 sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ CUtensorMap mq,
-                           const __grid_constant__ CUtensorMap mk,
-                           const __grid_constant__ CUtensorMap mv) {
+                           const __grid_constant__ CUtensorMap mk64,
+                           const __grid_constant__ CUtensorMap mv64) {
   extern __shared__ uint8_t smem_raw[];
   TileSmem& sm = *reinterpret_cast<TileSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~static_cast<uintptr_t>(1023));
@@ -171,16 +158,15 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
     // ------------------------------------------------------------ Q + K producer
     if (lane == 0) {
       tma_prefetch_desc(&mq);
-      tma_prefetch_desc(&mk);
+      tma_prefetch_desc(&mk64);
       mbar_arrive_expect_tx(&sm.q_full, kTileBytes);
       tma_load_4d(sm.q, &mq, &sm.q_full, 0, 128 * p, h, b);
       tma_load_4d(sm.q + kHalfBytes, &mq, &sm.q_full, 64, 128 * p, h, b);
-      int issued = 0, s = 0;
-      Item it;
-      for (int i = 0; next_item(T, s, it); ++i) {
+      int issued = 0;
+      for (int i = 0; i < T.n; ++i) {
         const int st = i % kStagesK;
         if (!mbar_wait(&sm.k_empty[st], ((i / kStagesK) & 1) ^ 1, abort)) break;
-        load_item(it, sm.k[st], &mk, &sm.k_full[st], hkv, b);
+        load_item(get_item(T, i), sm.k[st], &mk64, &sm.k_full[st], hkv, b);
         issued = i + 1;
       }
       // drain: the latest load of every stage, and Q, must land before exit
@@ -191,13 +177,12 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
   } else if (warp == 2) {
     // ------------------------------------------------------------ V producer
     if (lane == 0) {
-      tma_prefetch_desc(&mv);
-      int issued = 0, s = 0;
-      Item it;
-      for (int i = 0; next_item(T, s, it); ++i) {
+      tma_prefetch_desc(&mv64);
+      int issued = 0;
+      for (int i = 0; i < T.n; ++i) {
         const int st = i % kStagesV;
         if (!mbar_wait(&sm.v_empty[st], ((i / kStagesV) & 1) ^ 1, abort)) break;
-        load_item(it, sm.v[st], &mv, &sm.v_full[st], hkv, b);
+        load_item(get_item(T, i), sm.v[st], &mv64, &sm.v_full[st], hkv, b);
         issued = i + 1;
       }
       for (int i = max(0, issued - kStagesV); i < issued; ++i)
@@ -205,7 +190,7 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    const int n = count_items(T, lane);
+    const int n = T.n;
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idO = idesc_f32acc(128, 128, /*bf16=*/false, false, true);  // f16 P, f16 V
@@ -277,9 +262,8 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     int k = 0;  // items processed so far
-    int slot = 0;
-    Item it;
-    while (next_item(T, slot, it)) {
+    for (; k < T.n;) {
+      const Item it = get_item(T, k);
       const uint32_t s_col = lane_base + kColS + 128 * (k & 1);
       // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
       const bool waited = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[k & 1], (k >> 1) & 1, abort));
@@ -287,8 +271,10 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
       // A key tile whose quadrant (row half, key half g) is not admitted leaves
       // this warp nothing to do: its half of P is zero, its maximum -inf.
       const bool idle = !((it.qm >> (half * 2 + g)) & 1u);
-      // raw logits (unscaled) of this row's half with the diagonal tile's
-      // causal cut; scale * log2(e) is folded in below
+      // raw logits (unscaled) of this row's half with the causal cut (key
+      // 64 blk + e is admitted iff it is <= the row); scale * log2(e) is
+      // folded in below
+      const int lim = row - 64 * (g ? it.blk[1] : it.blk[0]);
       auto logits = [&](float (&x)[64]) {
         {
           uint32_t raw[64];
@@ -296,10 +282,10 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
 #pragma unroll
           for (int e = 0; e < 64; ++e) x[e] = __uint_as_float(raw[e]);
         }
-        if (it.idx == p) {
+        if (lim < 63) {
 #pragma unroll
           for (int e = 0; e < 64; ++e)
-            if (64 * g + e > r) x[e] = -INFINITY;
+            if (e > lim) x[e] = -INFINITY;
         }
       };
       // p = 2^(z log2(e) - m) as f16 pairs; returns this half's row sum
@@ -452,16 +438,16 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
 
 }  // namespace
 
-cudaError_t launch_prefill_tile(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
-                                const CUtensorMap& mv, const CUtensorMap& mkc,
-                                const CUtensorMap& mvc, cudaStream_t st, int* n_launch) {
+cudaError_t launch_prefill_tile(const PrefillParams& p, const CUtensorMap& mq,
+                                const CUtensorMap& mk64, const CUtensorMap& mv64, cudaStream_t st,
+                                int* n_launch) {
   const int smem = static_cast<int>(sizeof(TileSmem)) + 1024;
   cudaError_t e = cudaFuncSetAttribute(sparse_prefill_tile_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (p.kind != kPrefillBS) return cudaErrorInvalidValue;  // block-sparse tile lists only
   if (p.g.n_units == 0 || p.g.NQ == 0) return cudaSuccess;
-  sparse_prefill_tile_kernel<<<dim3(p.g.NQ, p.g.n_units), kThreads, smem, st>>>(p, mq, mk, mv);
+  sparse_prefill_tile_kernel<<<dim3(p.g.NQ, p.g.n_units), kThreads, smem, st>>>(p, mq, mk64, mv64);
   e = cudaGetLastError();
   if (e == cudaSuccess) ++*n_launch;
   return e;
