@@ -52,7 +52,7 @@ UNIT = "TFLOP/s"
 MEASURED_TRAFFIC = {
     "workload": "mixed_128k",
     "kind": "vs",
-    "bytes": 2.533e9 + 0.655e9,
+    "bytes": 2.533e9 + 0.652e9,
     "sources": ("dynamic_sparse_attention_slash_gb300/csrc/prefill.cu",
                 "dynamic_sparse_attention_slash_gb300/csrc/prefill_common.cuh",
                 "dynamic_sparse_attention_slash_gb300/csrc/sm103_ptx.cuh"),
