@@ -7,7 +7,9 @@
 // same set.  Ties go to the lower block.  Selection is an 8-bit radix select
 // over the row's scores in shared memory followed by an order-preserving
 // compaction, so the kept blocks come out ascending.  Everything is fp32 and
-// deterministic (fixed reduction trees, no atomics on values).
+// deterministic (fixed reduction trees, no atomics on values).  Last, each
+// 128-row query tile gets the prefill's item list: the union of the blocks its
+// two row blocks kept, ascending, two blocks to an item.
 #include <algorithm>
 #include "block_scan.cuh"
 #include "msa_internal.h"
