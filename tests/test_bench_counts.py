@@ -74,3 +74,24 @@ def test_exact_line_pairs_brute_force(N, nv, ns, seed):
     j = np.arange(N)[None, :]
     mask = (j <= i) & (np.isin(j, V) | np.isin(i - j, S))
     assert bench.vs_exact_line_pairs(V, S, N) == int(mask.sum())
+
+
+def test_reference_arm_prints_its_line_on_cpu():
+    """bench.py --impl reference times the oracle on the host cores and prints
+    one JSON line with the contract's keys (no GPU needed)."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--workload", "vs_tiny", "--steps", "1", "--warmup", "0",
+                        "--ref-rows", "8"], capture_output=True, text=True, timeout=300, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["steps"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["config"]["workload"] == "vs_tiny" and line["higher_is_better"] is True
