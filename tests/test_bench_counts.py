@@ -95,3 +95,24 @@ def test_reference_arm_prints_its_line_on_cpu():
     assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
     assert line["config"]["workload"] == "vs_tiny" and line["higher_is_better"] is True
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """Two ranks (gloo on CPU): rank 0 alone runs the oracle and prints; the
+    other rank exits 0 without work."""
+    import json
+    import os
+    import random
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    port = str(random.randint(20000, 40000))
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                        "--nproc-per-node", "2", "--master-addr", "127.0.0.1", "--master-port", port,
+                        os.path.join(root, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--workload", "vs_tiny", "--steps", "1", "--warmup", "0", "--ref-rows", "8"],
+                       capture_output=True, text=True, timeout=300, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(l) for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    assert lines[0]["impl"] == "reference" and lines[0]["n_gpus"] == 2 and lines[0]["value"] > 0
