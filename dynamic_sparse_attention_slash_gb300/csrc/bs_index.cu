@@ -409,7 +409,7 @@ cudaError_t launch_bs_index(const Geometry& g, const UnitMap& u, TensorView q, T
   ++*n_launch;
   pa.x = k.data; pa.sb = k.sb; pa.sh = k.sh; pa.sn = k.sn;
   pa.n_heads_x = g.Hkv;
-  pa.h_lo = g.Hkv;  // the KV heads the selected query heads read
+  pa.h_lo = g.Hkv;  // range of the KV heads the selected query heads read
   int h_hi = -1;
   for (int i = 0; i < u.n_heads; ++i) {
     pa.h_lo = std::min(pa.h_lo, u.heads[i] / g.G);

@@ -8,7 +8,8 @@ namespace msa {
 namespace {
 
 // v (bf16, any strides, [B][Hkv][N][128]) -> dst (f16, contiguous, same shape),
-// for KV heads [h_lo, h_lo + h_n) only: the heads a call's query heads read.
+// for KV heads [h_lo, h_lo + h_n) only: the range from the lowest to the
+// highest KV head that a call's query heads read.
 // The P.V product runs in f16 (P rounded to f16 keeps 3 more mantissa bits than
 // bf16); every bf16 value of magnitude <= 65504 is exactly representable in
 // f16 (tiny values become f16 subnormals, error < 3e-8).  Larger magnitudes
@@ -46,7 +47,7 @@ __global__ void v_to_f16_kernel(const __nv_bfloat16* __restrict__ v, int64_t sb,
 
 cudaError_t launch_v_to_f16(TensorView v, const Geometry& g, const UnitMap& u, __half* dst,
                             uint32_t* status, cudaStream_t st, int* n_launch) {
-  int h_lo = g.Hkv, h_hi = -1;  // KV heads read by the selected query heads
+  int h_lo = g.Hkv, h_hi = -1;  // range of the KV heads the selected query heads read
   for (int i = 0; i < u.n_heads; ++i) {
     h_lo = std::min(h_lo, u.heads[i] / g.G);
     h_hi = std::max(h_hi, u.heads[i] / g.G);
