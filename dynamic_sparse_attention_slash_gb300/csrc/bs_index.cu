@@ -10,7 +10,6 @@
 // deterministic (fixed reduction trees, no atomics on values).  Last, each
 // 128-row query tile gets the prefill's item list: the union of the blocks its
 // two row blocks kept, ascending, two blocks to an item.
-#include <algorithm>
 #include "block_scan.cuh"
 #include "msa_internal.h"
 
@@ -38,8 +37,8 @@ struct PoolArgs {
   const __nv_bfloat16* x;
   int64_t sb, sh, sn;
   int n_heads_x;     // heads of x per batch entry
-  int h_lo, h_n;     // without units: pool heads [h_lo, h_lo + h_n) of every batch entry
-  bool use_units;    // true: pool unit heads of q (out row = unit); false: heads of k
+  KvHeads kv;        // without units: the heads of k to pool in every batch entry
+  bool use_units;    // true: pool unit heads of q (out row = unit); false: heads kv of k
                      // (out row = b * n_heads_x + h)
   float* out;        // [rows of (b, head)][NB][128]
 };
@@ -55,8 +54,8 @@ __global__ void bs_pool_kernel(const __grid_constant__ PoolArgs a) {
     b = row / a.u.n_heads;
     h = a.u.heads[row % a.u.n_heads];
   } else {
-    b = row / a.h_n;
-    h = a.h_lo + row % a.h_n;
+    b = row / a.kv.n;
+    h = a.kv.h[row % a.kv.n];
     row = b * a.n_heads_x + h;
   }
   const __nv_bfloat16* base = a.x + b * a.sb + h * a.sh;
@@ -400,8 +399,7 @@ cudaError_t launch_bs_index(const Geometry& g, const UnitMap& u, TensorView q, T
   pa.G = g.G;
   pa.x = q.data; pa.sb = q.sb; pa.sh = q.sh; pa.sn = q.sn;
   pa.n_heads_x = g.Hq;
-  pa.h_lo = 0;
-  pa.h_n = g.Hq;
+  pa.kv.n = 0;
   pa.use_units = true;
   pa.out = qpool;
   bs_pool_kernel<<<dim3((g.NB + kPoolWarps - 1) / kPoolWarps, g.n_units), 32 * kPoolWarps, 0, st>>>(pa);
@@ -409,17 +407,11 @@ cudaError_t launch_bs_index(const Geometry& g, const UnitMap& u, TensorView q, T
   ++*n_launch;
   pa.x = k.data; pa.sb = k.sb; pa.sh = k.sh; pa.sn = k.sn;
   pa.n_heads_x = g.Hkv;
-  pa.h_lo = g.Hkv;  // range of the KV heads the selected query heads read
-  int h_hi = -1;
-  for (int i = 0; i < u.n_heads; ++i) {
-    pa.h_lo = std::min(pa.h_lo, u.heads[i] / g.G);
-    h_hi = std::max(h_hi, u.heads[i] / g.G);
-  }
-  if (h_hi < pa.h_lo) return cudaErrorInvalidValue;
-  pa.h_n = h_hi - pa.h_lo + 1;
+  pa.kv = kv_heads_of(g.Hkv, g.G, u);  // the KV heads the selected query heads read
+  if (pa.kv.n == 0) return cudaErrorInvalidValue;
   pa.use_units = false;
   pa.out = kpool;
-  bs_pool_kernel<<<dim3((g.NB + kPoolWarps - 1) / kPoolWarps, g.B * pa.h_n), 32 * kPoolWarps, 0,
+  bs_pool_kernel<<<dim3((g.NB + kPoolWarps - 1) / kPoolWarps, g.B * pa.kv.n), 32 * kPoolWarps, 0,
                    st>>>(pa);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   ++*n_launch;

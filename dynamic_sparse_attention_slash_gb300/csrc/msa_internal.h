@@ -26,6 +26,24 @@ struct UnitMap {
   int heads[1024];
 };
 
+// The KV heads a call's query heads read (h / G over the selected heads),
+// ascending, without repeats.
+struct KvHeads {
+  int n;
+  int h[1024];
+};
+
+inline KvHeads kv_heads_of(int Hkv, int G, const UnitMap& u) {
+  KvHeads kv;
+  kv.n = 0;
+  for (int x = 0; x < Hkv; ++x) {
+    bool used = false;
+    for (int i = 0; i < u.n_heads && !used; ++i) used = u.heads[i] / G == x;
+    if (used) kv.h[kv.n++] = x;
+  }
+  return kv;
+}
+
 struct TensorView {
   const __nv_bfloat16* data;
   int64_t sb, sh, sn;
