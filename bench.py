@@ -45,17 +45,18 @@ UNIT = "TFLOP/s"
 
 # ----------------------------------------------------------------------------- exact pair counts
 # dram__bytes_read.sum + dram__bytes_write.sum of the vertical-slash prefill
-# launch of the mixed 128K step, from one ncu capture (one pass, full size;
-# profiles/sparse_prefill_dram_mixed_128k.md).  The figure belongs to the kernel
-# source it was taken on: once any of its files changes, the bench reports null
-# until it is measured again.
+# launch of the mixed 128K step, from one ncu capture of that one launch (one
+# pass, full size).  The figure belongs to the kernel source it was taken on:
+# once any of its files changes, the bench reports null until it is measured
+# again.
 MEASURED_TRAFFIC = {
     "workload": "mixed_128k",
     "kind": "vs",
     "bytes": 2.533e9 + 0.652e9,
     "sources": ("dynamic_sparse_attention_slash_gb300/csrc/prefill.cu",
                 "dynamic_sparse_attention_slash_gb300/csrc/prefill_common.cuh",
-                "dynamic_sparse_attention_slash_gb300/csrc/sm103_ptx.cuh"),
+                "dynamic_sparse_attention_slash_gb300/csrc/sm103_ptx.cuh",
+                "dynamic_sparse_attention_slash_gb300/csrc/msa_internal.h"),
     "sha256": "0470a4bcfb3e50c906c3fbd6322c63a223f55238e12645a583b32c622a4f24fa",
 }
 
@@ -213,6 +214,42 @@ def oracle_sample(w, q, k, v, heads, rows_per_head: int, seed: int = 0):
     label = (f"one head of each type of {w.name}: full index construction + attention for "
              f"{rows_per_head} seeded query rows per head")
     return flops, secs, label
+
+
+def sdpa_selected_backend(q, k, v) -> str:
+    """The backend torch's scaled_dot_product_attention picks for these causal
+    inputs by default (its own dispatch rule, asked without running it)."""
+    try:
+        from torch.nn.attention import SDPBackend
+        idx = torch._fused_sdp_choice(q, k, v, None, 0.0, True)
+        return SDPBackend(idx).name
+    except Exception as exc:  # noqa: BLE001 - private helper; report why it failed
+        return f"unknown ({type(exc).__name__})"
+
+
+def time_sdpa(q, k, v, stream, d0, d1) -> float:
+    """ms of one causal SDPA call after one warm-up call."""
+    torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True)
+    d0.record(stream)
+    torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    return d0.elapsed_time(d1)
+
+
+def time_sdpa_backends(q, k, v, stream, d0, d1) -> dict:
+    """ms of causal SDPA forced onto each fused backend in turn (a string where
+    torch refuses the backend for these inputs)."""
+    from torch.nn.attention import SDPBackend, sdpa_kernel
+    res = {}
+    for b in (SDPBackend.CUDNN_ATTENTION, SDPBackend.FLASH_ATTENTION,
+              SDPBackend.EFFICIENT_ATTENTION):
+        try:
+            with sdpa_kernel([b]):
+                res[b.name] = time_sdpa(q, k, v, stream, d0, d1)
+        except RuntimeError as exc:
+            res[b.name] = f"unavailable: {exc}"[:80]
+    return res
 
 
 def l2_note(q, k) -> str:
@@ -471,23 +508,19 @@ def main():
         d1.record(stream)
         torch.cuda.synchronize()
         ours_ms = d0.elapsed_time(d1)
-        sdpa_ms, backend = None, None
+        sdpa_ms, backend, per_backend = None, None, {}
         try:
             G = w.n_q_heads // w.n_kv_heads
             kr, vr = k.repeat_interleave(G, dim=1), v.repeat_interleave(G, dim=1)
-            torch.nn.functional.scaled_dot_product_attention(q, kr, vr, is_causal=True)
-            d0.record(stream)
-            torch.nn.functional.scaled_dot_product_attention(q, kr, vr, is_causal=True)
-            d1.record(stream)
-            torch.cuda.synchronize()
-            sdpa_ms = d0.elapsed_time(d1)
-            backend = "torch SDPA (default backend selection)"
+            backend = sdpa_selected_backend(q, kr, vr)
+            sdpa_ms = time_sdpa(q, kr, vr, stream, d0, d1)
+            per_backend = time_sdpa_backends(q, kr, vr, stream, d0, d1)
             del kr, vr
         except RuntimeError as exc:  # pragma: no cover
             backend = f"unavailable: {exc}"[:120]
         dense = {"flops": 4 * D * dense_pairs, "ours_ms": ours_ms,
                  "ours_tflops": 4 * D * dense_pairs / (ours_ms * 1e-3) / 1e12,
-                 "sdpa_ms": sdpa_ms, "sdpa_backend": backend,
+                 "sdpa_ms": sdpa_ms, "sdpa_backend": backend, "sdpa_ms_per_backend": per_backend,
                  "sdpa_tflops": (4 * D * dense_pairs / (sdpa_ms * 1e-3) / 1e12) if sdpa_ms else None}
         del dout
 

@@ -347,6 +347,17 @@ cudaError_t run_kv_select(const Call& c, const msa_tensor* q, const msa_tensor* 
   return e;
 }
 
+// Every host-side check of a vertical-slash call that does not involve the
+// workspace; on MSA_OK, c and L describe the call.
+int vs_check(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v, int64_t vertical_topk,
+             int64_t slash, const msa_tensor* out, const msa_opts* opts, Call& c, VSLayout& L) {
+  const int s = prepare(q, k, v, out, opts, c);
+  if (s) return s;
+  if (vertical_topk <= 0 || slash <= 0) return MSA_ERR_INVALID;
+  L = vs_layout(c.g, vertical_topk, slash);
+  return MSA_OK;
+}
+
 KvMask base_mask(const Call& c, int kind) {
   KvMask m;
   std::memset(&m, 0, sizeof(m));
@@ -358,6 +369,16 @@ KvMask base_mask(const Call& c, int kind) {
 }  // namespace
 
 void note_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n)); }
+
+int vertical_slash_need(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v,
+                        int64_t vertical_topk, int64_t slash, const msa_tensor* out,
+                        const msa_opts* opts, size_t* need) {
+  Call c;
+  VSLayout L;
+  const int s = vs_check(q, k, v, vertical_topk, slash, out, opts, c, L);
+  if (s == MSA_OK) *need = L.total;
+  return s;
+}
 
 }  // namespace msa
 
@@ -393,10 +414,9 @@ int msa_vertical_slash(const msa_tensor* q, const msa_tensor* k, const msa_tenso
                        int64_t vertical_topk, int64_t slash, msa_tensor* out,
                        const msa_opts* opts) {
   Call c;
-  int s = prepare(q, k, v, out, opts, c);
+  VSLayout L;
+  int s = vs_check(q, k, v, vertical_topk, slash, out, opts, c, L);
   if (s) return s;
-  if (vertical_topk <= 0 || slash <= 0) return MSA_ERR_INVALID;
-  const VSLayout L = vs_layout(c.g, vertical_topk, slash);
   if ((s = check_workspace(c, L.total))) return s;
   void* ws = opts->workspace;
   CUtensorMap mq, mk, mv, mkc, mvc;
@@ -470,6 +490,10 @@ int msa_vertical_slash(const msa_tensor* q, const msa_tensor* k, const msa_tenso
     cp(x->vertical, L.vertical, U * L.kv * sizeof(int32_t));
     cp(x->slash, L.slash, U * L.ks * sizeof(int32_t));
     cp(x->tile_dist, L.tile_dist, U * L.dist_words * sizeof(uint32_t));
+    cp(x->col_chunks, L.col_chunks, U * c.g.NQ * L.chunk_words * sizeof(uint32_t));
+    if (x->col_count && e == cudaSuccess)
+      e = launch_vs_col_count(c.g, at<int32_t>(ws, L.vertical), L.kv, at<uint32_t>(ws, L.tile_dist),
+                              L.dist_words, x->col_count, c.st, &launches);
   }
   return finish(e, launches);
 }

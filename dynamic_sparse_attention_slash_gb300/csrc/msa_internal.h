@@ -7,6 +7,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include "../../include/msa.h"
+
 namespace msa {
 
 constexpr int kHeadDim = 128;
@@ -109,6 +111,13 @@ struct KvMask {
 // Adds n to the library's kernel-launch counter (msa_kernel_launches).
 void note_launches(int n);
 
+// Every host-side check msa_vertical_slash makes on its arguments before it
+// looks at the workspace (shapes, strides, overlaps, options, line counts); on
+// MSA_OK, *need holds the workspace bytes that call needs.  Enqueues nothing.
+int vertical_slash_need(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v,
+                        int64_t vertical_topk, int64_t slash, const msa_tensor* out,
+                        const msa_opts* opts, size_t* need);
+
 // ---------------------------------------------------------------- launches
 cudaError_t launch_vs_estimate(const Geometry& g, const UnitMap& u, TensorView q, TensorView k,
                                int last_q, float* partial, int n_split, float* row_stats,
@@ -137,6 +146,10 @@ cudaError_t launch_vs_index(const Geometry& g, const UnitMap& u, TensorView k, T
                             int32_t* qdelta_count, uint32_t* col_chunks, int chunk_words,
                             __nv_bfloat16* kc, __half* vc, int kv_pad, uint32_t* status,
                             cudaStream_t st, int* n_launch);
+// Export only: columns per row block of the vertical-slash format ([units][NB]).
+cudaError_t launch_vs_col_count(const Geometry& g, const int32_t* vertical, int kv,
+                                const uint32_t* tile_dist, int dist_words, int32_t* col_count,
+                                cudaStream_t st, int* n_launch);
 cudaError_t launch_bs_index(const Geometry& g, const UnitMap& u, TensorView q, TensorView k,
                             int topk, float* qpool, float* kpool, int32_t* block_count,
                             int32_t* block_ids, int32_t* tiles, int32_t* tile_count,

@@ -134,7 +134,6 @@ __device__ __forceinline__ int n_items(const PrefillParams& P, int unit, int c, 
                                        int n_tiles) {
   const int pA = 2 * c;
   if (P.kind == kPrefillVS) return n_chunks + n_tiles;
-  if (P.kind == kPrefillBS) return P.bs_tile_count[static_cast<int64_t>(unit) * P.npair + c];  // never taken
   int sink_hi, loc_lo;
   st_ranges(P, pA, sink_hi, loc_lo);
   return sink_hi + (pair_qmax(P, pA) - loc_lo + 1);
@@ -142,6 +141,7 @@ __device__ __forceinline__ int n_items(const PrefillParams& P, int unit, int c, 
 
 // Item i of pair c.  Vertical-slash: column chunks first (ascending), then key
 // tiles ascending (largest distance first; n_hi from vs_tiles_upto).
+// Streaming: the sink tiles, then the local window's tiles, ascending.
 __device__ __forceinline__ Item get_item(const PrefillParams& P, int unit, int c, int i,
                                          int n_chunks, int n_hi) {
   const int pA = 2 * c, pB = pA + 1;
@@ -181,24 +181,12 @@ __device__ __forceinline__ Item get_item(const PrefillParams& P, int unit, int c
     it.qmask[1] = mb;
     return it;
   }
-  if (P.kind == kPrefillBS) {
-    // Never taken: launch_prefill refuses block-sparse plans, whose lists now
-    // pair 64-key blocks per query tile (prefill_tile.cu).  This branch reads
-    // the earlier pair format of 128-key tiles and stays compiled in because
-    // the kernel measured 0.6-1 % faster on vertical-slash heads with it
-    // (63.5-63.7 ms against 64.1-64.3 ms on the 128K step without it, and with
-    // the kernel specialised per head kind at compile time).
-    const int32_t e = P.bs_tiles[(static_cast<int64_t>(unit) * P.npair + c) * P.bs_tile_cap + i];
-    it.idx = e >> 8;
-    it.qmask[0] = static_cast<uint32_t>(e & 15);
-    it.qmask[1] = static_cast<uint32_t>((e >> 4) & 15);
-  } else {
-    int sink_hi, loc_lo;
-    st_ranges(P, pA, sink_hi, loc_lo);
-    it.idx = i < sink_hi ? i : loc_lo + (i - sink_hi);
-    it.qmask[0] = quad_mask_st(P, pA, it.idx);
-    it.qmask[1] = quad_mask_st(P, pB, it.idx);
-  }
+  // streaming
+  int sink_hi, loc_lo;
+  st_ranges(P, pA, sink_hi, loc_lo);
+  it.idx = i < sink_hi ? i : loc_lo + (i - sink_hi);
+  it.qmask[0] = quad_mask_st(P, pA, it.idx);
+  it.qmask[1] = quad_mask_st(P, pB, it.idx);
   return it;
 }
 

@@ -142,7 +142,52 @@ __global__ void vs_gather_kernel(const __grid_constant__ GatherArgs a) {
   if (__any_sync(0xffffffffu, bad) && lane == 0 && a.status) atomicOr(a.status, kStatusRange);
 }
 
+// Export only (the per-row-block column counts of the format): one warp per
+// (unit, row block m) counts the chosen keys j <= 64m + 63 whose tile
+// distance m - j/64 is not active.  The list is ascending, so the warp stops
+// at the first key past the block.
+__global__ void vs_col_count_kernel(const int32_t* __restrict__ vertical, int kv, int NB,
+                                    const uint32_t* __restrict__ tile_dist, int dist_words,
+                                    int32_t* __restrict__ col_count, int n_units) {
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw >= static_cast<int64_t>(n_units) * NB) return;
+  const int unit = static_cast<int>(gw / NB), m = static_cast<int>(gw % NB);
+  const int32_t* V = vertical + static_cast<int64_t>(unit) * kv;
+  const uint32_t* dist = tile_dist + static_cast<int64_t>(unit) * dist_words;
+  const int last_row = 64 * m + 63;
+  int cnt = 0;
+  for (int s0 = 0; s0 < kv; s0 += 32) {
+    const int s = s0 + lane;
+    bool col = false, past = false;
+    if (s < kv) {
+      const int j = V[s];
+      if (j > last_row) {
+        past = true;
+      } else {
+        const int t = m - (j >> 6);
+        col = !((dist[t >> 5] >> (t & 31)) & 1u);
+      }
+    }
+    cnt += __popc(__ballot_sync(0xffffffffu, col));
+    if (__any_sync(0xffffffffu, past)) break;
+  }
+  if (lane == 0) col_count[gw] = cnt;
+}
+
 }  // namespace
+
+cudaError_t launch_vs_col_count(const Geometry& g, const int32_t* vertical, int kv,
+                                const uint32_t* tile_dist, int dist_words, int32_t* col_count,
+                                cudaStream_t st, int* n_launch) {
+  const int64_t warps = static_cast<int64_t>(g.n_units) * g.NB;
+  if (warps == 0) return cudaSuccess;
+  vs_col_count_kernel<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, st>>>(
+      vertical, kv, g.NB, tile_dist, dist_words, col_count, g.n_units);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) ++*n_launch;
+  return e;
+}
 
 cudaError_t launch_vs_index(const Geometry& g, const UnitMap& u, TensorView k, TensorView v,
                             const int32_t* slash, int ks, const int32_t* vertical, int kv,

@@ -18,7 +18,9 @@ from typing import Optional, Sequence
 import torch
 
 _PKG_DIR = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG_DIR, "libmsa.so")
+# MSA_LIBRARY names another build of the same library to load instead (for
+# instance the bounds-checking build, libmsa_checked.so).
+LIB_PATH = os.environ.get("MSA_LIBRARY") or os.path.join(_PKG_DIR, "libmsa.so")
 
 MSA_OK = 0
 MSA_ERR_INVALID = 1
@@ -62,7 +64,8 @@ class MsaIndexExport(ctypes.Structure):
     _fields_ = [("v_score", ctypes.c_void_p), ("s_score", ctypes.c_void_p),
                 ("vertical", ctypes.c_void_p), ("slash", ctypes.c_void_p),
                 ("tile_dist", ctypes.c_void_p), ("block_count", ctypes.c_void_p),
-                ("block_ids", ctypes.c_void_p)]
+                ("block_ids", ctypes.c_void_p), ("col_count", ctypes.c_void_p),
+                ("col_chunks", ctypes.c_void_p)]
 
 
 class MsaKvSelect(ctypes.Structure):
@@ -217,8 +220,11 @@ def _check_buffers(q, kind, p0, p1, heads, export, kv_select):
     U = B * (len(heads) if heads is not None else Hq)
     need = {}
     if kind == MSA_KIND_VERTICAL_SLASH:
+        NQ = (N + 127) // 128
+        chunk_words = ((min(p0, N) + 127) // 128 + 31) // 32
         need = {"v_score": U * N, "s_score": U * N, "vertical": U * min(p0, N),
-                "slash": U * min(p1, N), "tile_dist": U * ((NB + 32) // 32)}
+                "slash": U * min(p1, N), "tile_dist": U * ((NB + 32) // 32),
+                "col_count": U * NB, "col_chunks": U * NQ * chunk_words}
     elif kind == MSA_KIND_BLOCK_SPARSE:
         need = {"block_count": U * NB, "block_ids": U * NB * min(p0, NB)}
     for name, t in (export or {}).items():

@@ -104,10 +104,17 @@ typedef struct msa_tensor {
  *   slash     int32 [units][min(slash, N)]          chosen offsets, ascending
  *   tile_dist uint32 [units][(N/64 + 32) / 32]      bit t set iff 64x64 key tile
  *             m - t is active for row block m (the set is the same for every m)
+ *   col_count  int32 [units][N/64]  number of columns of row block m: chosen keys
+ *              j <= 64 m + 63 whose key tile m - t (t = m - j/64) is not active
+ *   col_chunks uint32 [units][NQ][CW] with NQ = ceil(N/128) query tiles of 128
+ *              rows and CW = ceil(ceil(min(vertical_topk, N)/128)/32) words: bit c
+ *              of tile p is set iff positions [128c, 128c+128) of the ascending
+ *              vertical list hold a column of row block 2p or 2p + 1
  * block-sparse:
  *   block_count int32 [units][N/64]             blocks kept per row block
  *   block_ids   int32 [units][N/64][min(topk, N/64)] kept key blocks, ascending
  *               (entries past block_count are unspecified)
+ * (N/64 and N/128 round up when N is not a multiple.)
  */
 typedef struct msa_index_export {
   float* v_score;
@@ -117,6 +124,8 @@ typedef struct msa_index_export {
   uint32_t* tile_dist;
   int32_t* block_count;
   int32_t* block_ids;
+  int32_t* col_count;
+  uint32_t* col_chunks;
 } msa_index_export;
 
 /*
@@ -230,21 +239,32 @@ int msa_streaming(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v,
  *    enqueued (4 query heads over 2 KV heads at N = 32768 with vertical_topk
  *    1000 and slash 6096 fit; 32 heads over 8 KV heads at that N do not);
  *    invalid arguments return MSA_ERR_INVALID.
- *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current): make that first call
- *    before any stream capture.
+ *  - The first call in a CUDA context (normally: the first call on a device)
+ *    looks up the array's device address (cudaGetSymbolAddress, with that
+ *    device current) and caches it under the context's id: make that first
+ *    call before any stream capture.  A context created anew (for instance
+ *    after cudaDeviceReset) gets a lookup of its own.
  *  - Every call on a device shares the one array, which keeps the last call's
  *    contents (each call clears what must start at zero).  Calls that may
  *    overlap on the GPU (different streams or host threads) race on it; the
  *    caller must serialise them.
- *  - Device-side status (bounded-wait timeouts, the f16 range check of v) lands
- *    in the array and is not reported by this entry point.
+ *  - Device-side status (a bounded wait that gave up) lands in the array;
+ *    msa_vertical_slash_static_status() reads and clears it.
  * stream is a cudaStream_t (NULL: the legacy default stream).
  */
 #define MSA_STATIC_SCRATCH_BYTES (64u << 20)
 int msa_vertical_slash_static(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v,
                               int64_t vertical_topk, int64_t slash, msa_tensor* out,
                               void* stream);
+
+/*
+ * Device status of msa_vertical_slash_static's array on the current device,
+ * as msa_device_status() reports it for a workspace: enqueues a read of the
+ * status word on `stream` after the work already enqueued there, synchronises
+ * that stream, then clears the word.  Returns MSA_OK, MSA_ERR_TIMEOUT, or
+ * MSA_ERR_CUDA if the lookup or the copy failed.  Allocates nothing.
+ */
+int msa_vertical_slash_static_status(void* stream);
 
 /*
  * Recall of the dense attention that a sparse mask keeps, per head (MInference

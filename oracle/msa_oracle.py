@@ -32,8 +32,8 @@ from bf16 inputs converted exactly.  Sources, by page title and section:
             last queries, computed from the row max and the row sum l that the
             attention pass exports; each head keeps its top-scoring tokens.
 
-Readings where the pages are silent or garbled (each one is listed in the
-design notes with its reason):
+Readings where the pages are silent or garbled (the plainest completion in
+each case):
 
 * masked entries are excluded exactly (c -> infinity); a row with no allowed
   key outputs zeros;

@@ -36,17 +36,58 @@ def run_vs(q, k, v, vertical_topk, slash, last_q=64, heads=None):
     U = B * len(heads_l)
     kv, ks = min(vertical_topk, N), min(slash, N)
     dev = q.device
-    ex = {
-        "v_score": torch.empty(U, N, dtype=torch.float32, device=dev),
-        "s_score": torch.empty(U, N, dtype=torch.float32, device=dev),
-        "vertical": torch.empty(U, kv, dtype=torch.int32, device=dev),
-        "slash": torch.empty(U, ks, dtype=torch.int32, device=dev),
-        "tile_dist": torch.empty(U, ((N + 63) // 64 + 32) // 32, dtype=torch.int32, device=dev),
-    }
+    ex = vs_export_buffers(U, N, kv, ks, dev)
     out = msa.msa_vertical_slash(q, k, v, vertical_topk, slash, last_q=last_q, heads=heads,
                                  export=ex)
     torch.cuda.synchronize()
     return out, {name: t.cpu().numpy() for name, t in ex.items()}
+
+
+def vs_export_buffers(U, N, kv, ks, dev):
+    """Device buffers for every vertical-slash export of U units (sizes as in
+    include/msa.h)."""
+    NB, NQ = (N + 63) // 64, (N + 127) // 128
+    return {
+        "v_score": torch.empty(U, N, dtype=torch.float32, device=dev),
+        "s_score": torch.empty(U, N, dtype=torch.float32, device=dev),
+        "vertical": torch.empty(U, kv, dtype=torch.int32, device=dev),
+        "slash": torch.empty(U, ks, dtype=torch.int32, device=dev),
+        "tile_dist": torch.empty(U, (NB + 32) // 32, dtype=torch.int32, device=dev),
+        "col_count": torch.empty(U, NB, dtype=torch.int32, device=dev),
+        "col_chunks": torch.empty(U, NQ, ((kv + 127) // 128 + 31) // 32, dtype=torch.int32,
+                                  device=dev),
+    }
+
+
+def vs_block_columns(V, S, N, m):
+    """Columns of row block m (the oracle's format rule), from the chosen sets."""
+    act = O.vs_active_tiles(S, N, [m])[0]
+    last_row = min(N, (m + 1) * 64) - 1
+    c = V[V <= last_row]
+    return c[~act[c // 64]]
+
+
+def check_vs_columns(ex, u, V, S, N, blocks, what):
+    """The exported column format of unit u, compared exactly with the oracle's
+    columns on row blocks `blocks`: the per-row-block count, and every
+    128-position chunk of the vertical list that the block's query tile
+    needs (the chunk words of a query tile are checked when both of its row
+    blocks are in `blocks`, or when its second block is past the sequence)."""
+    NB = (N + 63) // 64
+    words = np.asarray(ex["col_chunks"][u], dtype=np.int64) & 0xFFFFFFFF
+    cols = {m: vs_block_columns(V, S, N, m) for m in blocks}
+    for m in blocks:
+        assert int(ex["col_count"][u, m]) == cols[m].size, (
+            f"{what}: row block {m} has {int(ex['col_count'][u, m])} columns, oracle {cols[m].size}")
+    for p in sorted({m // 2 for m in blocks}):
+        pair = [m for m in (2 * p, 2 * p + 1) if m < NB]
+        if not all(m in cols for m in pair):
+            continue
+        want = np.zeros(words.shape[1], dtype=np.int64)
+        for m in pair:
+            for c in np.unique(np.searchsorted(V, cols[m]) // 128):
+                want[c // 32] |= 1 << int(c % 32)
+        np.testing.assert_array_equal(words[p], want, err_msg=f"{what}: chunk mask of query tile {p}")
 
 
 def run_bs(q, k, v, topk, heads=None):

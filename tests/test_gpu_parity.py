@@ -220,6 +220,7 @@ def check_vs_case(q, k, v, vertical_topk, slash, last_q=64, heads=None):
             act = O.vs_active_tiles(S, N)
             np.testing.assert_array_equal(P.dist_bits_to_active(ex["tile_dist"][u], NB), act)
             cols = O.vs_columns(V, act, N)
+            P.check_vs_columns(ex, u, V, S, N, list(range(NB)), f"vs b{b} h{h}")
             ref, _ = O.attend_blocks(qn[b, h], kn[b, h // G], vn[b, h // G],
                                      O.vs_block_mask(act, cols, N), scale)
             P.compare_out(np64(out[b, h]), ref, f"vs b{b} h{h}")

@@ -27,12 +27,7 @@ def run_step(w, q, k, v, heads):
     ex = {}
     if heads["vs"]:
         U = B * len(heads["vs"])
-        ex["vs"] = {
-            "v_score": torch.empty(U, N, dtype=torch.float32, device=q.device),
-            "s_score": torch.empty(U, N, dtype=torch.float32, device=q.device),
-            "vertical": torch.empty(U, min(w.vertical_topk, N), dtype=torch.int32, device=q.device),
-            "slash": torch.empty(U, min(w.slash, N), dtype=torch.int32, device=q.device),
-            "tile_dist": torch.empty(U, ((N + 63) // 64 + 32) // 32, dtype=torch.int32, device=q.device)}
+        ex["vs"] = P.vs_export_buffers(U, N, min(w.vertical_topk, N), min(w.slash, N), q.device)
         msa.msa_vertical_slash(q, k, v, w.vertical_topk, w.slash, out, last_q=w.last_q,
                                heads=heads["vs"], export=ex["vs"])
     if heads["bs"]:
@@ -93,6 +88,10 @@ def test_workload_full_size(name):
                     np.testing.assert_array_equal(got, ref_act[r, :m + 1], err_msg=f"h{h} m{m}")
                     if bits is not None:
                         np.testing.assert_array_equal(bits[m], ref_act[r])
+                # the column part of the format, exactly, on the sampled row
+                # blocks and their query tiles' partner blocks
+                col_blocks = sorted({b_ for m in blocks for b_ in (m ^ 1, m) if b_ < (N + 63) // 64})
+                P.check_vs_columns(e, u, V, S, N, col_blocks, f"{name} h{h}")
                 mask = O.vs_row_block_mask(S, V, N)
             elif kind == "bs":
                 u = heads["bs"].index(h)
