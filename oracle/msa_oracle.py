@@ -26,6 +26,12 @@ from bf16 inputs converted exactly.  Sources, by page title and section:
             vertical_slash_sparse_attention(q,k,v,vertical_topk,slash),
             block_sparse_attention(q,k,v,topk) and
             streaming_forward(q,k,v,init_num,local_window_num).
+* [HiP-prune] InfiniteHiP summary (dtcms.com page), section "modular
+            hierarchical token pruning algorithm": the key sequence is split
+            into fixed-length chunks, each chunk is represented by its token
+            with the highest attention score, only the most important chunks
+            go on to the next pruning module; stacked modules refine the
+            block-sparse mask stage by stage for the current query block.
 * [KV-1.5x] "How KV sparsity achieves 1.5x acceleration for vLLM" (Novita AI
             blog), section "Key Techniques / 2. Attention modification": the
             token score is a sum of softmax probabilities over a window of the
@@ -52,6 +58,13 @@ each case):
 * the block-sparse head keeps the diagonal block plus the top-(topk-1) earlier
   blocks by pooled score; streaming keeps blocks [0, init_num) and the
   ``local_window_num`` blocks ending at the query's own block;
+* the hierarchical pruning head scores a key token for query block m as the
+  block's mean-pooled query against the key, scale * Qhat_m . k_j, over the
+  causal candidates j <= 64m + 63; chunks are aligned groups of c 64-token
+  blocks, c decreasing stage by stage down to 1, each dividing the previous;
+  a chunk's score is its highest candidate token score; every stage keeps the
+  chunk holding block m plus the keep-1 best other chunks (ties to the lower
+  chunk), as the block-sparse head keeps its diagonal block;
 * query head h reads KV head h // (Hq / Hkv);
 * KV selection: the exported normaliser is lse = rowmax + ln(l); a window row's
   probabilities are those of the attention the call computed (zero outside
@@ -350,6 +363,75 @@ def streaming_head(q, k, v, init_num: int, local_window_num: int, scale: float |
     return out, {"blocks": sel, "nnz": int(counts.sum())}
 
 
+# ----------------------------------------------------------------------------- hierarchical pruning head
+def check_stages(stages):
+    """Stages [(chunk_blocks, keep), ...] of the hierarchical head: chunk sizes
+    in 64-token blocks, decreasing, each dividing the one before, the last 1;
+    keep >= 1 chunks per stage."""
+    stages = [(int(c), int(kp)) for c, kp in stages]
+    assert stages and stages[-1][0] == 1, "the last stage must select single blocks"
+    for (c0, _), (c1, _) in zip(stages, stages[1:]):
+        assert c0 > c1 and c0 % c1 == 0, "chunk sizes must decrease, each dividing the previous"
+    assert all(c >= 1 and kp >= 1 for c, kp in stages)
+    return stages
+
+
+def hip_token_scores(q, k, m: int, scale: float) -> np.ndarray:
+    """Attention score of every candidate key token for query block m
+    [HiP-prune]: scale * Qhat_m . k_j for the keys j <= 64m + 63 (cut at N),
+    Qhat_m the mean of the block's query rows."""
+    N = q.shape[0]
+    qhat = q[m * BLOCK:min(N, (m + 1) * BLOCK)].mean(0)
+    return (k[:min(N, (m + 1) * BLOCK)] @ qhat) * scale
+
+
+def hierarchical_blocks(q, k, stages, scale: float | None = None):
+    """Kept key blocks per query block after multi-stage pruning [HiP-prune].
+
+    For query block m the candidates start as every key j <= 64m + 63.  Stage
+    (c, keep) splits the candidate keys into chunks of c consecutive 64-token
+    blocks (chunk x = blocks [x c, (x + 1) c)); a chunk's score is the score of
+    its representative, the candidate token with the highest attention score
+    (hip_token_scores); the chunk holding block m and the keep - 1 other
+    chunks with the highest scores (ties to the lower chunk) stay, and the
+    keys of every other chunk leave the candidates.  The last stage has c = 1:
+    its kept blocks, ascending, are the block-sparse mask of m (at most
+    min(keep_last, m + 1) blocks).  Returns (blocks per query block, the
+    per-stage kept chunk lists [m][stage])."""
+    stages = check_stages(stages)
+    N, d = q.shape
+    scale = default_scale(d) if scale is None else scale
+    NB = (N + BLOCK - 1) // BLOCK
+    sel, kept_chunks = [], []
+    for m in range(NB):
+        t = hip_token_scores(q, k, m, scale)
+        blk = np.arange(t.size) // BLOCK  # key block of every candidate key
+        cand = np.ones(t.size, dtype=bool)
+        per_stage = []
+        for c, keep in stages:
+            chunk = blk // c
+            own = m // c
+            live = np.unique(chunk[cand])
+            score = {int(x): float(t[cand & (chunk == x)].max()) for x in live}
+            others = sorted((x for x in score if x != own), key=lambda x: (-score[x], x))
+            kept = sorted(others[:keep - 1] + [own])
+            per_stage.append(np.array(kept, dtype=np.int64))
+            cand &= np.isin(chunk, kept)
+        sel.append(np.unique(blk[cand]).astype(np.int64))
+        kept_chunks.append(per_stage)
+    return sel, kept_chunks
+
+
+def hierarchical_head(q, k, v, stages, scale: float | None = None):
+    """One hierarchical-pruning head end to end: kept blocks, then block-sparse
+    attention over them [HiP-prune], [MInf-1]."""
+    N, d = q.shape
+    scale = default_scale(d) if scale is None else scale
+    sel, kept = hierarchical_blocks(q, k, stages, scale)
+    out, counts = attend_blocks(q, k, v, block_mask_from_blocks(sel, N), scale)
+    return out, {"blocks": sel, "stage_chunks": kept, "nnz": int(counts.sum())}
+
+
 # ----------------------------------------------------------------------------- multi-head entry points
 def _kv_head(h: int, n_q: int, n_kv: int) -> int:
     return h // (n_q // n_kv)
@@ -400,6 +482,20 @@ def streaming_forward(q, k, v, init_num, local_window_num, heads=None, scale=Non
             g = _kv_head(h, Hq, k.shape[1])
             out[b, t], recs[(b, h)] = streaming_head(q[b, h], k[b, g], v[b, g], init_num,
                                                      local_window_num, scale)
+    return out, recs
+
+
+def hierarchical_sparse_attention(q, k, v, stages, heads=None, scale=None):
+    """The hierarchical pruning head on q [B,Hq,N,d], k/v [B,Hkv,N,d] [HiP-prune]."""
+    q, k, v = as_f64(q), as_f64(k), as_f64(v)
+    B, Hq, N, d = q.shape
+    heads = list(range(Hq)) if heads is None else list(heads)
+    out = np.zeros((B, len(heads), N, d))
+    recs = {}
+    for b in range(B):
+        for t, h in enumerate(heads):
+            g = _kv_head(h, Hq, k.shape[1])
+            out[b, t], recs[(b, h)] = hierarchical_head(q[b, h], k[b, g], v[b, g], stages, scale)
     return out, recs
 
 
