@@ -18,9 +18,9 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libmsa.so")
 
-SOURCES = ["msa_api.cu", "estimate.cu", "topk.cu", "vs_index.cu", "bs_index.cu", "prefill.cu",
-           "prefill_tile.cu", "v_f16.cu", "static_scratch.cu", "kv_select.cu", "recall.cu",
-           "selftest.cu"]
+SOURCES = ["msa_api.cu", "estimate.cu", "topk.cu", "vs_index.cu", "bs_index.cu", "hip_index.cu",
+           "prefill.cu", "prefill_tile.cu", "v_f16.cu", "static_scratch.cu", "kv_select.cu",
+           "recall.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "--expt-relaxed-constexpr"]

@@ -387,11 +387,8 @@ __global__ void __launch_bounds__(32 * kTilesWarps) bs_tiles_kernel(TileArgs a) 
 
 }  // namespace
 
-cudaError_t launch_bs_index(const Geometry& g, const UnitMap& u, TensorView q, TensorView k,
-                            int topk, float* qpool, float* kpool, int32_t* block_count,
-                            int32_t* block_ids, int32_t* tiles, int32_t* tile_count,
-                            int tile_cap, cudaStream_t st, int* n_launch) {
-  cudaError_t e;
+cudaError_t launch_pool_q(const Geometry& g, const UnitMap& u, TensorView q, float* qpool,
+                          cudaStream_t st, int* n_launch) {
   PoolArgs pa;
   pa.u = u;
   pa.NB = g.NB;
@@ -403,8 +400,50 @@ cudaError_t launch_bs_index(const Geometry& g, const UnitMap& u, TensorView q, T
   pa.use_units = true;
   pa.out = qpool;
   bs_pool_kernel<<<dim3((g.NB + kPoolWarps - 1) / kPoolWarps, g.n_units), 32 * kPoolWarps, 0, st>>>(pa);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) ++*n_launch;
+  return e;
+}
+
+cudaError_t launch_bs_tiles(const Geometry& g, int kb, const int32_t* block_count,
+                            const int32_t* block_ids, int32_t* tiles, int32_t* tile_count,
+                            int tile_cap, cudaStream_t st, int* n_launch) {
+  TileArgs ta;
+  ta.NB = g.NB;
+  ta.NQ = g.NQ;
+  ta.kb = kb;
+  ta.tile_cap = tile_cap;
+  ta.n_units = g.n_units;
+  ta.block_count = block_count;
+  ta.block_ids = block_ids;
+  ta.tiles = tiles;
+  ta.tile_count = tile_count;
+  ta.words_per_warp = 2 * ((g.NB + 31) >> 5);
+  const int tsmem = kTilesWarps * ta.words_per_warp * 4;
+  cudaError_t e;
+  if (tsmem > 48 * 1024) {
+    e = cudaFuncSetAttribute(bs_tiles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tsmem);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t warps = static_cast<int64_t>(g.n_units) * g.NQ;
+  bs_tiles_kernel<<<static_cast<unsigned>((warps + kTilesWarps - 1) / kTilesWarps),
+                    32 * kTilesWarps, tsmem, st>>>(ta);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   ++*n_launch;
+  return cudaSuccess;
+}
+
+cudaError_t launch_bs_index(const Geometry& g, const UnitMap& u, TensorView q, TensorView k,
+                            int topk, float* qpool, float* kpool, int32_t* block_count,
+                            int32_t* block_ids, int32_t* tiles, int32_t* tile_count,
+                            int tile_cap, cudaStream_t st, int* n_launch) {
+  cudaError_t e = launch_pool_q(g, u, q, qpool, st, n_launch);
+  if (e != cudaSuccess) return e;
+  PoolArgs pa;
+  pa.u = u;
+  pa.NB = g.NB;
+  pa.N = g.N;
+  pa.G = g.G;
   pa.x = k.data; pa.sb = k.sb; pa.sh = k.sh; pa.sn = k.sn;
   pa.n_heads_x = g.Hkv;
   pa.kv = kv_heads_of(g.Hkv, g.G, u);  // the KV heads the selected query heads read
@@ -446,28 +485,8 @@ cudaError_t launch_bs_index(const Geometry& g, const UnitMap& u, TensorView q, T
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   ++*n_launch;
-  TileArgs ta;
-  ta.NB = g.NB;
-  ta.NQ = g.NQ;
-  ta.kb = sa.kb;
-  ta.tile_cap = tile_cap;
-  ta.n_units = g.n_units;
-  ta.block_count = block_count;
-  ta.block_ids = block_ids;
-  ta.tiles = tiles;
-  ta.tile_count = tile_count;
-  ta.words_per_warp = 2 * ((g.NB + 31) >> 5);
-  const int tsmem = kTilesWarps * ta.words_per_warp * 4;
-  if (tsmem > 48 * 1024) {
-    e = cudaFuncSetAttribute(bs_tiles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tsmem);
-    if (e != cudaSuccess) return e;
-  }
-  const int64_t warps = static_cast<int64_t>(g.n_units) * g.NQ;
-  bs_tiles_kernel<<<static_cast<unsigned>((warps + kTilesWarps - 1) / kTilesWarps),
-                    32 * kTilesWarps, tsmem, st>>>(ta);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  ++*n_launch;
-  return cudaSuccess;
+  return launch_bs_tiles(g, sa.kb, block_count, block_ids, tiles, tile_count, tile_cap, st,
+                         n_launch);
 }
 
 }  // namespace msa

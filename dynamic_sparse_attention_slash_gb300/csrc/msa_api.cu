@@ -216,6 +216,47 @@ BSLayout bs_layout(const Geometry& g, int64_t topk) {
   return L;
 }
 
+// Hierarchical pruning head: pooled queries, the block maxima of one slab of
+// query blocks, the kept blocks (block-sparse format) and their item lists.
+struct HIPLayout {
+  int kb, tile_cap, slab;
+  size_t qpool, rmax, block_count, block_ids, tiles, tile_count, v16, total;
+};
+
+HIPLayout hip_layout(const Geometry& g, int64_t keep_last) {
+  HIPLayout L;
+  L.kb = static_cast<int>(keep_last < g.NB ? keep_last : g.NB);
+  L.tile_cap = L.kb;
+  L.slab = hip_slab_rows(g.n_units, g.NB);
+  const size_t U = static_cast<size_t>(g.n_units);
+  Carver c;
+  c.off = kStatusBytes;
+  L.qpool = c.take<float>(U * g.NB * kHeadDim);
+  L.rmax = c.take<float>(U * L.slab * g.NB);
+  L.block_count = c.take<int32_t>(U * g.NB);
+  L.block_ids = c.take<int32_t>(U * g.NB * L.kb);
+  L.tiles = c.take<int32_t>(U * g.NQ * L.tile_cap * 2);
+  L.tile_count = c.take<int32_t>(U * g.NQ);
+  L.v16 = c.take<__half>(v16_elems(g));
+  L.total = (c.off + 255) & ~size_t{255};
+  return L;
+}
+
+// Stage list of the hierarchical head (see include/msa.h); fills c[] and keep[]
+// (keep clamped to what can matter: one more than the number of blocks).
+int check_hip_stages(const msa_hip_stage* stages, int32_t n, int NB, int32_t* c, int32_t* keep) {
+  if (!stages || n < 1 || n > MSA_HIP_MAX_STAGES) return MSA_ERR_INVALID;
+  for (int s = 0; s < n; ++s) {
+    const int64_t cb = stages[s].chunk_blocks, kp = stages[s].keep;
+    if (cb < 1 || cb > (int64_t{1} << 21) || kp < 1) return MSA_ERR_INVALID;
+    if (s > 0 && (cb >= stages[s - 1].chunk_blocks || stages[s - 1].chunk_blocks % cb != 0))
+      return MSA_ERR_INVALID;
+    c[s] = static_cast<int32_t>(cb);
+    keep[s] = static_cast<int32_t>(kp < NB + 1 ? kp : NB + 1);
+  }
+  return stages[n - 1].chunk_blocks == 1 ? MSA_OK : MSA_ERR_INVALID;
+}
+
 struct STLayout {
   size_t v16, total;
 };
@@ -407,6 +448,10 @@ size_t msa_workspace_bytes(int kind, const msa_tensor* q, const msa_tensor* k, i
     return bs_layout(g, p0).total;
   }
   if (kind == MSA_KIND_STREAMING) return st_layout(g).total;
+  if (kind == MSA_KIND_HIERARCHICAL) {
+    if (p0 <= 0) return 0;
+    return hip_layout(g, p0).total;
+  }
   return 0;
 }
 
@@ -531,6 +576,71 @@ int msa_block_sparse(const msa_tensor* q, const msa_tensor* k, const msa_tensor*
   if (e != cudaSuccess) return finish(e, launches);
   PrefillParams p = base_prefill(c, out, at<uint32_t>(ws, 0));
   p.kind = kPrefillBS;
+  p.bs_tiles = at<int32_t>(ws, L.tiles);
+  p.bs_tile_count = at<int32_t>(ws, L.tile_count);
+  p.bs_tile_cap = L.tile_cap;
+  tm.begin(MSA_STAGE_PREFILL);
+  e = launch_prefill_tile(p, mq, mk64, mv64, c.st, &launches);
+  tm.end(MSA_STAGE_PREFILL);
+  if (e != cudaSuccess) return finish(e, launches);
+  {
+    KvMask km = base_mask(c, kPrefillBS);
+    km.block_count = at<int32_t>(ws, L.block_count);
+    km.block_ids = at<int32_t>(ws, L.block_ids);
+    km.kb = L.kb;
+    e = run_kv_select(c, q, k, km, tm, &launches);
+    if (e != cudaSuccess) return finish(e, launches);
+  }
+  if (const msa_index_export* x = opts->export_idx) {
+    const size_t U = static_cast<size_t>(c.g.n_units);
+    if (x->block_count)
+      e = cudaMemcpyAsync(x->block_count, at<void>(ws, L.block_count), U * c.g.NB * sizeof(int32_t),
+                          cudaMemcpyDeviceToDevice, c.st);
+    if (x->block_ids && e == cudaSuccess)
+      e = cudaMemcpyAsync(x->block_ids, at<void>(ws, L.block_ids),
+                          U * c.g.NB * L.kb * sizeof(int32_t), cudaMemcpyDeviceToDevice, c.st);
+  }
+  return finish(e, launches);
+}
+
+int msa_hierarchical(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v,
+                     const msa_hip_stage* stages, int32_t n_stages, msa_tensor* out,
+                     const msa_opts* opts) {
+  Call c;
+  int s = prepare(q, k, v, out, opts, c);
+  if (s) return s;
+  int32_t sc[MSA_HIP_MAX_STAGES], sk[MSA_HIP_MAX_STAGES];
+  if ((s = check_hip_stages(stages, n_stages, c.g.NB, sc, sk))) return s;
+  const HIPLayout L = hip_layout(c.g, stages[n_stages - 1].keep);
+  if ((s = check_workspace(c, L.total))) return s;
+  void* ws = opts->workspace;
+  // the kept blocks feed the block-sparse attention kernel: K and the f16 copy
+  // of v are read in 64-key boxes
+  CUtensorMap mq, mk64, mv64;
+  if ((s = make_map_4d(&mq, q)) ||
+      (s = make_map_4d(&mk64, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 64)) ||
+      (s = make_map_f16(&mv64, at<void>(ws, L.v16), c.g, 64)))
+    return s;
+  const StageTimer tm{opts->stage_events, c.st};
+  int launches = 0;
+  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), c.st);
+  if (e != cudaSuccess) return finish(e, launches);
+  tm.begin(MSA_STAGE_INDEX);
+  e = launch_v_to_f16(view(v), c.g, c.u, at<__half>(ws, L.v16), at<uint32_t>(ws, 0), c.st,
+                      &launches);
+  if (e == cudaSuccess) e = launch_pool_q(c.g, c.u, view(q), at<float>(ws, L.qpool), c.st, &launches);
+  if (e == cudaSuccess)
+    e = launch_hip_index(c.g, c.u, view(k), at<float>(ws, L.qpool), sc, sk, n_stages,
+                         at<float>(ws, L.rmax), L.slab, at<int32_t>(ws, L.block_count),
+                         at<int32_t>(ws, L.block_ids), L.kb, c.st, &launches);
+  if (e == cudaSuccess)
+    e = launch_bs_tiles(c.g, L.kb, at<int32_t>(ws, L.block_count), at<int32_t>(ws, L.block_ids),
+                        at<int32_t>(ws, L.tiles), at<int32_t>(ws, L.tile_count), L.tile_cap, c.st,
+                        &launches);
+  tm.end(MSA_STAGE_INDEX);
+  if (e != cudaSuccess) return finish(e, launches);
+  PrefillParams p = base_prefill(c, out, at<uint32_t>(ws, 0));
+  p.kind = kPrefillBS;  // same per-query-tile item lists as the block-sparse head
   p.bs_tiles = at<int32_t>(ws, L.tiles);
   p.bs_tile_count = at<int32_t>(ws, L.tile_count);
   p.bs_tile_cap = L.tile_cap;

@@ -154,6 +154,22 @@ cudaError_t launch_bs_index(const Geometry& g, const UnitMap& u, TensorView q, T
                             int topk, float* qpool, float* kpool, int32_t* block_count,
                             int32_t* block_ids, int32_t* tiles, int32_t* tile_count,
                             int tile_cap, cudaStream_t st, int* n_launch);
+// Mean of each 64-row block of q for the selected units ([units][NB][128] f32).
+cudaError_t launch_pool_q(const Geometry& g, const UnitMap& u, TensorView q, float* qpool,
+                          cudaStream_t st, int* n_launch);
+// Per-query-tile item lists of the one-tile prefill from kept blocks per row
+// block ([units][NB] counts, [units][NB][kb] ascending ids).
+cudaError_t launch_bs_tiles(const Geometry& g, int kb, const int32_t* block_count,
+                            const int32_t* block_ids, int32_t* tiles, int32_t* tile_count,
+                            int tile_cap, cudaStream_t st, int* n_launch);
+// Hierarchical pruning head: block maxima of the token scores and the stages,
+// slab by slab of slab_rows query blocks; writes kept blocks in the
+// block-sparse format.  hip_slab_rows gives the slab height for a call.
+int hip_slab_rows(int n_units, int NB);
+cudaError_t launch_hip_index(const Geometry& g, const UnitMap& u, TensorView k, const float* qpool,
+                             const int32_t* stage_c, const int32_t* stage_keep, int n_stages,
+                             float* rmax, int slab_rows, int32_t* block_count, int32_t* block_ids,
+                             int kb, cudaStream_t st, int* n_launch);
 cudaError_t launch_v_to_f16(TensorView v, const Geometry& g, const UnitMap& u, __half* dst,
                             uint32_t* status, cudaStream_t st, int* n_launch);
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,

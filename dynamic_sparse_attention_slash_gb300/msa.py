@@ -33,6 +33,8 @@ MSA_ERR_RANGE = 6
 MSA_KIND_VERTICAL_SLASH = 0
 MSA_KIND_BLOCK_SPARSE = 1
 MSA_KIND_STREAMING = 2
+MSA_KIND_HIERARCHICAL = 3
+MSA_HIP_MAX_STAGES = 8
 
 MSA_STAGE_ESTIMATE = 0
 MSA_STAGE_TOPK = 1
@@ -44,7 +46,8 @@ MSA_STAGE_COUNT = 5
 EXPORTED_SYMBOLS = (
     "msa_vertical_slash", "msa_block_sparse", "msa_streaming", "msa_workspace_bytes",
     "msa_device_status", "msa_status_string", "msa_kernel_launches", "msa_mass_recall",
-    "msa_selftest_wait_timeout",
+    "msa_selftest_wait_timeout", "msa_hierarchical", "msa_vertical_slash_static",
+    "msa_vertical_slash_static_status",
 )
 
 
@@ -66,6 +69,10 @@ class MsaIndexExport(ctypes.Structure):
                 ("tile_dist", ctypes.c_void_p), ("block_count", ctypes.c_void_p),
                 ("block_ids", ctypes.c_void_p), ("col_count", ctypes.c_void_p),
                 ("col_chunks", ctypes.c_void_p)]
+
+
+class MsaHipStage(ctypes.Structure):
+    _fields_ = [("chunk_blocks", ctypes.c_int64), ("keep", ctypes.c_int64)]
 
 
 class MsaKvSelect(ctypes.Structure):
@@ -102,6 +109,8 @@ def load_library():
     lib.msa_block_sparse.restype = ctypes.c_int
     lib.msa_streaming.argtypes = [T, T, T, ctypes.c_int64, ctypes.c_int64, T, O]
     lib.msa_streaming.restype = ctypes.c_int
+    lib.msa_hierarchical.argtypes = [T, T, T, ctypes.POINTER(MsaHipStage), ctypes.c_int32, T, O]
+    lib.msa_hierarchical.restype = ctypes.c_int
     lib.msa_workspace_bytes.argtypes = [ctypes.c_int, T, T, ctypes.c_int64, ctypes.c_int64,
                                         ctypes.c_int32]
     lib.msa_workspace_bytes.restype = ctypes.c_size_t
@@ -225,7 +234,7 @@ def _check_buffers(q, kind, p0, p1, heads, export, kv_select):
         need = {"v_score": U * N, "s_score": U * N, "vertical": U * min(p0, N),
                 "slash": U * min(p1, N), "tile_dist": U * ((NB + 32) // 32),
                 "col_count": U * NB, "col_chunks": U * NQ * chunk_words}
-    elif kind == MSA_KIND_BLOCK_SPARSE:
+    elif kind in (MSA_KIND_BLOCK_SPARSE, MSA_KIND_HIERARCHICAL):
         need = {"block_count": U * NB, "block_ids": U * NB * min(p0, NB)}
     for name, t in (export or {}).items():
         if t is None:
@@ -339,6 +348,28 @@ def msa_block_sparse(q, k, v, topk: int, out=None, *, scale: Optional[float] = N
     """Block-sparse attention (MInference 1.0 overview, section 2.2)."""
     return _run("msa_block_sparse", MSA_KIND_BLOCK_SPARSE, q, k, v, (ctypes.c_int64(topk),), out,
                 topk, 0, 0, scale, heads, workspace, export, stage_events, stream, kv_select)
+
+
+def hip_stages(stages):
+    """ctypes array of msa_hip_stage from [(chunk_blocks, keep), ...]."""
+    arr = (MsaHipStage * len(stages))()
+    for i, (c, kp) in enumerate(stages):
+        arr[i].chunk_blocks = int(c)
+        arr[i].keep = int(kp)
+    return arr
+
+
+def msa_hierarchical(q, k, v, stages, out=None, *, scale: Optional[float] = None,
+                     heads: Optional[Sequence[int]] = None, workspace=None, export=None,
+                     stage_events=None, stream=None, kv_select=None):
+    """Hierarchical multi-stage pruning head (InfiniteHiP summary page, modular
+    hierarchical token pruning).  stages: [(chunk_blocks, keep), ...], chunk
+    sizes in 64-token blocks, decreasing, each dividing the previous, the last 1."""
+    arr = hip_stages(stages)
+    keep_last = int(stages[-1][1]) if len(stages) else 0
+    return _run("msa_hierarchical", MSA_KIND_HIERARCHICAL, q, k, v,
+                (arr, ctypes.c_int32(len(stages))), out, keep_last, 0, 0, scale, heads, workspace,
+                export, stage_events, stream, kv_select)
 
 
 def msa_streaming(q, k, v, init_num: int, local_window_num: int, out=None, *,

@@ -73,6 +73,7 @@ extern "C" {
 #define MSA_KIND_VERTICAL_SLASH 0
 #define MSA_KIND_BLOCK_SPARSE 1
 #define MSA_KIND_STREAMING 2
+#define MSA_KIND_HIERARCHICAL 3
 
 /* Stage ids for msa_opts.stage_events (CUDA events recorded around each stage). */
 #define MSA_STAGE_ESTIMATE 0 /* vertical-slash: last-query estimate (both passes) */
@@ -221,6 +222,39 @@ int msa_streaming(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v,
                   const msa_opts* opts);
 
 /*
+ * Hierarchical multi-stage pruning head (InfiniteHiP summary page, section on
+ * the modular hierarchical token pruning algorithm: the key sequence is cut
+ * into fixed-length chunks, each represented by its token with the highest
+ * attention score; only the best chunks pass on, and stacked stages refine the
+ * block-sparse mask of the current query block).
+ *
+ * For query block m (64 rows) a key token's score is scale * Qhat_m . k_j,
+ * Qhat_m the mean of the block's query rows, over the candidates j <= 64m + 63.
+ * Stage s splits the surviving candidates into chunks of
+ * stages[s].chunk_blocks consecutive 64-token blocks (chunk x = blocks
+ * [x c, (x + 1) c)); a chunk's score is its best surviving token's score; the
+ * chunk holding block m and the stages[s].keep - 1 best other chunks (ties to
+ * the lower chunk) survive.  The last stage has chunk_blocks = 1: its
+ * surviving blocks, ascending (block m included), are the mask, and attention
+ * runs over them as for the block-sparse head.
+ *
+ * 1 <= n_stages <= MSA_HIP_MAX_STAGES; chunk_blocks >= 1, strictly
+ * decreasing, each dividing the one before, the last 1; keep >= 1.  Other
+ * stage lists return MSA_ERR_INVALID.  Needs a workspace of
+ * msa_workspace_bytes(MSA_KIND_HIERARCHICAL, q, k, stages[n_stages-1].keep, 0,
+ * n_heads).  The index export fills block_count / block_ids as for the
+ * block-sparse head (min(keep_last, N/64) ids per row block).
+ */
+#define MSA_HIP_MAX_STAGES 8
+typedef struct msa_hip_stage {
+  int64_t chunk_blocks; /* chunk size in 64-token blocks */
+  int64_t keep;         /* chunks kept, the query block's own chunk included */
+} msa_hip_stage;
+int msa_hierarchical(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v,
+                     const msa_hip_stage* stages, int32_t n_stages, msa_tensor* out,
+                     const msa_opts* opts);
+
+/*
  * Vertical-slash attention without a caller-provided workspace.  The MInference
  * pages have no counterpart; this entry point exists for callers that cannot
  * allocate device memory where they run attention: an allocator frozen for the
@@ -288,7 +322,8 @@ int msa_mass_recall(const float* lse, const float* ref_lse, int64_t B, int64_t H
 
 /*
  * Workspace bytes needed by one call.  kind is MSA_KIND_*; p0/p1 are
- * (vertical_topk, slash) for vertical-slash, (topk, unused) for block-sparse.
+ * (vertical_topk, slash) for vertical-slash, (topk, unused) for block-sparse,
+ * (keep of the last stage, unused) for the hierarchical head.
  * n_heads is the number of selected query heads (<= 0: all of q's heads).
  * Returns 0 for invalid arguments.
  */

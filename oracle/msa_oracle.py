@@ -385,7 +385,8 @@ def hip_token_scores(q, k, m: int, scale: float) -> np.ndarray:
     return (k[:min(N, (m + 1) * BLOCK)] @ qhat) * scale
 
 
-def hierarchical_blocks(q, k, stages, scale: float | None = None):
+def hierarchical_blocks(q, k, stages, scale: float | None = None, row_blocks=None,
+                        with_scores: bool = False):
     """Kept key blocks per query block after multi-stage pruning [HiP-prune].
 
     For query block m the candidates start as every key j <= 64m + 63.  Stage
@@ -397,17 +398,19 @@ def hierarchical_blocks(q, k, stages, scale: float | None = None):
     keys of every other chunk leave the candidates.  The last stage has c = 1:
     its kept blocks, ascending, are the block-sparse mask of m (at most
     min(keep_last, m + 1) blocks).  Returns (blocks per query block, the
-    per-stage kept chunk lists [m][stage])."""
+    per-stage kept chunk lists [m][stage]), for every query block or for
+    those in `row_blocks`; with_scores adds the per-stage chunk scores
+    ({chunk: score} for every chunk holding a candidate) as a third item."""
     stages = check_stages(stages)
     N, d = q.shape
     scale = default_scale(d) if scale is None else scale
     NB = (N + BLOCK - 1) // BLOCK
-    sel, kept_chunks = [], []
-    for m in range(NB):
+    sel, kept_chunks, stage_scores = [], [], []
+    for m in (range(NB) if row_blocks is None else row_blocks):
         t = hip_token_scores(q, k, m, scale)
         blk = np.arange(t.size) // BLOCK  # key block of every candidate key
         cand = np.ones(t.size, dtype=bool)
-        per_stage = []
+        per_stage, per_scores = [], []
         for c, keep in stages:
             chunk = blk // c
             own = m // c
@@ -416,9 +419,13 @@ def hierarchical_blocks(q, k, stages, scale: float | None = None):
             others = sorted((x for x in score if x != own), key=lambda x: (-score[x], x))
             kept = sorted(others[:keep - 1] + [own])
             per_stage.append(np.array(kept, dtype=np.int64))
+            per_scores.append(score)
             cand &= np.isin(chunk, kept)
         sel.append(np.unique(blk[cand]).astype(np.int64))
         kept_chunks.append(per_stage)
+        stage_scores.append(per_scores)
+    if with_scores:
+        return sel, kept_chunks, stage_scores
     return sel, kept_chunks
 
 

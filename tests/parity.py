@@ -106,6 +106,48 @@ def run_bs(q, k, v, topk, heads=None):
     return out, {name: t.cpu().numpy() for name, t in ex.items()}
 
 
+def run_hip(q, k, v, stages, heads=None, kv_select=None):
+    """CUDA hierarchical-head call with block export; returns (out, export dict of numpy)."""
+    B, Hq, N, _ = q.shape
+    U = B * (Hq if heads is None else len(heads))
+    NB = (N + 63) // 64
+    kb = min(int(stages[-1][1]), NB)
+    ex = {"block_count": torch.empty(U, NB, dtype=torch.int32, device=q.device),
+          "block_ids": torch.empty(U, NB, kb, dtype=torch.int32, device=q.device)}
+    out = msa.msa_hierarchical(q, k, v, stages, heads=heads, export=ex, kv_select=kv_select)
+    torch.cuda.synchronize()
+    return out, {name: t.cpu().numpy() for name, t in ex.items()}
+
+
+def check_hip_blocks(counts, ids, qn, kn, stages, row_blocks, what):
+    """Kept blocks of one hierarchical head (counts [NB], ids [NB][kb] from the
+    GPU) against the oracle on `row_blocks`.  Exact, except for a row block
+    where some stage's cut is a near-tie in the oracle's own chunk scores (the
+    last kept and the first dropped other chunk within 1e-5 relative): there
+    the GPU may keep either chunk, so only the structure of its set is checked.
+    Returns ({m: GPU blocks} for the attention check, number of near-tie rows)."""
+    sel, _, scores = O.hierarchical_blocks(qn, kn, stages, row_blocks=row_blocks, with_scores=True)
+    keep_last = int(stages[-1][1])
+    got_sel, near = {}, 0
+    for i, m in enumerate(row_blocks):
+        cnt = int(counts[m])
+        got = np.asarray(ids[m, :cnt], dtype=np.int64)
+        assert cnt >= 1 and got[-1] == m and np.all(np.diff(got) > 0), f"{what} m{m}: {got}"
+        assert cnt <= keep_last, f"{what} m{m}: {cnt} blocks"
+        tie = False
+        for st, (c, keep) in enumerate(stages):
+            others = sorted((val for x, val in scores[i][st].items() if x != m // c), reverse=True)
+            if keep >= 2 and len(others) >= keep:
+                a, b = others[keep - 2], others[keep - 1]
+                tie |= abs(a - b) <= TIE_REL * max(abs(a), 1e-30)
+        if tie:
+            near += 1
+        else:
+            np.testing.assert_array_equal(got, sel[i], err_msg=f"{what} m{m}")
+        got_sel[m] = got
+    return got_sel, near
+
+
 def check_topk(gpu_set, oracle_scores, k, what):
     """Exact set equality, except near-ties at the k-th score (see module doc)."""
     ref = O.topk_indices(oracle_scores, k)

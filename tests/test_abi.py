@@ -135,6 +135,44 @@ def test_block_sparse_and_streaming_reject(lib):
     assert lib.msa_streaming(*args, 1, 4, ctypes.byref(out), ctypes.byref(small)) == 3
 
 
+@pytest.mark.parametrize("stages,expect", [
+    ([(4, 3), (1, 4)], 3),            # valid: stops at the missing workspace
+    ([(1, 5)], 3),
+    ([], 1),                          # no stage
+    ([(4, 3), (2, 4)], 1),            # the last stage must select single blocks
+    ([(4, 3), (4, 2), (1, 4)], 1),    # chunk sizes must decrease
+    ([(6, 3), (4, 2), (1, 4)], 1),    # ... each dividing the one before
+    ([(4, 0), (1, 4)], 1),            # keep >= 1
+    ([(0, 3), (1, 4)], 1),
+    ([(2 ** c, 2) for c in range(8, -1, -1)], 1),  # more than MSA_HIP_MAX_STAGES stages
+])
+def test_hierarchical_rejects(lib, stages, expect):
+    from dynamic_sparse_attention_slash_gb300 import msa
+    q, k, v, out = T(), T(H=2), T(H=2), T()
+    arr = msa.hip_stages(stages) if stages else (msa.MsaHipStage * 1)()
+    st = lib.msa_hierarchical(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), arr,
+                              len(stages), ctypes.byref(out), None)
+    assert st == expect
+
+
+def test_hierarchical_workspace_bytes(lib):
+    from dynamic_sparse_attention_slash_gb300 import msa
+    q, k = T(H=32, N=131072), T(H=8, N=131072)
+    w = lib.msa_workspace_bytes(msa.MSA_KIND_HIERARCHICAL, ctypes.byref(q), ctypes.byref(k),
+                                100, 0, 8)
+    NB = 131072 // 64
+    # pooled queries, one slab of block maxima (all 2048 query blocks fit), kept ids
+    assert w >= 8 * NB * (128 * 4 + NB * 4 + 100 * 4) and w % 256 == 0
+    assert lib.msa_workspace_bytes(msa.MSA_KIND_HIERARCHICAL, ctypes.byref(q), ctypes.byref(k),
+                                   0, 0, 8) == 0
+    # long sequences keep the block maxima to one slab of query blocks
+    q2, k2 = T(H=32, N=1 << 20), T(H=8, N=1 << 20)
+    w2 = lib.msa_workspace_bytes(msa.MSA_KIND_HIERARCHICAL, ctypes.byref(q2), ctypes.byref(k2),
+                                 100, 0, 32)
+    NB2 = (1 << 20) // 64
+    assert w2 < 32 * NB2 * NB2 * 4 / 8 and w2 > (512 << 20)
+
+
 def test_status_strings_and_counter(lib):
     for code in range(7):
         assert lib.msa_status_string(code)
