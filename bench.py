@@ -191,7 +191,7 @@ def oracle_sample(w, q, k, v, heads, rows_per_head: int, seed: int = 0):
     scale = 1 / np.sqrt(D)
     flops = 0
     t0 = time.perf_counter()
-    for kind in ("vs", "bs", "st"):
+    for kind in ("vs", "bs", "st", "hip"):
         if not heads[kind]:
             continue
         h = heads[kind][0]
@@ -204,6 +204,9 @@ def oracle_sample(w, q, k, v, heads, rows_per_head: int, seed: int = 0):
             mask = O.vs_block_mask(idx["active"], idx["columns"], N)
         elif kind == "bs":
             sel, _ = O.block_sparse_blocks(qn, kn, w.block_topk, scale)
+            mask = O.block_mask_from_blocks(sel, N)
+        elif kind == "hip":
+            sel, _ = O.hierarchical_blocks(qn, kn, w.hip_stages, scale)
             mask = O.block_mask_from_blocks(sel, N)
         else:
             sel = [O.streaming_blocks(m, w.init_num, w.local_window_num) for m in range((N + 63) // 64)]
@@ -365,6 +368,10 @@ def main():
     if heads["st"]:
         ws["st"] = torch.empty(msa.workspace_bytes(msa.MSA_KIND_STREAMING, q, k, 0, 0,
                                                    len(heads["st"])), dtype=torch.uint8, device=dev)
+    if heads["hip"]:
+        ws["hip"] = torch.empty(msa.workspace_bytes(msa.MSA_KIND_HIERARCHICAL, q, k,
+                                                    w.hip_stages[-1][1], 0, len(heads["hip"])),
+                                dtype=torch.uint8, device=dev)
 
     def new_events():
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * msa.MSA_STAGE_COUNT)]
@@ -385,9 +392,13 @@ def main():
         if heads["st"]:
             msa.msa_streaming(qq, kk, vv, w.init_num, w.local_window_num, oo, heads=heads["st"],
                               workspace=ws["st"], stage_events=ev.get("st"), kv_select=kv)
+        if heads["hip"]:
+            msa.msa_hierarchical(qq, kk, vv, w.hip_stages, oo, heads=heads["hip"],
+                                 workspace=ws["hip"], stage_events=ev.get("hip"),
+                                 export=(export or {}).get("hip"), kv_select=kv)
 
     # exact work of one step, from the GPU's own index sets
-    U_vs, U_bs = B * len(heads["vs"]), B * len(heads["bs"])
+    U_vs, U_bs, U_hip = B * len(heads["vs"]), B * len(heads["bs"]), B * len(heads["hip"])
     export = {}
     if U_vs:
         export["vs"] = {"vertical": torch.empty(U_vs, min(w.vertical_topk, N), dtype=torch.int32, device=dev),
@@ -395,9 +406,12 @@ def main():
                         "tile_dist": torch.empty(U_vs, ((N + 63) // 64 + 32) // 32, dtype=torch.int32, device=dev)}
     if U_bs:
         export["bs"] = {"block_count": torch.empty(U_bs, (N + 63) // 64, dtype=torch.int32, device=dev)}
+    if U_hip:
+        export["hip"] = {"block_count": torch.empty(U_hip, (N + 63) // 64, dtype=torch.int32,
+                                                    device=dev)}
     step(export=export)
     torch.cuda.synchronize()
-    pairs = {"vs": 0, "bs": 0, "st": 0}
+    pairs = {"vs": 0, "bs": 0, "st": 0, "hip": 0}
     exact_line = 0  # vertical-slash pairs on the chosen lines alone (diagnostic)
     if U_vs:
         td, vt = export["vs"]["tile_dist"].cpu().numpy(), export["vs"]["vertical"].cpu().numpy()
@@ -408,6 +422,8 @@ def main():
         pairs["bs"] = bs_pairs(export["bs"]["block_count"].cpu().numpy(), N)
     if heads["st"]:
         pairs["st"] = B * len(heads["st"]) * st_pairs(N, w.init_num, w.local_window_num)
+    if U_hip:  # whole kept blocks, the query block's own always among them
+        pairs["hip"] = bs_pairs(export["hip"]["block_count"].cpu().numpy(), N)
     flops = {kk_: 4 * D * vv_ for kk_, vv_ in pairs.items()}
     step_flops = sum(flops.values())
     dense_pairs = B * w.n_q_heads * N * (N + 1) // 2
@@ -418,7 +434,8 @@ def main():
     status = {kind: msa.device_status(buf) for kind, buf in ws.items()}
 
     # ---- timed region (device-resident inputs)
-    ev_sets = [{kind: new_events() for kind in ("vs", "bs", "st") if heads[kind]} for _ in range(args.steps)]
+    kinds = [kind for kind in ("vs", "bs", "st", "hip") if heads[kind]]
+    ev_sets = [{kind: new_events() for kind in kinds} for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     l0 = msa.kernel_launches()
@@ -441,9 +458,7 @@ def main():
 
     stage_ms = {}
     names = ["estimate", "topk", "index", "prefill"]
-    for kind in ("vs", "bs", "st"):
-        if not heads[kind]:
-            continue
+    for kind in kinds:
         for si, nm in enumerate(names):
             if kind != "vs" and nm in ("estimate", "topk"):
                 continue
@@ -453,20 +468,21 @@ def main():
             stage_ms[f"{kind}_{nm}"] = sum(vals) / len(vals)
 
     # ---- roofline of the dominant kernel: the first head kind present of
-    # vertical-slash, block-sparse, streaming (the block-sparse heads run the
-    # one-tile kernel, the others the two-tile kernel)
+    # vertical-slash, block-sparse, hierarchical, streaming (block-sparse and
+    # hierarchical heads run the one-tile kernel, the others the two-tile kernel)
     peaks = {}
     try:
         peaks = _json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
         peak, peak_src = float(peaks["bf16_tflops_sustained"]), "measured (sustained)"
     except (OSError, KeyError, ValueError):
         peak, peak_src = 1700.0, "fallback (sustained)"
-    dom = "vs" if heads["vs"] else ("bs" if heads["bs"] else "st")
+    dom = next(kind for kind in ("vs", "bs", "hip", "st") if heads[kind])
     dom_ms = stage_ms[f"{dom}_prefill"]
     achieved = flops[dom] / (dom_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": measured_traffic(args.workload, dom),
-                "kernel": "sparse_prefill_tile_kernel" if dom == "bs" else "sparse_prefill_kernel",
+                "kernel": ("sparse_prefill_tile_kernel" if dom in ("bs", "hip")
+                           else "sparse_prefill_kernel"),
                 "peak_source": peak_src,
                 "frac_of_burst": achieved / float(peaks.get("bf16_tflops", 1900.0))}
 
@@ -531,7 +547,7 @@ def main():
     if not args.no_kv_select and rank == 0:
         kvb = msa.kv_select_buffers(q, KV_WINDOW, KV_KEEP)
         step(kv=kvb)  # warm-up
-        ev = {kind: new_events() for kind in ("vs", "bs", "st") if heads[kind]}
+        ev = {kind: new_events() for kind in kinds}
         torch.cuda.synchronize()
         step(events=ev, kv=kvb)
         torch.cuda.synchronize()
@@ -586,6 +602,7 @@ def main():
                        "vertical_topk": w.vertical_topk, "slash": w.slash, "last_q": w.last_q,
                        "block_topk": w.block_topk, "init_num": w.init_num,
                        "local_window_num": w.local_window_num,
+                       "hip_stages": [list(x) for x in w.hip_stages],
                        "l2": l2_note(q, k)},
             "roofline": roofline,
             "cpu_baseline": cpu,

@@ -11,6 +11,9 @@ Workload recipes (one per named workload, all causal, d = 128):
 * ``mixed_128k``  batch 1, 32/8 heads, N = 131072, both plantings, seeded split of the
                   heads into 20 vertical-slash, 8 block-sparse and 4 streaming heads.
 * ``vs_1m``       batch 1, 32/8 heads, N = 1048576, vertical-slash planting.
+* ``hip_64k``     batch 1, 32/8 heads, N = 65536, block-local planting, every head
+                  a hierarchical pruning head (chunks of 16, 4 and 1 blocks keeping
+                  16, 40 and 100: 1024 candidate blocks -> 256 -> 160 -> 100).
 
 Generation steps, in this order (all in fp32, one bf16 cast at the end):
 
@@ -53,6 +56,10 @@ class Workload:
     local_window_num: int = 0
     # number of heads of each type (vertical-slash, block-sparse, streaming)
     head_split: tuple = (0, 0, 0)
+    # hierarchical pruning heads (all heads when set) and their stages
+    # ((chunk_blocks, keep), ...)
+    hip_heads: int = 0
+    hip_stages: tuple = ()
     extra: dict = field(default_factory=dict)
 
 
@@ -68,20 +75,26 @@ WORKLOADS = {
                            init_num=1, local_window_num=64, head_split=(20, 8, 4)),
     "vs_1m": Workload("vs_1m", 1, 32, 8, 1048576, 1004, True, False,
                       vertical_topk=1000, slash=6096, head_split=(32, 0, 0)),
+    "hip_64k": Workload("hip_64k", 1, 32, 8, 65536, 1005, False, True,
+                        hip_heads=32, hip_stages=((16, 16), (4, 40), (1, 100))),
 }
 
 
 def head_assignment(w: Workload) -> dict:
     """Seeded split of the query heads into the three head types.
 
-    Returns {"vs": [...], "bs": [...], "st": [...]} with ascending head ids.
+    Returns {"vs": [...], "bs": [...], "st": [...], "hip": [...]} with
+    ascending head ids.
     """
+    if w.hip_heads:
+        assert w.hip_heads == w.n_q_heads
+        return {"vs": [], "bs": [], "st": [], "hip": list(range(w.n_q_heads))}
     n_vs, n_bs, n_st = w.head_split
     assert n_vs + n_bs + n_st == w.n_q_heads
     if n_bs == 0 and n_st == 0:
-        return {"vs": list(range(w.n_q_heads)), "bs": [], "st": []}
+        return {"vs": list(range(w.n_q_heads)), "bs": [], "st": [], "hip": []}
     if n_vs == 0 and n_st == 0:
-        return {"vs": [], "bs": list(range(w.n_q_heads)), "st": []}
+        return {"vs": [], "bs": list(range(w.n_q_heads)), "st": [], "hip": []}
     g = torch.Generator(device="cpu")
     g.manual_seed(w.seed * 7919 + 17)
     perm = torch.randperm(w.n_q_heads, generator=g).tolist()
@@ -89,6 +102,7 @@ def head_assignment(w: Workload) -> dict:
         "vs": sorted(perm[:n_vs]),
         "bs": sorted(perm[n_vs:n_vs + n_bs]),
         "st": sorted(perm[n_vs + n_bs:]),
+        "hip": [],
     }
 
 
