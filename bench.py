@@ -491,27 +491,40 @@ def main():
     # and outputs double-buffered, copies on two side streams while steps compute)
     e2e = None
     if args.e2e_steps > 0:
-        from dynamic_sparse_attention_slash_gb300.pipeline import run_pipelined
+        from dynamic_sparse_attention_slash_gb300 import pipeline as pl
         S = args.e2e_steps
+        # pinned buffers in the memory of the GPU's own NUMA node (the CPU
+        # affinity is restored after the measurement)
+        affinity = os.sched_getaffinity(0)
+        numa = pl.bind_to_gpu_node(dev)
         qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
         oh = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
+        numa["q_pages_per_node"] = pl.buffer_numa_pages(qh)
+        numa["out_pages_per_node"] = pl.buffer_numa_pages(oh[0])
         barrier(world)
         torch.cuda.synchronize()
-        evs = run_pipelined(lambda qq, kk, vv, oo: step(qq=qq, kk=kk, vv=vv, oo=oo),
+        evs = pl.run_pipelined(lambda qq, kk, vv, oo: step(qq=qq, kk=kk, vv=vv, oo=oo),
                             [(qh, kh, vh)] * S, [oh[i % 2] for i in range(S)], stream=stream,
                             device=dev)
         torch.cuda.synchronize()
         barrier(world)
         e_ms = max_over_ranks(evs["start"].elapsed_time(evs["end"]), world)
         compute_ms = sum(a_.elapsed_time(b_) for a_, b_ in evs["compute"]) / S
+        h2d_ms = sum(a_.elapsed_time(b_) for a_, b_ in evs["h2d"]) / S
+        d2h_ms = sum(a_.elapsed_time(b_) for a_, b_ in evs["d2h"]) / S
         e_val = sum_over_ranks(step_flops * S, world) / (e_ms * 1e-3) / 1e12
         h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+        d2h = oh[0].numel() * oh[0].element_size()
         e2e = {"value": e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": oh[0].numel() * oh[0].element_size(),
+               "d2h_bytes_per_step": d2h,
                "ms_per_step": e_ms / S, "compute_ms_per_step": compute_ms, "steps": S,
+               "h2d_ms_per_step": h2d_ms, "d2h_ms_per_step": d2h_ms,
+               "h2d_gbps": h2d / (h2d_ms * 1e6), "d2h_gbps": d2h / (d2h_ms * 1e6),
+               "numa": numa,
                "pipelined": "pipeline.run_pipelined: double-buffered inputs/outputs, "
                             "copies on two side streams"}
         del qh, kh, vh, oh, evs
+        os.sched_setaffinity(0, affinity)
 
     # ---- dense causal attention on the same GPU (context)
     dense = None

@@ -317,6 +317,7 @@ struct TileArgs {
   const int32_t* block_ids;
   int32_t* tiles;       // [units][NQ][tile_cap][2]: key-block slots, blk | flags << 16
   int32_t* tile_count;  // [units][NQ]
+  uint32_t* status;
 };
 
 // One warp per (unit, 128-row query tile p): the union U of the blocks kept by
@@ -341,11 +342,11 @@ __global__ void __launch_bounds__(32 * kTilesWarps) bs_tiles_kernel(TileArgs a) 
   __syncwarp();
   for (int t = 0; t < 2 && 2 * p + t < a.NB; ++t) {
     const int64_t rb = static_cast<int64_t>(unit) * a.NB + 2 * p + t;
-    const int cnt = a.block_count[rb];
+    const int cnt = MSA_COUNT(a.block_count[rb], a.kb, a.status);
     const int32_t* L = a.block_ids + rb * a.kb;
     uint32_t* w = t ? w1 : w0;
     for (int i = lane; i < cnt; i += 32) {
-      const int blk = L[i];
+      const int blk = MSA_IDX(L[i], 0, nblk, a.status);
       atomicOr(&w[blk >> 5], 1u << (blk & 31));
     }
   }
@@ -368,7 +369,8 @@ __global__ void __launch_bounds__(32 * kTilesWarps) bs_tiles_kernel(TileArgs a) 
       const int bit = __ffs(u) - 1;
       u &= u - 1;
       const int flags = static_cast<int>(((b0 >> bit) & 1u) | (((b1 >> bit) & 1u) << 1));
-      out[r++] = (32 * i + bit) | (flags << 16);
+      out[MSA_IDX(r, 0, 2 * a.tile_cap, a.status)] = (32 * i + bit) | (flags << 16);
+      ++r;
     }
     const int total = __shfl_sync(0xffffffffu, incl, 31);
     if (total > 0) {  // the highest lane with a block holds the largest so far
@@ -380,7 +382,8 @@ __global__ void __launch_bounds__(32 * kTilesWarps) bs_tiles_kernel(TileArgs a) 
     n += total;
   }
   if (lane == 0) {
-    if (n & 1) out[n] = last;  // second half of the last item: the same block, no flags
+    if (n & 1) out[MSA_IDX(n, 0, 2 * a.tile_cap, a.status)] = last;  // second half of the last
+                                                                    // item: same block, no flags
     a.tile_count[gid] = (n + 1) >> 1;
   }
 }
@@ -407,7 +410,7 @@ cudaError_t launch_pool_q(const Geometry& g, const UnitMap& u, TensorView q, flo
 
 cudaError_t launch_bs_tiles(const Geometry& g, int kb, const int32_t* block_count,
                             const int32_t* block_ids, int32_t* tiles, int32_t* tile_count,
-                            int tile_cap, cudaStream_t st, int* n_launch) {
+                            int tile_cap, uint32_t* status, cudaStream_t st, int* n_launch) {
   TileArgs ta;
   ta.NB = g.NB;
   ta.NQ = g.NQ;
@@ -418,6 +421,7 @@ cudaError_t launch_bs_tiles(const Geometry& g, int kb, const int32_t* block_coun
   ta.block_ids = block_ids;
   ta.tiles = tiles;
   ta.tile_count = tile_count;
+  ta.status = status;
   ta.words_per_warp = 2 * ((g.NB + 31) >> 5);
   const int tsmem = kTilesWarps * ta.words_per_warp * 4;
   cudaError_t e;
@@ -436,7 +440,7 @@ cudaError_t launch_bs_tiles(const Geometry& g, int kb, const int32_t* block_coun
 cudaError_t launch_bs_index(const Geometry& g, const UnitMap& u, TensorView q, TensorView k,
                             int topk, float* qpool, float* kpool, int32_t* block_count,
                             int32_t* block_ids, int32_t* tiles, int32_t* tile_count,
-                            int tile_cap, cudaStream_t st, int* n_launch) {
+                            int tile_cap, uint32_t* status, cudaStream_t st, int* n_launch) {
   cudaError_t e = launch_pool_q(g, u, q, qpool, st, n_launch);
   if (e != cudaSuccess) return e;
   PoolArgs pa;
@@ -485,8 +489,8 @@ cudaError_t launch_bs_index(const Geometry& g, const UnitMap& u, TensorView q, T
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   ++*n_launch;
-  return launch_bs_tiles(g, sa.kb, block_count, block_ids, tiles, tile_count, tile_cap, st,
-                         n_launch);
+  return launch_bs_tiles(g, sa.kb, block_count, block_ids, tiles, tile_count, tile_cap, status,
+                         st, n_launch);
 }
 
 }  // namespace msa

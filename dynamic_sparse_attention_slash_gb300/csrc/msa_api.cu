@@ -150,9 +150,18 @@ constexpr size_t kStatusBytes = 256;
 
 struct VSLayout {
   int kv, ks, kv_pad, n_split, dist_words, chunk_words;
-  size_t partial, v_score, s_score, vertical, slash, tile_dist, qdelta, qdelta_count, col_chunks,
+  size_t vmax, partial, v_score, s_score, vertical, slash, tile_dist, qdelta, qdelta_count, col_chunks,
       kc, vc, v16, total;
 };
+
+// Largest |v| per (batch, KV head), right after the status word; both are
+// cleared by one memset at the start of every call.
+size_t vmax_count(const Geometry& g) { return static_cast<size_t>(g.B) * g.Hkv; }
+
+template <typename L>
+size_t cleared_bytes(const L& layout, const Geometry& g) {
+  return layout.vmax + vmax_count(g) * sizeof(uint32_t);
+}
 
 // f16 copy of v for the P.V product: [B][Hkv][N][128], contiguous.
 size_t v16_elems(const Geometry& g) {
@@ -177,6 +186,7 @@ VSLayout vs_layout(const Geometry& g, int64_t vertical_topk, int64_t slash) {
   const size_t U = static_cast<size_t>(g.n_units);
   Carver c;
   c.off = kStatusBytes;
+  L.vmax = c.take<uint32_t>(vmax_count(g));
   L.partial = c.take<float>(U * L.n_split * 128);
   L.v_score = c.take<float>(U * g.N);
   L.s_score = c.take<float>(U * g.N);
@@ -195,7 +205,7 @@ VSLayout vs_layout(const Geometry& g, int64_t vertical_topk, int64_t slash) {
 
 struct BSLayout {
   int kb, tile_cap;
-  size_t qpool, kpool, block_count, block_ids, tiles, tile_count, v16, total;
+  size_t vmax, qpool, kpool, block_count, block_ids, tiles, tile_count, v16, total;
 };
 
 BSLayout bs_layout(const Geometry& g, int64_t topk) {
@@ -205,6 +215,7 @@ BSLayout bs_layout(const Geometry& g, int64_t topk) {
   const size_t U = static_cast<size_t>(g.n_units);
   Carver c;
   c.off = kStatusBytes;
+  L.vmax = c.take<uint32_t>(vmax_count(g));
   L.qpool = c.take<float>(U * g.NB * kHeadDim);
   L.kpool = c.take<float>(static_cast<size_t>(g.B) * g.Hkv * g.NB * kHeadDim);
   L.block_count = c.take<int32_t>(U * g.NB);
@@ -220,7 +231,7 @@ BSLayout bs_layout(const Geometry& g, int64_t topk) {
 // query blocks, the kept blocks (block-sparse format) and their item lists.
 struct HIPLayout {
   int kb, tile_cap, slab;
-  size_t qpool, rmax, block_count, block_ids, tiles, tile_count, v16, total;
+  size_t vmax, qpool, rmax, block_count, block_ids, tiles, tile_count, v16, total;
 };
 
 HIPLayout hip_layout(const Geometry& g, int64_t keep_last) {
@@ -231,6 +242,7 @@ HIPLayout hip_layout(const Geometry& g, int64_t keep_last) {
   const size_t U = static_cast<size_t>(g.n_units);
   Carver c;
   c.off = kStatusBytes;
+  L.vmax = c.take<uint32_t>(vmax_count(g));
   L.qpool = c.take<float>(U * g.NB * kHeadDim);
   L.rmax = c.take<float>(U * L.slab * g.NB);
   L.block_count = c.take<int32_t>(U * g.NB);
@@ -258,13 +270,14 @@ int check_hip_stages(const msa_hip_stage* stages, int32_t n, int NB, int32_t* c,
 }
 
 struct STLayout {
-  size_t v16, total;
+  size_t vmax, v16, total;
 };
 
 STLayout st_layout(const Geometry& g) {
   STLayout L;
   Carver c;
   c.off = kStatusBytes;
+  L.vmax = c.take<uint32_t>(vmax_count(g));
   L.v16 = c.take<__half>(v16_elems(g));
   L.total = (c.off + 255) & ~size_t{255};
   return L;
@@ -354,7 +367,8 @@ int finish(cudaError_t e, int launches) {
   return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
-PrefillParams base_prefill(const Call& c, msa_tensor* out, uint32_t* status) {
+PrefillParams base_prefill(const Call& c, msa_tensor* out, uint32_t* status,
+                           const uint32_t* vmax) {
   PrefillParams p;
   std::memset(&p, 0, sizeof(p));
   p.lse = (c.opts && c.opts->kv_select) ? c.opts->kv_select->lse : nullptr;
@@ -366,6 +380,7 @@ PrefillParams base_prefill(const Call& c, msa_tensor* out, uint32_t* status) {
   p.out_sh = out->sh;
   p.out_sn = out->sn;
   p.status = status;
+  p.vmax = vmax;
   p.units = c.u;
   return p;
 }
@@ -473,7 +488,7 @@ int msa_vertical_slash(const msa_tensor* q, const msa_tensor* k, const msa_tenso
     return s;
   const StageTimer tm{opts->stage_events, c.st};
   int launches = 0;
-  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), c.st);
+  cudaError_t e = cudaMemsetAsync(ws, 0, cleared_bytes(L, c.g), c.st);
   if (e != cudaSuccess) return finish(e, launches);
   tm.begin(MSA_STAGE_ESTIMATE);
   e = launch_vs_estimate(c.g, c.u, view(q), view(k), c.last_q, at<float>(ws, L.partial), L.n_split,
@@ -490,17 +505,19 @@ int msa_vertical_slash(const msa_tensor* q, const msa_tensor* k, const msa_tenso
   tm.end(MSA_STAGE_TOPK);
   if (e != cudaSuccess) return finish(e, launches);
   tm.begin(MSA_STAGE_INDEX);
-  e = launch_vs_index(c.g, c.u, view(k), view(v), at<int32_t>(ws, L.slash), L.ks,
-                      at<int32_t>(ws, L.vertical), L.kv, at<uint32_t>(ws, L.tile_dist),
-                      L.dist_words, at<int32_t>(ws, L.qdelta), at<int32_t>(ws, L.qdelta_count),
-                      at<uint32_t>(ws, L.col_chunks), L.chunk_words, at<__nv_bfloat16>(ws, L.kc),
-                      at<__half>(ws, L.vc), L.kv_pad, at<uint32_t>(ws, 0), c.st, &launches);
+  // the f16 copy of v first: the format's gathered column rows copy from it
+  e = launch_v_to_f16(view(v), c.g, c.u, at<__half>(ws, L.v16), at<uint32_t>(ws, L.vmax), c.st,
+                      &launches);
   if (e == cudaSuccess)
-    e = launch_v_to_f16(view(v), c.g, c.u, at<__half>(ws, L.v16), at<uint32_t>(ws, 0),
-                        c.st, &launches);
+    e = launch_vs_index(c.g, c.u, view(k), at<__half>(ws, L.v16), at<int32_t>(ws, L.slash), L.ks,
+                        at<int32_t>(ws, L.vertical), L.kv, at<uint32_t>(ws, L.tile_dist),
+                        L.dist_words, at<int32_t>(ws, L.qdelta), at<int32_t>(ws, L.qdelta_count),
+                        at<uint32_t>(ws, L.col_chunks), L.chunk_words,
+                        at<__nv_bfloat16>(ws, L.kc), at<__half>(ws, L.vc), L.kv_pad,
+                        at<uint32_t>(ws, 0), c.st, &launches);
   tm.end(MSA_STAGE_INDEX);
   if (e != cudaSuccess) return finish(e, launches);
-  PrefillParams p = base_prefill(c, out, at<uint32_t>(ws, 0));
+  PrefillParams p = base_prefill(c, out, at<uint32_t>(ws, 0), at<uint32_t>(ws, L.vmax));
   p.kind = kPrefillVS;
   p.tile_dist = at<uint32_t>(ws, L.tile_dist);
   p.dist_words = L.dist_words;
@@ -538,7 +555,7 @@ int msa_vertical_slash(const msa_tensor* q, const msa_tensor* k, const msa_tenso
     cp(x->col_chunks, L.col_chunks, U * c.g.NQ * L.chunk_words * sizeof(uint32_t));
     if (x->col_count && e == cudaSuccess)
       e = launch_vs_col_count(c.g, at<int32_t>(ws, L.vertical), L.kv, at<uint32_t>(ws, L.tile_dist),
-                              L.dist_words, x->col_count, c.st, &launches);
+                              L.dist_words, x->col_count, at<uint32_t>(ws, 0), c.st, &launches);
   }
   return finish(e, launches);
 }
@@ -562,19 +579,20 @@ int msa_block_sparse(const msa_tensor* q, const msa_tensor* k, const msa_tensor*
     return s;
   const StageTimer tm{opts->stage_events, c.st};
   int launches = 0;
-  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), c.st);
+  cudaError_t e = cudaMemsetAsync(ws, 0, cleared_bytes(L, c.g), c.st);
   if (e != cudaSuccess) return finish(e, launches);
   tm.begin(MSA_STAGE_INDEX);
-  e = launch_v_to_f16(view(v), c.g, c.u, at<__half>(ws, L.v16), at<uint32_t>(ws, 0),
+  e = launch_v_to_f16(view(v), c.g, c.u, at<__half>(ws, L.v16), at<uint32_t>(ws, L.vmax),
                       c.st, &launches);
   if (e != cudaSuccess) return finish(e, launches);
   e = launch_bs_index(c.g, c.u, view(q), view(k), static_cast<int>(L.kb < topk ? L.kb : topk),
                       at<float>(ws, L.qpool), at<float>(ws, L.kpool), at<int32_t>(ws, L.block_count),
                       at<int32_t>(ws, L.block_ids), at<int32_t>(ws, L.tiles),
-                      at<int32_t>(ws, L.tile_count), L.tile_cap, c.st, &launches);
+                      at<int32_t>(ws, L.tile_count), L.tile_cap, at<uint32_t>(ws, 0), c.st,
+                      &launches);
   tm.end(MSA_STAGE_INDEX);
   if (e != cudaSuccess) return finish(e, launches);
-  PrefillParams p = base_prefill(c, out, at<uint32_t>(ws, 0));
+  PrefillParams p = base_prefill(c, out, at<uint32_t>(ws, 0), at<uint32_t>(ws, L.vmax));
   p.kind = kPrefillBS;
   p.bs_tiles = at<int32_t>(ws, L.tiles);
   p.bs_tile_count = at<int32_t>(ws, L.tile_count);
@@ -623,10 +641,10 @@ int msa_hierarchical(const msa_tensor* q, const msa_tensor* k, const msa_tensor*
     return s;
   const StageTimer tm{opts->stage_events, c.st};
   int launches = 0;
-  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), c.st);
+  cudaError_t e = cudaMemsetAsync(ws, 0, cleared_bytes(L, c.g), c.st);
   if (e != cudaSuccess) return finish(e, launches);
   tm.begin(MSA_STAGE_INDEX);
-  e = launch_v_to_f16(view(v), c.g, c.u, at<__half>(ws, L.v16), at<uint32_t>(ws, 0), c.st,
+  e = launch_v_to_f16(view(v), c.g, c.u, at<__half>(ws, L.v16), at<uint32_t>(ws, L.vmax), c.st,
                       &launches);
   if (e == cudaSuccess) e = launch_pool_q(c.g, c.u, view(q), at<float>(ws, L.qpool), c.st, &launches);
   if (e == cudaSuccess)
@@ -635,11 +653,11 @@ int msa_hierarchical(const msa_tensor* q, const msa_tensor* k, const msa_tensor*
                          at<int32_t>(ws, L.block_ids), L.kb, c.st, &launches);
   if (e == cudaSuccess)
     e = launch_bs_tiles(c.g, L.kb, at<int32_t>(ws, L.block_count), at<int32_t>(ws, L.block_ids),
-                        at<int32_t>(ws, L.tiles), at<int32_t>(ws, L.tile_count), L.tile_cap, c.st,
-                        &launches);
+                        at<int32_t>(ws, L.tiles), at<int32_t>(ws, L.tile_count), L.tile_cap,
+                        at<uint32_t>(ws, 0), c.st, &launches);
   tm.end(MSA_STAGE_INDEX);
   if (e != cudaSuccess) return finish(e, launches);
-  PrefillParams p = base_prefill(c, out, at<uint32_t>(ws, 0));
+  PrefillParams p = base_prefill(c, out, at<uint32_t>(ws, 0), at<uint32_t>(ws, L.vmax));
   p.kind = kPrefillBS;  // same per-query-tile item lists as the block-sparse head
   p.bs_tiles = at<int32_t>(ws, L.tiles);
   p.bs_tile_count = at<int32_t>(ws, L.tile_count);
@@ -684,14 +702,14 @@ int msa_streaming(const msa_tensor* q, const msa_tensor* k, const msa_tensor* v,
     return s;
   const StageTimer tm{opts->stage_events, c.st};
   int launches = 0;
-  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), c.st);
+  cudaError_t e = cudaMemsetAsync(ws, 0, cleared_bytes(L, c.g), c.st);
   if (e != cudaSuccess) return finish(e, launches);
   tm.begin(MSA_STAGE_INDEX);
-  e = launch_v_to_f16(view(v), c.g, c.u, at<__half>(ws, L.v16), at<uint32_t>(ws, 0),
+  e = launch_v_to_f16(view(v), c.g, c.u, at<__half>(ws, L.v16), at<uint32_t>(ws, L.vmax),
                       c.st, &launches);
   tm.end(MSA_STAGE_INDEX);
   if (e != cudaSuccess) return finish(e, launches);
-  PrefillParams p = base_prefill(c, out, at<uint32_t>(ws, 0));
+  PrefillParams p = base_prefill(c, out, at<uint32_t>(ws, 0), at<uint32_t>(ws, L.vmax));
   p.kind = kPrefillST;
   const int64_t nb = c.g.NB;
   p.init_num = static_cast<int>(init_num < nb ? init_num : nb);
@@ -717,7 +735,7 @@ int msa_device_status(void* workspace, void* stream) {
   if (cudaStreamSynchronize(st) != cudaSuccess) return MSA_ERR_CUDA;
   if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), st) != cudaSuccess) return MSA_ERR_CUDA;
   if (h & kStatusTimeout) return MSA_ERR_TIMEOUT;
-  if (h & kStatusRange) return MSA_ERR_RANGE;
+  if (h & kStatusBounds) return MSA_ERR_BOUNDS;
   return MSA_OK;
 }
 
@@ -729,7 +747,7 @@ const char* msa_status_string(int status) {
     case MSA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case MSA_ERR_CUDA: return "CUDA error";
     case MSA_ERR_TIMEOUT: return "device-side wait timed out";
-    case MSA_ERR_RANGE: return "a value of v lies outside the f16 range of the P.V product";
+    case MSA_ERR_BOUNDS: return "a kernel read an index out of range (bounds-checking build)";
     default: return "unknown status";
   }
 }

@@ -20,7 +20,40 @@ constexpr int kMaxUnits = 65535;
 
 // Device status word bits (first word of every workspace).
 constexpr uint32_t kStatusTimeout = 1u;
-constexpr uint32_t kStatusRange = 2u;  // a value of v outside the f16 range
+constexpr uint32_t kStatusBounds = 2u;  // bounds-checking build: an index read was out of range
+
+// Bounds checks of the indices the kernels read from index data (the
+// bounds-checking build, compiled with MSA_CHECKED).  An index outside
+// [lo, hi) sets kStatusBounds in the status word and is replaced by lo, so the
+// access stays inside its buffer (the result is then wrong, and the status
+// says so); there is no trap.  A count above cap is reported and cut to cap.
+// In the ordinary build both are the plain value.
+#ifdef MSA_CHECKED
+__device__ __forceinline__ int checked_index(int i, int lo, int hi, uint32_t* status) {
+  if (i >= lo && i < hi) return i;
+  if (status) atomicOr(status, kStatusBounds);
+  return lo;
+}
+__device__ __forceinline__ int checked_count(int c, int cap, uint32_t* status) {
+  if (c >= 0 && c <= cap) return c;
+  if (status) atomicOr(status, kStatusBounds);
+  return c < 0 ? 0 : cap;
+}
+#define MSA_IDX(i, lo, hi, status) ::msa::checked_index((i), (lo), (hi), (status))
+#define MSA_COUNT(c, cap, status) ::msa::checked_count((c), (cap), (status))
+#else
+#define MSA_IDX(i, lo, hi, status) (i)
+#define MSA_COUNT(c, cap, status) (c)
+#endif
+
+// Exponent e >= 0 of the power-of-two scale 2^-e that brings a KV head's
+// largest |v| (amax) into the f16 range of the P.V product: 0 when amax <=
+// 65504, else the smallest e with amax * 2^-e <= 65504 (ldexpf is exact).
+__host__ __device__ inline int v_scale_exp(float amax) {
+  int e = 0;
+  while (e < 200 && ldexpf(amax, -e) > 65504.f) ++e;
+  return e;
+}
 
 // A selected (batch, query head) pair and the KV head it reads.
 struct UnitMap {
@@ -86,6 +119,9 @@ struct PrefillParams {
   int init_num, local_num;
   // row normalisers lse_i (natural log) for KV selection: [B][Hq][N] f32, or null
   float* lse;
+  // largest |v| per (batch, KV head) as float bits: the output of a head copied
+  // with the scale 2^-e (v_scale_exp) is multiplied by 2^e
+  const uint32_t* vmax;
   uint32_t* status;
   UnitMap units;
 };
@@ -140,7 +176,9 @@ cudaError_t launch_topk_units(const float* scores, int64_t n, int k, int Hq, con
 cudaError_t launch_kv_score(const Geometry& g, const UnitMap& u, TensorView q, TensorView k,
                             const float* lse, float* score, int window, const KvMask& mask,
                             cudaStream_t st, int* n_launch);
-cudaError_t launch_vs_index(const Geometry& g, const UnitMap& u, TensorView k, TensorView v,
+// The vertical-slash format; the gathered V rows of the columns are copied
+// from the f16 copy of v (v16, [B][Hkv][N][128], already scaled).
+cudaError_t launch_vs_index(const Geometry& g, const UnitMap& u, TensorView k, const __half* v16,
                             const int32_t* slash, int ks, const int32_t* vertical, int kv,
                             uint32_t* tile_dist, int dist_words, int32_t* qdelta,
                             int32_t* qdelta_count, uint32_t* col_chunks, int chunk_words,
@@ -149,11 +187,11 @@ cudaError_t launch_vs_index(const Geometry& g, const UnitMap& u, TensorView k, T
 // Export only: columns per row block of the vertical-slash format ([units][NB]).
 cudaError_t launch_vs_col_count(const Geometry& g, const int32_t* vertical, int kv,
                                 const uint32_t* tile_dist, int dist_words, int32_t* col_count,
-                                cudaStream_t st, int* n_launch);
+                                uint32_t* status, cudaStream_t st, int* n_launch);
 cudaError_t launch_bs_index(const Geometry& g, const UnitMap& u, TensorView q, TensorView k,
                             int topk, float* qpool, float* kpool, int32_t* block_count,
                             int32_t* block_ids, int32_t* tiles, int32_t* tile_count,
-                            int tile_cap, cudaStream_t st, int* n_launch);
+                            int tile_cap, uint32_t* status, cudaStream_t st, int* n_launch);
 // Mean of each 64-row block of q for the selected units ([units][NB][128] f32).
 cudaError_t launch_pool_q(const Geometry& g, const UnitMap& u, TensorView q, float* qpool,
                           cudaStream_t st, int* n_launch);
@@ -161,7 +199,7 @@ cudaError_t launch_pool_q(const Geometry& g, const UnitMap& u, TensorView q, flo
 // block ([units][NB] counts, [units][NB][kb] ascending ids).
 cudaError_t launch_bs_tiles(const Geometry& g, int kb, const int32_t* block_count,
                             const int32_t* block_ids, int32_t* tiles, int32_t* tile_count,
-                            int tile_cap, cudaStream_t st, int* n_launch);
+                            int tile_cap, uint32_t* status, cudaStream_t st, int* n_launch);
 // Hierarchical pruning head: block maxima of the token scores and the stages,
 // slab by slab of slab_rows query blocks; writes kept blocks in the
 // block-sparse format.  hip_slab_rows gives the slab height for a call.
@@ -170,8 +208,11 @@ cudaError_t launch_hip_index(const Geometry& g, const UnitMap& u, TensorView k, 
                              const int32_t* stage_c, const int32_t* stage_keep, int n_stages,
                              float* rmax, int slab_rows, int32_t* block_count, int32_t* block_ids,
                              int kb, cudaStream_t st, int* n_launch);
+// The f16 copy of v for the KV heads the call reads, with each head's largest
+// |v| in vmax ([B][Hkv] float bits, zeroed before the call) and heads beyond
+// the f16 range scaled by 2^-v_scale_exp(vmax).
 cudaError_t launch_v_to_f16(TensorView v, const Geometry& g, const UnitMap& u, __half* dst,
-                            uint32_t* status, cudaStream_t st, int* n_launch);
+                            uint32_t* vmax, cudaStream_t st, int* n_launch);
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                            const CUtensorMap& mv, const CUtensorMap& mkc, const CUtensorMap& mvc,
                            cudaStream_t st, int* n_launch);

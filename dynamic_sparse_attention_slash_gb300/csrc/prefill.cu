@@ -125,7 +125,7 @@ __device__ __forceinline__ void st_ranges(const PrefillParams& P, int pA, int& s
 // list; the smallest (distance 0, key tile pB) is dropped when pB is past the
 // sequence.  Item t maps to distance list[n_hi - 1 - t].
 __device__ __forceinline__ int vs_n_tiles(const PrefillParams& P, int unit, int pA, int n_hi) {
-  const int32_t* qd = P.qdelta + static_cast<int64_t>(unit) * (P.g.NQ + 1);
+  const int32_t* qd = P.qdelta + static_cast<int64_t>(unit) * (P.g.NQ + 1);  // n_hi <= NQ + 1
   const bool drop = pA + 1 > P.g.NQ - 1 && n_hi > 0 && (qd[0] >> 5) == 0;
   return n_hi - (drop ? 1 : 0);
 }
@@ -152,20 +152,29 @@ __device__ __forceinline__ Item get_item(const PrefillParams& P, int unit, int c
     if (i < n_chunks) {
       int seen = 0;
       for (int x = 0;; ++x) {
+#ifdef MSA_CHECKED
+        if (x >= P.chunk_words) {  // fewer chunks than items: report, take chunk 0
+          MSA_IDX(x, 0, P.chunk_words, P.status);
+          it.cols = true;
+          it.idx = 0;
+          return it;
+        }
+#endif
         uint32_t word = vs_chunk_word(P, unit, pA, x);
         const int cnt = __popc(word);
         if (seen + cnt > i) {
           for (int skip = i - seen; skip > 0; --skip) word &= word - 1;
           it.cols = true;
-          it.idx = 32 * x + (__ffs(word) - 1);
+          it.idx = MSA_IDX(32 * x + (__ffs(word) - 1), 0, (P.kv + 127) / 128, P.status);
           return it;
         }
         seen += cnt;
       }
     }
     const int t = i - n_chunks;
-    const int32_t e = P.qdelta[static_cast<int64_t>(unit) * (P.g.NQ + 1) + n_hi - 1 - t];
-    it.idx = pB - (e >> 5);
+    const int32_t e = P.qdelta[static_cast<int64_t>(unit) * (P.g.NQ + 1) +
+                               MSA_IDX(n_hi - 1 - t, 0, P.g.NQ + 1, P.status)];
+    it.idx = MSA_IDX(pB - (e >> 5), 0, P.g.NQ, P.status);
     // quadrant (a, b) of tile pB sits at distance 2D + a - b (bit a - b + 3 of
     // the packed window), of tile pA at 2D - 2 + a - b (bit a - b + 1)
     uint32_t ma = 0, mb = 0;
@@ -184,7 +193,7 @@ __device__ __forceinline__ Item get_item(const PrefillParams& P, int unit, int c
   // streaming
   int sink_hi, loc_lo;
   st_ranges(P, pA, sink_hi, loc_lo);
-  it.idx = i < sink_hi ? i : loc_lo + (i - sink_hi);
+  it.idx = MSA_IDX(i < sink_hi ? i : loc_lo + (i - sink_hi), 0, P.g.NQ, P.status);
   it.qmask[0] = quad_mask_st(P, pA, it.idx);
   it.qmask[1] = quad_mask_st(P, pB, it.idx);
   return it;
@@ -407,8 +416,8 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
           for (int e = 0; e < 128; ++e) {
             bool keep = false;
             if (e < valid) {
-              const int j = V[e];
-              keep = j <= row && !dist_bit(dist, mblk - (j >> 6));
+              const int j = MSA_IDX(V[e], 0, P.g.N, P.status);
+              keep = j <= row && !dist_bit_checked(P, dist, mblk - (j >> 6));
             }
             if (!keep) x[e] = -INFINITY;
           }
@@ -519,7 +528,10 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
       tc_fence_after();
     }
     if (ok && k > 0) {
-      const float inv = have ? 1.f / l_run : 0.f;
+      // 1 / l, times 2^e for a KV head whose f16 copy of v was scaled by 2^-e
+      float inv = have ? 1.f / l_run : 0.f;
+      if (P.vmax)
+        inv = ldexpf(inv, v_scale_exp(__uint_as_float(P.vmax[b * P.g.Hkv + hkv])));
       uint32_t o[128];
       tmem_ld128(o_col, o);
 #pragma unroll

@@ -21,10 +21,15 @@ __device__ __forceinline__ bool dist_bit(const uint32_t* dist, int t) {
   return t >= 0 && ((dist[t >> 5] >> (t & 31)) & 1u);
 }
 
+// dist_bit with the bit index checked against the bitset's dist_words words.
+__device__ __forceinline__ bool dist_bit_checked(const PrefillParams& P, const uint32_t* dist, int t) {
+  return t >= 0 && dist_bit(dist, MSA_IDX(t, 0, 32 * P.dist_words, P.status));
+}
+
 // Number of pair distances <= pB (the vertical-slash pair list is ascending).
 __device__ __forceinline__ int vs_tiles_upto(const PrefillParams& P, int unit, int pB) {
   const int32_t* qd = P.qdelta + static_cast<int64_t>(unit) * (P.g.NQ + 1);  // (D << 5) | bits
-  int lo = 0, hi = P.qdelta_count[unit];
+  int lo = 0, hi = MSA_COUNT(P.qdelta_count[unit], P.g.NQ + 1, P.status);
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
     if ((qd[mid] >> 5) <= pB) lo = mid + 1; else hi = mid;

@@ -85,17 +85,17 @@ struct Tile {
 __device__ __forceinline__ Tile make_tile(const PrefillParams& P, int unit, int p) {
   const int64_t t = static_cast<int64_t>(unit) * P.g.NQ + p;
   Tile T;
-  T.n = P.bs_tile_count[t];
+  T.n = MSA_COUNT(P.bs_tile_count[t], P.bs_tile_cap, P.status);
   T.list = P.bs_tiles + t * P.bs_tile_cap * 2;
   return T;
 }
 
-__device__ __forceinline__ Item get_item(const Tile& T, int i) {
+__device__ __forceinline__ Item get_item(const PrefillParams& P, const Tile& T, int i) {
   const int32_t s0 = T.list[2 * i], s1 = T.list[2 * i + 1];
   const uint32_t f0 = static_cast<uint32_t>(s0 >> 16) & 3u, f1 = static_cast<uint32_t>(s1 >> 16) & 3u;
   Item it;
-  it.blk[0] = s0 & 0xffff;
-  it.blk[1] = s1 & 0xffff;
+  it.blk[0] = MSA_IDX(s0 & 0xffff, 0, P.g.NB, P.status);
+  it.blk[1] = MSA_IDX(s1 & 0xffff, 0, P.g.NB, P.status);
   it.qm = (f0 & 1u) | ((f1 & 1u) << 1) | ((f0 >> 1) << 2) | ((f1 >> 1) << 3);
   return it;
 }
@@ -166,7 +166,7 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
       for (int i = 0; i < T.n; ++i) {
         const int st = i % kStagesK;
         if (!mbar_wait(&sm.k_empty[st], ((i / kStagesK) & 1) ^ 1, abort)) break;
-        load_item(get_item(T, i), sm.k[st], &mk64, &sm.k_full[st], hkv, b);
+        load_item(get_item(P, T, i), sm.k[st], &mk64, &sm.k_full[st], hkv, b);
         issued = i + 1;
       }
       // drain: the latest load of every stage, and Q, must land before exit
@@ -182,7 +182,7 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
       for (int i = 0; i < T.n; ++i) {
         const int st = i % kStagesV;
         if (!mbar_wait(&sm.v_empty[st], ((i / kStagesV) & 1) ^ 1, abort)) break;
-        load_item(get_item(T, i), sm.v[st], &mv64, &sm.v_full[st], hkv, b);
+        load_item(get_item(P, T, i), sm.v[st], &mv64, &sm.v_full[st], hkv, b);
         issued = i + 1;
       }
       for (int i = max(0, issued - kStagesV); i < issued; ++i)
@@ -263,7 +263,7 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
     bool ok = true;
     int k = 0;  // items processed so far
     for (; k < T.n;) {
-      const Item it = get_item(T, k);
+      const Item it = get_item(P, T, k);
       const uint32_t s_col = lane_base + kColS + 128 * (k & 1);
       // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
       const bool waited = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[k & 1], (k >> 1) & 1, abort));
@@ -400,7 +400,10 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
       tc_fence_after();
     }
     if (ok && k > 0) {
-      const float inv = have ? 1.f / l_row : 0.f;
+      // 1 / l, times 2^e for a KV head whose f16 copy of v was scaled by 2^-e
+      float inv = have ? 1.f / l_row : 0.f;
+      if (P.vmax)
+        inv = ldexpf(inv, v_scale_exp(__uint_as_float(P.vmax[b * P.g.Hkv + hkv])));
       uint32_t o[64];
       tmem_ld64(o_col, o);
 #pragma unroll

@@ -20,7 +20,8 @@
 //    positions [128c, 128c+128) of the ascending vertical list is needed as a
 //    column by row block 2p or 2p+1, i.e. lies at or before the block's last
 //    row and outside the block's active tiles.
-//  * kc / vc: the K and V rows of the chosen vertical keys, gathered into a
+//  * kc / vc: the K rows and the f16 V rows (from the f16 copy of v, so with
+//    the head's scale) of the chosen vertical keys, gathered into a
 //    contiguous per-unit buffer so column chunks load like ordinary tiles.
 #include "block_scan.cuh"
 #include "msa_internal.h"
@@ -31,8 +32,9 @@ namespace {
 constexpr int kTilesThreads = 512;
 
 __global__ void __launch_bounds__(kTilesThreads) vs_tile_dist_kernel(
-    const int32_t* __restrict__ slash, int ks, int NB, int NQ, uint32_t* __restrict__ tile_dist,
-    int dist_words, int32_t* __restrict__ qdelta, int32_t* __restrict__ qdelta_count) {
+    const int32_t* __restrict__ slash, int ks, int N, int NB, int NQ, uint32_t* __restrict__ tile_dist,
+    int dist_words, int32_t* __restrict__ qdelta, int32_t* __restrict__ qdelta_count,
+    uint32_t* status) {
   extern __shared__ uint32_t bits[];
   __shared__ int warp_sums[kTilesThreads / 32 + 1];
   const int unit = blockIdx.x, tid = threadIdx.x;
@@ -40,7 +42,7 @@ __global__ void __launch_bounds__(kTilesThreads) vs_tile_dist_kernel(
   __syncthreads();
   const int32_t* S = slash + static_cast<int64_t>(unit) * ks;
   for (int s = tid; s < ks; s += kTilesThreads) {
-    const int o = S[s];
+    const int o = MSA_IDX(S[s], 0, N, status);  // t + 1 <= NB < 32 * dist_words
     const int t = o >> 6;
     atomicOr(&bits[t >> 5], 1u << (t & 31));
     if (o & 63) atomicOr(&bits[(t + 1) >> 5], 1u << ((t + 1) & 31));
@@ -59,17 +61,17 @@ __global__ void __launch_bounds__(kTilesThreads) vs_tile_dist_kernel(
     const int pos = block_exclusive_scan<kTilesThreads>(act ? 1 : 0, warp_sums, &total);
     uint32_t near = 0;  // tile-distance bits 2d-3 .. 2d+1: all the quadrant masks need
     for (int k = 0; k < 5; ++k) near |= (bit(2 * d - 3 + k) ? 1u : 0u) << k;
-    if (act) qd[written + pos] = (d << 5) | static_cast<int>(near);
+    if (act) qd[MSA_IDX(written + pos, 0, NQ + 1, status)] = (d << 5) | static_cast<int>(near);
     written += total;
   }
   if (tid == 0) qdelta_count[unit] = written;
 }
 
 // One warp per (unit, query tile p, 32-chunk word).
-__global__ void vs_col_chunks_kernel(const int32_t* __restrict__ vertical, int kv, int NB, int NQ,
-                                     const uint32_t* __restrict__ tile_dist, int dist_words,
+__global__ void vs_col_chunks_kernel(const int32_t* __restrict__ vertical, int kv, int N, int NB,
+                                     int NQ, const uint32_t* __restrict__ tile_dist, int dist_words,
                                      uint32_t* __restrict__ col_chunks, int chunk_words,
-                                     int n_units) {
+                                     int n_units, uint32_t* status) {
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t per_unit = static_cast<int64_t>(NQ) * chunk_words;
@@ -86,7 +88,7 @@ __global__ void vs_col_chunks_kernel(const int32_t* __restrict__ vertical, int k
     const int s_end = min(128 * c + 128, kv);
     const int last_row = min(64 * (2 * p + 1) + 63, 64 * NB - 1);
     for (int s = 128 * c; s < s_end && !need; ++s) {
-      const int j = V[s];
+      const int j = MSA_IDX(V[s], 0, N, status);
       if (j > last_row) break;  // ascending: later keys are after the tile too
       for (int a = 0; a < 2; ++a) {
         const int m = 2 * p + a;
@@ -102,11 +104,10 @@ __global__ void vs_col_chunks_kernel(const int32_t* __restrict__ vertical, int k
 
 struct GatherArgs {
   UnitMap u;
-  int G, kv, kv_pad;
+  int G, Hkv, N, kv, kv_pad;
   const __nv_bfloat16* k;
   int64_t k_sb, k_sh, k_sn;
-  const __nv_bfloat16* v;
-  int64_t v_sb, v_sh, v_sn;
+  const __half* v16;  // [B][Hkv][N][128], the (scaled) f16 copy of v
   const int32_t* vertical;
   __nv_bfloat16* kc;
   __half* vc;
@@ -114,7 +115,8 @@ struct GatherArgs {
 };
 
 // One warp per gathered row; rows past kv are zero.  K rows stay bf16; V rows
-// are converted to f16 (exact within the f16 range) for the f16 P.V product.
+// come from the f16 copy of v that the tiles read, so columns and tiles share
+// the head's scale.
 __global__ void vs_gather_kernel(const __grid_constant__ GatherArgs a) {
   const int unit = blockIdx.y;
   const int s = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -123,32 +125,25 @@ __global__ void vs_gather_kernel(const __grid_constant__ GatherArgs a) {
   const int b = unit / a.u.n_heads;
   const int hkv = a.u.heads[unit % a.u.n_heads] / a.G;
   uint2 kx = make_uint2(0u, 0u), vx = make_uint2(0u, 0u);
-  bool bad = false;
   if (s < a.kv) {
-    const int j = a.vertical[static_cast<int64_t>(unit) * a.kv + s];
+    const int j = MSA_IDX(a.vertical[static_cast<int64_t>(unit) * a.kv + s], 0, a.N, a.status);
     kx = reinterpret_cast<const uint2*>(a.k + b * a.k_sb + hkv * a.k_sh + j * a.k_sn)[lane];
-    const uint2 raw = reinterpret_cast<const uint2*>(a.v + b * a.v_sb + hkv * a.v_sh + j * a.v_sn)[lane];
-    const __nv_bfloat162* in = reinterpret_cast<const __nv_bfloat162*>(&raw);
-    const float f0 = __low2float(in[0]), f1 = __high2float(in[0]);
-    const float f2 = __low2float(in[1]), f3 = __high2float(in[1]);
-    bad = fabsf(f0) > 65504.f || fabsf(f1) > 65504.f || fabsf(f2) > 65504.f || fabsf(f3) > 65504.f;
-    __half2 h01 = __floats2half2_rn(f0, f1), h23 = __floats2half2_rn(f2, f3);
-    vx.x = *reinterpret_cast<uint32_t*>(&h01);
-    vx.y = *reinterpret_cast<uint32_t*>(&h23);
+    const int64_t vrow = (static_cast<int64_t>(b) * a.Hkv + hkv) * a.N + j;
+    vx = reinterpret_cast<const uint2*>(a.v16 + vrow * kHeadDim)[lane];
   }
   const int64_t row = static_cast<int64_t>(unit) * a.kv_pad + s;
   reinterpret_cast<uint2*>(a.kc + row * kHeadDim)[lane] = kx;
   reinterpret_cast<uint2*>(a.vc + row * kHeadDim)[lane] = vx;
-  if (__any_sync(0xffffffffu, bad) && lane == 0 && a.status) atomicOr(a.status, kStatusRange);
 }
 
 // Export only (the per-row-block column counts of the format): one warp per
 // (unit, row block m) counts the chosen keys j <= 64m + 63 whose tile
 // distance m - j/64 is not active.  The list is ascending, so the warp stops
 // at the first key past the block.
-__global__ void vs_col_count_kernel(const int32_t* __restrict__ vertical, int kv, int NB,
+__global__ void vs_col_count_kernel(const int32_t* __restrict__ vertical, int kv, int N, int NB,
                                     const uint32_t* __restrict__ tile_dist, int dist_words,
-                                    int32_t* __restrict__ col_count, int n_units) {
+                                    int32_t* __restrict__ col_count, int n_units,
+                                    uint32_t* status) {
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (gw >= static_cast<int64_t>(n_units) * NB) return;
@@ -161,7 +156,7 @@ __global__ void vs_col_count_kernel(const int32_t* __restrict__ vertical, int kv
     const int s = s0 + lane;
     bool col = false, past = false;
     if (s < kv) {
-      const int j = V[s];
+      const int j = MSA_IDX(V[s], 0, N, status);
       if (j > last_row) {
         past = true;
       } else {
@@ -179,17 +174,17 @@ __global__ void vs_col_count_kernel(const int32_t* __restrict__ vertical, int kv
 
 cudaError_t launch_vs_col_count(const Geometry& g, const int32_t* vertical, int kv,
                                 const uint32_t* tile_dist, int dist_words, int32_t* col_count,
-                                cudaStream_t st, int* n_launch) {
+                                uint32_t* status, cudaStream_t st, int* n_launch) {
   const int64_t warps = static_cast<int64_t>(g.n_units) * g.NB;
   if (warps == 0) return cudaSuccess;
   vs_col_count_kernel<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, st>>>(
-      vertical, kv, g.NB, tile_dist, dist_words, col_count, g.n_units);
+      vertical, kv, g.N, g.NB, tile_dist, dist_words, col_count, g.n_units, status);
   const cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) ++*n_launch;
   return e;
 }
 
-cudaError_t launch_vs_index(const Geometry& g, const UnitMap& u, TensorView k, TensorView v,
+cudaError_t launch_vs_index(const Geometry& g, const UnitMap& u, TensorView k, const __half* v16,
                             const int32_t* slash, int ks, const int32_t* vertical, int kv,
                             uint32_t* tile_dist, int dist_words, int32_t* qdelta,
                             int32_t* qdelta_count, uint32_t* col_chunks, int chunk_words,
@@ -201,23 +196,27 @@ cudaError_t launch_vs_index(const Geometry& g, const UnitMap& u, TensorView k, T
     e = cudaFuncSetAttribute(vs_tile_dist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
   }
-  vs_tile_dist_kernel<<<g.n_units, kTilesThreads, smem, st>>>(slash, ks, g.NB, g.NQ, tile_dist,
-                                                             dist_words, qdelta, qdelta_count);
+  vs_tile_dist_kernel<<<g.n_units, kTilesThreads, smem, st>>>(slash, ks, g.N, g.NB, g.NQ, tile_dist,
+                                                             dist_words, qdelta, qdelta_count,
+                                                             status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   ++*n_launch;
   const int64_t warps = static_cast<int64_t>(g.n_units) * g.NQ * chunk_words;
   const int64_t blocks = (warps * 32 + 255) / 256;
   vs_col_chunks_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-      vertical, kv, g.NB, g.NQ, tile_dist, dist_words, col_chunks, chunk_words, g.n_units);
+      vertical, kv, g.N, g.NB, g.NQ, tile_dist, dist_words, col_chunks, chunk_words, g.n_units,
+      status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   ++*n_launch;
   GatherArgs a;
   a.u = u;
   a.G = g.G;
+  a.Hkv = g.Hkv;
+  a.N = g.N;
   a.kv = kv;
   a.kv_pad = kv_pad;
   a.k = k.data; a.k_sb = k.sb; a.k_sh = k.sh; a.k_sn = k.sn;
-  a.v = v.data; a.v_sb = v.sb; a.v_sh = v.sh; a.v_sn = v.sn;
+  a.v16 = v16;
   a.vertical = vertical;
   a.kc = kc;
   a.vc = vc;

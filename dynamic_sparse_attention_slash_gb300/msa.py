@@ -21,6 +21,9 @@ _PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 # MSA_LIBRARY names another build of the same library to load instead (for
 # instance the bounds-checking build, libmsa_checked.so).
 LIB_PATH = os.environ.get("MSA_LIBRARY") or os.path.join(_PKG_DIR, "libmsa.so")
+# MSA_STRICT_STATUS=1: every call waits for its work and raises MsaError when
+# its device status word is not MSA_OK (a debugging mode; it synchronises).
+STRICT_STATUS = bool(os.environ.get("MSA_STRICT_STATUS"))
 
 MSA_OK = 0
 MSA_ERR_INVALID = 1
@@ -28,7 +31,7 @@ MSA_ERR_UNSUPPORTED = 2
 MSA_ERR_WORKSPACE = 3
 MSA_ERR_CUDA = 4
 MSA_ERR_TIMEOUT = 5
-MSA_ERR_RANGE = 6
+MSA_ERR_BOUNDS = 6
 
 MSA_KIND_VERTICAL_SLASH = 0
 MSA_KIND_BLOCK_SPARSE = 1
@@ -302,13 +305,17 @@ def _run(fn_name, kind, q, k, v, args, out, p0, p1, last_q, scale, heads, worksp
     lib = load_library()
     prep = _Prepared(q, k, v, out, stream)
     keep = []
-    opts, _ = _opts(prep.q, prep.k, kind, p0, p1, last_q, scale, heads, workspace, export,
-                    stage_events, stream, keep, kv_select)
+    opts, ws = _opts(prep.q, prep.k, kind, p0, p1, last_q, scale, heads, workspace, export,
+                     stage_events, stream, keep, kv_select)
     qt, kt, vt, ot = describe(prep.q), describe(prep.k), describe(prep.v), describe(prep.out)
     status = getattr(lib, fn_name)(ctypes.byref(qt), ctypes.byref(kt), ctypes.byref(vt), *args,
                                    ctypes.byref(ot), ctypes.byref(opts))
     if status != MSA_OK:
         raise MsaError(status, fn_name)
+    if STRICT_STATUS:  # wait for the call and read (and clear) its device status word
+        status = device_status(ws, stream)
+        if status != MSA_OK:
+            raise MsaError(status, f"{fn_name} (device status)")
     return prep.result()
 
 

@@ -10,6 +10,7 @@ synchronous call would give.
 """
 from __future__ import annotations
 
+import os
 from typing import Callable, Sequence, Tuple
 
 import torch
@@ -26,9 +27,11 @@ def run_pipelined(step: Callable[[torch.Tensor, torch.Tensor, torch.Tensor, torc
              repeat (it is rewritten only after its previous copy finished).
     step:    enqueues the attention of device q, k, v into device out on the
              current stream (e.g. one or more msa_* calls).
-    Returns the CUDA events of the run ({"start", "end"} on the compute stream
-    and per-batch "compute" (start, end) pairs) once everything is enqueued;
-    the caller synchronises (events["end"].synchronize()).
+    Returns the CUDA events of the run once everything is enqueued: "start" and
+    "end" on the compute stream, and per batch the (start, end) pairs of its
+    "compute", its host->device copies ("h2d", on the upload stream) and its
+    device->host copy ("d2h", on the download stream); the caller
+    synchronises (events["end"].synchronize()).
     """
     if len(batches) != len(outs) or not batches:
         raise ValueError("one host output per batch, at least one batch")
@@ -54,9 +57,9 @@ def run_pipelined(step: Callable[[torch.Tensor, torch.Tensor, torch.Tensor, torc
         t.record_stream(down)
     n = len(batches)
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    h2d_done = [ev() for _ in range(n)]
+    h2d_start, h2d_done = [ev() for _ in range(n)], [ev() for _ in range(n)]
     comp = [(ev(), ev()) for _ in range(n)]
-    d2h_done = [ev() for _ in range(n)]
+    d2h_start, d2h_done = [ev() for _ in range(n)], [ev() for _ in range(n)]
     start, end = ev(), ev()
     last_out_copy = {}
     start.record(stream)
@@ -67,6 +70,7 @@ def run_pipelined(step: Callable[[torch.Tensor, torch.Tensor, torch.Tensor, torc
             up.wait_event(start)
             if i >= 2:                      # device inputs b were read by batch i-2
                 up.wait_event(comp[i - 2][1])
+            h2d_start[i].record(up)
             qd.copy_(qh, non_blocking=True)
             kd.copy_(kh, non_blocking=True)
             vd.copy_(vh, non_blocking=True)
@@ -83,9 +87,75 @@ def run_pipelined(step: Callable[[torch.Tensor, torch.Tensor, torch.Tensor, torc
             prev = last_out_copy.get(id(outs[i]))
             if prev is not None:            # same host buffer: keep the copies in order
                 down.wait_event(prev)
+            d2h_start[i].record(down)
             outs[i].copy_(dev_out[b], non_blocking=True)
             d2h_done[i].record(down)
             last_out_copy[id(outs[i])] = d2h_done[i]
     stream.wait_event(d2h_done[n - 1])
     end.record(stream)
-    return {"start": start, "end": end, "compute": comp}
+    return {"start": start, "end": end, "compute": comp,
+            "h2d": list(zip(h2d_start, h2d_done)), "d2h": list(zip(d2h_start, d2h_done))}
+
+
+# ----------------------------------------------------------------------------- NUMA placement
+def gpu_numa_node(device) -> int | None:
+    """NUMA node of the host CPUs attached to a GPU (its PCI device's node in
+    sysfs), or None where the system does not say."""
+    try:
+        p = torch.cuda.get_device_properties(torch.device(device))
+        bdf = f"{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+        with open(f"/sys/bus/pci/devices/{bdf}/numa_node") as f:
+            node = int(f.read().strip())
+        return node if node >= 0 else None
+    except (AttributeError, OSError, ValueError):
+        return None
+
+
+def node_cpus(node: int) -> set:
+    """The CPUs of a NUMA node (sysfs cpulist, e.g. "0-71,144-215")."""
+    cpus = set()
+    with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
+        for part in f.read().strip().split(","):
+            if part:
+                lo, _, hi = part.partition("-")
+                cpus.update(range(int(lo), int(hi or lo) + 1))
+    return cpus
+
+
+def bind_to_gpu_node(device) -> dict:
+    """Restricts this process to the CPUs of the GPU's NUMA node (those the
+    process may use), so that pinned host buffers allocated afterwards are
+    placed in that node's memory (first touch).  Returns what was done."""
+    node = gpu_numa_node(device)
+    if node is None:
+        return {"gpu_numa_node": None, "bound": False}
+    try:
+        cpus = node_cpus(node) & os.sched_getaffinity(0)
+        if cpus:
+            os.sched_setaffinity(0, cpus)
+        return {"gpu_numa_node": node, "bound": bool(cpus), "cpus": len(cpus)}
+    except OSError:
+        return {"gpu_numa_node": node, "bound": False}
+
+
+def buffer_numa_pages(t: torch.Tensor) -> dict:
+    """Pages of the host mapping holding tensor t, per NUMA node, from
+    /proc/self/numa_maps ({node: pages}; empty where the kernel does not say)."""
+    addr = t.data_ptr()
+    best = None
+    try:
+        with open("/proc/self/numa_maps") as f:
+            for line in f:
+                start = int(line.split(" ", 1)[0], 16)
+                if start <= addr and (best is None or start > best[0]):
+                    best = (start, line)
+    except OSError:
+        return {}
+    pages = {}
+    if best is not None:
+        for field in best[1].split():
+            if field[:1] == "N" and "=" in field:
+                node, cnt = field[1:].split("=")
+                if node.isdigit():
+                    pages[int(node)] = pages.get(int(node), 0) + int(cnt)
+    return pages

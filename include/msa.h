@@ -37,9 +37,12 @@
  *           msa_workspace_bytes() bytes any of the four (MSA_ERR_WORKSPACE);
  *           q, k and v may share memory with one another.
  * Precision S = Q K^T is a bf16 x bf16 product with f32 accumulation; the
- *           softmax runs in f32; P and a staged f16 copy of v (exact for
- *           |v| <= 65504, which is checked) form the P.V product with f32
- *           accumulation; out is written as bf16 (round to nearest even).
+ *           softmax runs in f32; P and a staged f16 copy of v form the P.V
+ *           product with f32 accumulation; out is written as bf16 (round to
+ *           nearest even).  The f16 copy is exact for a KV head whose values
+ *           all lie within |v| <= 65504; a head with larger values is copied
+ *           scaled by a power of two 2^-e that brings it into range, and its
+ *           output is multiplied by 2^e (exact).
  * Streams   Work is enqueued on opts->stream (NULL: the legacy default
  *           stream) and runs asynchronously; a return of MSA_OK means every
  *           launch was enqueued.  Nothing synchronises with the host.
@@ -67,7 +70,9 @@ extern "C" {
 #define MSA_ERR_WORKSPACE 3   /* workspace missing, misaligned or too small */
 #define MSA_ERR_CUDA 4        /* a CUDA call or kernel launch failed */
 #define MSA_ERR_TIMEOUT 5     /* a bounded device-side wait gave up (read by msa_device_status) */
-#define MSA_ERR_RANGE 6       /* |v| > 65504 somewhere: outside the f16 range of P.V (read by msa_device_status) */
+#define MSA_ERR_BOUNDS 6      /* bounds-checking build (libmsa_checked.so): a kernel read an
+                                 index out of range and used a valid one instead (read by
+                                 msa_device_status; the output of that call is not valid) */
 
 /* Workspace kinds for msa_workspace_bytes(). */
 #define MSA_KIND_VERTICAL_SLASH 0
@@ -295,8 +300,9 @@ int msa_vertical_slash_static(const msa_tensor* q, const msa_tensor* k, const ms
  * Device status of msa_vertical_slash_static's array on the current device,
  * as msa_device_status() reports it for a workspace: enqueues a read of the
  * status word on `stream` after the work already enqueued there, synchronises
- * that stream, then clears the word.  Returns MSA_OK, MSA_ERR_TIMEOUT, or
- * MSA_ERR_CUDA if the lookup or the copy failed.  Allocates nothing.
+ * that stream, then clears the word.  Returns MSA_OK, MSA_ERR_TIMEOUT,
+ * MSA_ERR_BOUNDS (bounds-checking build only), or MSA_ERR_CUDA if the lookup or
+ * the copy failed.  Allocates nothing.
  */
 int msa_vertical_slash_static_status(void* stream);
 
@@ -333,8 +339,8 @@ size_t msa_workspace_bytes(int kind, const msa_tensor* q, const msa_tensor* k, i
 /*
  * Reads (and clears) the device status word of a workspace after the work of
  * an earlier call has been enqueued on `stream`; synchronises that stream.
- * Returns MSA_OK, MSA_ERR_TIMEOUT, MSA_ERR_RANGE, or MSA_ERR_CUDA if the copy
- * itself failed.
+ * Returns MSA_OK, MSA_ERR_TIMEOUT, MSA_ERR_BOUNDS (bounds-checking build only),
+ * or MSA_ERR_CUDA if the copy itself failed.
  */
 int msa_device_status(void* workspace, void* stream);
 

@@ -10,6 +10,16 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
+def test_checked_build_exports_the_same_functions():
+    """The bounds-checking build declares and rejects exactly like the ordinary one."""
+    from dynamic_sparse_attention_slash_gb300 import build
+    chk = ctypes.CDLL(build.build(checked=True))
+    for name in declared_functions():
+        assert hasattr(chk, name), name
+    chk.msa_status_string.restype = ctypes.c_char_p
+    assert b"bounds" in chk.msa_status_string(6)
+
+
 @pytest.fixture(scope="module")
 def lib():
     from dynamic_sparse_attention_slash_gb300 import build, msa

@@ -280,18 +280,71 @@ def test_host_tensors_round_trip():
     P.compare_out(np64(out[0]), ref[0], "host path")
 
 
-def test_value_outside_f16_range_is_reported():
-    """v is staged to f16 for P.V; a value beyond 65504 must be reported, not hidden."""
-    q, k, v = qkv(1, 2, 1, 256, 20)
-    v[0, 0, 5, 3] = 1.0e5
-    ws = torch.empty(msa.workspace_bytes(msa.MSA_KIND_STREAMING, q, k), dtype=torch.uint8,
-                     device="cuda")
-    msa.msa_streaming(q, k, v, 1, 2, workspace=ws)
-    assert msa.device_status(ws) == msa.MSA_ERR_RANGE
-    assert msa.device_status(ws) == msa.MSA_OK  # reading clears the word
-    v[0, 0, 5, 3] = 60000.0
-    msa.msa_streaming(q, k, v, 1, 2, workspace=ws)
-    assert msa.device_status(ws) == msa.MSA_OK
+def _all_heads(q, k, v):
+    """One call of every head type on all heads (block-sparse and hierarchical
+    heads with a few kept blocks, vertical-slash with column chunks)."""
+    return {
+        "streaming": msa.msa_streaming(q, k, v, 1, 3),
+        "vertical-slash": msa.msa_vertical_slash(q, k, v, 150, 60),
+        "block-sparse": msa.msa_block_sparse(q, k, v, 5),
+        "hierarchical": msa.msa_hierarchical(q, k, v, [(4, 3), (1, 5)]),
+    }
+
+
+def test_values_beyond_f16_range_scale_exactly():
+    """The P.V product reads an f16 copy of v; a KV head whose values leave the
+    f16 range is copied scaled by 2^-e and its output multiplied by 2^e.
+    Powers of two scale every f16 product and f32 sum exactly, so multiplying
+    one KV head's v by 2^17 (values up to ~6e5) must multiply exactly that
+    head group's outputs by 2^17, bit for bit, for every head type, while the
+    other group's outputs stay the same.  (Values below the f16 normal range
+    are zeroed first: the unscaled copy would round them, the scaled one not.)"""
+    q, k, v = qkv(1, 4, 2, 1088, 21, bs=True)
+    # no value in the f16 subnormal range, where the unscaled copy would round
+    v = torch.where(v.abs() < 2.0 ** -13, torch.zeros_like(v), v)
+    base = _all_heads(q, k, v)
+    v2 = v.clone()
+    v2[0, 0] *= 2.0 ** 17
+    assert v2[0, 0].abs().max().item() > 65504
+    big = _all_heads(q, k, v2)
+    torch.cuda.synchronize()
+    for name in base:
+        assert torch.equal(big[name][0, :2], base[name][0, :2] * 2.0 ** 17), name
+        assert torch.equal(big[name][0, 2:], base[name][0, 2:]), name
+
+
+def test_values_beyond_f16_range_match_the_oracle():
+    """v ~ 3e4 N(0, 1) (up to ~1.4e5, not a power-of-two multiple of anything in
+    range) against the oracle on every head type.  The kernel's error scales
+    with |v|, so the bounds are the parity tolerances times 3e4 (plus half a
+    bf16 ulp of the reference)."""
+    F = 3.0e4
+    q, k, v = qkv(1, 2, 1, 1088, 22, bs=True)
+    v = (v.float() * F).to(torch.bfloat16)
+    assert v.abs().max().item() > 65504
+    outs = _all_heads(q, k, v)
+    torch.cuda.synchronize()
+    qn, kn, vn = np64(q), np64(k), np64(v)
+    ref = {"streaming": O.streaming_forward(q.cpu(), k.cpu(), v.cpu(), 1, 3)[0][0],
+           "block-sparse": O.block_sparse_attention(q.cpu(), k.cpu(), v.cpu(), 5)[0][0],
+           "hierarchical": O.hierarchical_sparse_attention(q.cpu(), k.cpu(), v.cpu(),
+                                                           [(4, 3), (1, 5)])[0][0]}
+    # vertical-slash: the oracle's attention over the GPU's own sets
+    _, ex = P.run_vs(q, k, v, 150, 60)
+    vsr = []
+    for h in range(2):
+        V, S = ex["vertical"][h].astype(np.int64), ex["slash"][h].astype(np.int64)
+        act = O.vs_active_tiles(S, 1088)
+        vsr.append(O.attend_blocks(qn[0, h], kn[0, 0], vn[0, 0],
+                                   O.vs_block_mask(act, O.vs_columns(V, act, 1088), 1088),
+                                   1 / math.sqrt(D))[0])
+    ref["vertical-slash"] = np.stack(vsr)
+    for name, out in outs.items():
+        got, want = np64(out[0]), ref[name]
+        d = np.abs(got - want)
+        assert np.isfinite(got).all(), name
+        assert (d <= F * P.MAX_TOL + P.half_ulp_bf16(want)).all(), (name, d.max())
+        assert d.mean() <= F * P.MEAN_TOL, (name, d.mean())
 
 
 def test_golden_tiny_block_sparse_and_streaming():
