@@ -329,7 +329,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="mixed_128k", choices=sorted(inputs.WORKLOADS))
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-rows", type=int, default=1536, help="oracle rows per head (cpu_baseline)")
     ap.add_argument("--ref-rows", type=int, default=24, help="oracle rows per head (reference arm)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -512,6 +512,13 @@ def main():
         compute_ms = sum(a_.elapsed_time(b_) for a_, b_ in evs["compute"]) / S
         h2d_ms = sum(a_.elapsed_time(b_) for a_, b_ in evs["h2d"]) / S
         d2h_ms = sum(a_.elapsed_time(b_) for a_, b_ in evs["d2h"]) / S
+        # where the time between the steps' compute went: before the first
+        # step (its inputs' upload), between steps, after the last (the last
+        # output's download)
+        comp = evs["compute"]
+        gaps = [comp[i - 1][1].elapsed_time(comp[i][0]) for i in range(1, S)]
+        head_ms = evs["start"].elapsed_time(comp[0][0])
+        tail_ms = comp[-1][1].elapsed_time(evs["end"])
         e_val = sum_over_ranks(step_flops * S, world) / (e_ms * 1e-3) / 1e12
         h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
         d2h = oh[0].numel() * oh[0].element_size()
@@ -520,6 +527,8 @@ def main():
                "ms_per_step": e_ms / S, "compute_ms_per_step": compute_ms, "steps": S,
                "h2d_ms_per_step": h2d_ms, "d2h_ms_per_step": d2h_ms,
                "h2d_gbps": h2d / (h2d_ms * 1e6), "d2h_gbps": d2h / (d2h_ms * 1e6),
+               "before_first_ms": head_ms, "after_last_ms": tail_ms,
+               "gap_ms_mean": sum(gaps) / max(len(gaps), 1), "gap_ms_max": max(gaps, default=0.0),
                "numa": numa,
                "pipelined": "pipeline.run_pipelined: double-buffered inputs/outputs, "
                             "copies on two side streams"}

@@ -9,12 +9,15 @@
 // the block's mean-pooled query (the block-sparse head's pooling), over the
 // candidates j <= 64m + 63.  Every chunk is a group of whole 64-token blocks,
 // so every stage reads only the block maxima r[m][n] = max over the keys of
-// block n of the token scores: hip_block_max_kernel computes them, fp32 with
-// packed f32x2 FMAs in a fixed order (deterministic), for the causal blocks
-// n <= m only.  It is a register-tiled product of 64 pooled queries with 128
-// keys per CTA: each thread holds 8 rows x 8 keys, the two operands staged in
-// shared memory transposed (dimension-major), so one dimension step is four
-// 16-byte shared loads for 32 f32x2 FMAs.
+// block n of the token scores: hip_block_max_kernel computes them for the
+// causal blocks n <= m only, on the tensor cores.  The pooled queries (f32)
+// are split into three bf16 parts whose sum holds ~24 significant bits
+// (hip_split_kernel); each 128 x 128 score tile is the f32-accumulated sum of
+// the three parts' products with a TMA-staged bf16 key tile (tcgen05.mma into
+// TMEM, two TMEM buffers so the next tile's products overlap the maxima of
+// this one), which matches an f32 dot product to within a few f32 roundings.
+// Four warps read the tile from TMEM, one query block per thread, and keep
+// the maximum of each 64-key half.
 //
 // Selection.  hip_select_kernel runs the stages for one query block per CTA:
 // a stage's chunk score is the maximum of r over the chunk's surviving
@@ -35,112 +38,187 @@
 namespace msa {
 namespace {
 
-constexpr int kRT = 64;             // pooled query rows (query blocks) per score CTA
-constexpr int kKT = 128;            // keys per score CTA (two key blocks)
-constexpr int kScoreThreads = 128;  // 8 x 16 threads: 8 rows x 8 keys each
+constexpr int kTileBytes = 128 * 128 * 2;  // 128 rows x 128 dims of 16-bit values
+constexpr int kHalfBytes = kTileBytes / 2;   // one 64-dim half (128-byte swizzled rows)
+constexpr int kRT = 128;                     // pooled query rows (query blocks) per score CTA
+constexpr int kKT = 128;                     // keys per key tile (two key blocks)
+constexpr int kChunkTiles = 32;              // key tiles per score CTA
+constexpr int kScoreThreads = 256;
+constexpr int kSplitThreads = 256;
 constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
 
+// Pooled queries as three bf16 parts hi + mid + lo (hi = bf16(x), mid =
+// bf16(x - hi), lo = bf16(x - hi - mid); each difference is exact in f32), so
+// the sum carries ~24 significant bits: three bf16 products with an exact f32
+// product and f32 accumulation give the score to about f32 accuracy.
+// qsplit is [3][units * NB][128].
+__global__ void __launch_bounds__(kSplitThreads) hip_split_kernel(const float* __restrict__ qpool,
+                                                                  int64_t n, __nv_bfloat16* qsplit) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kSplitThreads + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * kSplitThreads) {
+    const float x = qpool[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+    const float r1 = x - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    qsplit[i] = hi;
+    qsplit[n + i] = mid;
+    qsplit[2 * n + i] = __float2bfloat16_rn(r2);
+  }
+}
+
 struct HipScoreArgs {
   UnitMap u;
-  int N, NB, G;
+  int N, NB, G, n_units;
   int m0, rows;        // the slab: query blocks [m0, m0 + rows)
   int slab_stride;     // rows of rmax per unit
   float scale;
-  const float* qpool;  // [units][NB][128]
-  const __nv_bfloat16* k;
-  int64_t k_sb, k_sh, k_sn;
   float* rmax;         // [units][slab_stride][NB]; entry (m - m0, n) for n <= m
+  uint32_t* status;
 };
 
-struct __align__(16) ScoreSmem {
-  float q[kHeadDim][kRT];  // q[d][r]: dimension d of pooled row r
-  float k[kHeadDim][kKT];  // k[d][j]: dimension d of key j
+struct __align__(1024) ScoreSmem {
+  uint8_t q[3][kTileBytes];  // hi, mid, lo parts of 128 pooled rows
+  uint8_t k[2][kTileBytes];  // key tiles, two stages
+  uint64_t q_full, k_full[2], k_empty[2], s_full[2], s_empty[2], final_bar;
+  uint32_t tmem_base;
+  int abort;
 };
 
-// grid (key tile kt, row tile, unit): block maxima of query blocks
-// [m0 + 64 rt, +64) against key blocks 2kt and 2kt + 1.
-__global__ void __launch_bounds__(kScoreThreads) hip_block_max_kernel(const __grid_constant__ HipScoreArgs a) {
-  extern __shared__ __align__(16) uint8_t dyn[];
-  ScoreSmem& sm = *reinterpret_cast<ScoreSmem*>(dyn);
-  const int kt = blockIdx.x, unit = blockIdx.z;
-  const int r0 = blockIdx.y * kRT;                 // first slab row of the tile
-  const int m_first = a.m0 + r0;
-  const int m_last = a.m0 + min(r0 + kRT, a.rows) - 1;
-  if (2 * kt > m_last) return;  // every key of the tile is after every row's candidates
-  const int tid = threadIdx.x;
-  const int b = unit / a.u.n_heads;
-  const int hkv = a.u.heads[unit % a.u.n_heads] / a.G;
-  // stage the pooled queries (rows past the slab read as zero)
-  const float* qp = a.qpool + static_cast<int64_t>(unit) * a.NB * kHeadDim;
-  for (int i = tid; i < kRT * (kHeadDim / 4); i += kScoreThreads) {
-    const int r = i % kRT, d4 = i / kRT;  // consecutive threads: consecutive rows (no bank conflict)
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (m_first + r <= m_last)
-      v = reinterpret_cast<const float4*>(qp + static_cast<int64_t>(m_first + r) * kHeadDim)[d4];
-    sm.q[4 * d4 + 0][r] = v.x;
-    sm.q[4 * d4 + 1][r] = v.y;
-    sm.q[4 * d4 + 2][r] = v.z;
-    sm.q[4 * d4 + 3][r] = v.w;
+// grid (key chunk, row tile, unit): block maxima of query blocks
+// [m0 + 128 rt, +128) against the key tiles [32 chunk, +32) they reach.
+// Warp 0 loads (TMA), warp 1 issues tcgen05.mma (S = hi K^T + mid K^T + lo K^T
+// into one of two TMEM buffers), warps 4-7 read S from TMEM (thread r: query
+// block m0 + 128 rt + r) and write the maxima of its two 64-key halves.
+__global__ void __launch_bounds__(kScoreThreads, 1)
+hip_block_max_kernel(const __grid_constant__ HipScoreArgs a, const __grid_constant__ CUtensorMap mqs,
+                     const __grid_constant__ CUtensorMap mk) {
+  extern __shared__ uint8_t smem_raw[];
+  ScoreSmem& sm = *reinterpret_cast<ScoreSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+  const int unit = blockIdx.z, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int M0 = a.m0 + blockIdx.y * kRT;                    // first query block of the tile
+  const int m_last = min(M0 + kRT, a.m0 + a.rows) - 1;
+  const int kt_end = min((a.N + kKT - 1) / kKT, m_last / 2 + 1);  // tiles holding candidates
+  const int kt0 = blockIdx.x * kChunkTiles;
+  const int n = min(kt_end - kt0, kChunkTiles);
+  if (n <= 0) return;  // uniform for the CTA, before any barrier
+  const int b = unit / a.u.n_heads, hkv = a.u.heads[unit % a.u.n_heads] / a.G;
+  volatile int* abort = &sm.abort;
+  if (tid == 0) {
+    mbar_init(&sm.q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.k_empty[s], 1);
+      mbar_init(&sm.s_full[s], 1);
+      mbar_init(&sm.s_empty[s], 4);  // one arrival per reading warp
+    }
+    mbar_init(&sm.final_bar, 1);
+    sm.abort = 0;
+    fence_mbar_init();
   }
-  // stage the keys as f32 (keys past N read as zero; they are masked below)
-  {
-    const int j = kKT * kt + tid;
-    const __nv_bfloat16* kr = a.k + b * a.k_sb + hkv * a.k_sh + static_cast<int64_t>(j) * a.k_sn;
-#pragma unroll 4
-    for (int d8 = 0; d8 < kHeadDim / 8; ++d8) {
-      uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-      if (j < a.N) raw = reinterpret_cast<const uint4*>(kr)[d8];
-      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&mqs);
+      tma_prefetch_desc(&mk);
+      const int rows_total = a.n_units * a.NB;
+      mbar_arrive_expect_tx(&sm.q_full, 3 * kTileBytes);
+      for (int part = 0; part < 3; ++part) {
+        const int row = part * rows_total + unit * a.NB + M0;
+        tma_load_2d(sm.q[part], &mqs, &sm.q_full, 0, row);
+        tma_load_2d(sm.q[part] + kHalfBytes, &mqs, &sm.q_full, 64, row);
+      }
+      int issued = 0;
+      for (int i = 0; i < n; ++i) {
+        const int s = i & 1;
+        if (!mbar_wait(&sm.k_empty[s], ((i >> 1) & 1) ^ 1, abort)) break;
+        mbar_arrive_expect_tx(&sm.k_full[s], kTileBytes);
+        tma_load_4d(sm.k[s], &mk, &sm.k_full[s], 0, kKT * (kt0 + i), hkv, b);
+        tma_load_4d(sm.k[s] + kHalfBytes, &mk, &sm.k_full[s], 64, kKT * (kt0 + i), hkv, b);
+        issued = i + 1;
+      }
+      // drain: the latest load of every stage, and Q, must land before exit
+      int never = 0;
+      mbar_wait(&sm.q_full, 0, &never);
+      for (int i = max(0, issued - 2); i < issued; ++i) mbar_wait(&sm.k_full[i & 1], (i >> 1) & 1, &never);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+      bool ok = mbar_wait(&sm.q_full, 0, abort);
+      tc_fence_after();
+      uint64_t qd[3];
+      for (int part = 0; part < 3; ++part) qd[part] = sdesc_sw128(smem_u32(sm.q[part]), 16, 1024);
+      const uint64_t kd0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
+      constexpr uint64_t kStageStep = kTileBytes >> 4;
+      for (int i = 0; ok && i < n; ++i) {
+        const int s = i & 1;
+        if (!mbar_wait(&sm.k_full[s], (i >> 1) & 1, abort) ||
+            !mbar_wait(&sm.s_empty[s], ((i >> 1) & 1) ^ 1, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t s_tm = tmem + 128 * s;
+        const uint64_t kd = kd0 + s * kStageStep;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        sm.k[8 * d8 + 2 * e][tid] = __low2float(h2[e]);
-        sm.k[8 * d8 + 2 * e + 1][tid] = __high2float(h2[e]);
+        for (int part = 0; part < 3; ++part) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+            mma_ss(s_tm, qd[part] + off, kd + off, idS, (part > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        mma_commit(&sm.s_full[s]);
+        mma_commit(&sm.k_empty[s]);
+      }
+      // every MMA issued above must complete before TMEM is released
+      mma_commit(&sm.final_bar);
+      int never = 0;
+      mbar_wait(&sm.final_bar, 0, &never);
+    }
+  } else if (warp >= 4) {
+    const int r = tid - 128;  // TMEM lane == row of the tile
+    const int m = M0 + r;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    for (int i = 0; i < n; ++i) {
+      const int s = i & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[s], (i >> 1) & 1, abort))) break;
+      tc_fence_after();
+      uint32_t raw[128];
+      tmem_ld128(lane_base + 128 * s, raw);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.s_empty[s]);
+      const int kt = kt0 + i;
+      const int j0 = kKT * kt;
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 64; ++e)
+          if (j0 + 64 * h2 + e < a.N) mx = fmaxf(mx, __uint_as_float(raw[64 * h2 + e]));
+        const int nb = 2 * kt + h2;
+        if (m <= m_last && nb <= m)
+          a.rmax[(static_cast<int64_t>(unit) * a.slab_stride + (m - a.m0)) * a.NB + nb] =
+              mx * a.scale;
       }
     }
   }
+  tc_fence_before();
   __syncthreads();
-  const int ty = tid >> 4, tx = tid & 15;  // rows 8 ty .. + 7, keys 8 tx .. + 7
-  float2 acc[8][4];
-#pragma unroll
-  for (int r = 0; r < 8; ++r)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) acc[r][c] = make_float2(0.f, 0.f);
-#pragma unroll 4
-  for (int d = 0; d < kHeadDim; ++d) {
-    const float4 qa = *reinterpret_cast<const float4*>(&sm.q[d][8 * ty]);
-    const float4 qb = *reinterpret_cast<const float4*>(&sm.q[d][8 * ty + 4]);
-    const float4 ka = *reinterpret_cast<const float4*>(&sm.k[d][8 * tx]);
-    const float4 kb = *reinterpret_cast<const float4*>(&sm.k[d][8 * tx + 4]);
-    const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-    const float2 kv[4] = {make_float2(ka.x, ka.y), make_float2(ka.z, ka.w),
-                          make_float2(kb.x, kb.y), make_float2(kb.z, kb.w)};
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const float2 q2 = make_float2(qv[r], qv[r]);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) acc[r][c] = ffma2(q2, kv[c], acc[r][c]);
-    }
-  }
-  // block maxima: this thread's 8 keys, then the 8 threads of a key block
-  // (lanes differing in bits 0..2); keys past N do not count
-  const int j0 = kKT * kt + 8 * tx;
-  const int n = 2 * kt + (tx >> 3);
-#pragma unroll
-  for (int r = 0; r < 8; ++r) {
-    float mx = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      if (j0 + 2 * c < a.N) mx = fmaxf(mx, acc[r][c].x);
-      if (j0 + 2 * c + 1 < a.N) mx = fmaxf(mx, acc[r][c].y);
-    }
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-    const int m = m_first + 8 * ty + r;
-    if ((tx & 7) == 0 && m <= m_last && n <= m)
-      a.rmax[(static_cast<int64_t>(unit) * a.slab_stride + (m - a.m0)) * a.NB + n] = mx * a.scale;
-  }
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 256);
+  if (tid == 0 && sm.abort && a.status) atomicOr(a.status, kStatusTimeout);
 }
 
 struct HipStages {
@@ -287,21 +365,31 @@ int hip_slab_rows(int n_units, int NB) {
   return static_cast<int>(rows < kRT ? kRT : rows);
 }
 
-cudaError_t launch_hip_index(const Geometry& g, const UnitMap& u, TensorView k, const float* qpool,
-                             const int32_t* stage_c, const int32_t* stage_keep, int n_stages,
-                             float* rmax, int slab_rows, int32_t* block_count, int32_t* block_ids,
-                             int kb, cudaStream_t st, int* n_launch) {
+cudaError_t launch_hip_index(const Geometry& g, const UnitMap& u, const CUtensorMap& mk,
+                             const float* qpool, __nv_bfloat16* qsplit,
+                             const CUtensorMap& mqs, const int32_t* stage_c,
+                             const int32_t* stage_keep, int n_stages, float* rmax, int slab_rows,
+                             int32_t* block_count, int32_t* block_ids, int kb, uint32_t* status,
+                             cudaStream_t st, int* n_launch) {
   if (n_stages < 1 || n_stages > MSA_HIP_MAX_STAGES) return cudaErrorInvalidValue;
+  const int64_t n_split = static_cast<int64_t>(g.n_units) * g.NB * kHeadDim;
+  int64_t split_blocks = (n_split + kSplitThreads - 1) / kSplitThreads;
+  if (split_blocks > 152 * 8) split_blocks = 152 * 8;
+  hip_split_kernel<<<static_cast<unsigned>(split_blocks), kSplitThreads, 0, st>>>(qpool, n_split,
+                                                                                qsplit);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ++*n_launch;
   HipScoreArgs sa;
   sa.u = u;
   sa.N = g.N;
   sa.NB = g.NB;
   sa.G = g.G;
+  sa.n_units = g.n_units;
   sa.slab_stride = slab_rows;
   sa.scale = g.scale;
-  sa.qpool = qpool;
-  sa.k = k.data; sa.k_sb = k.sb; sa.k_sh = k.sh; sa.k_sn = k.sn;
   sa.rmax = rmax;
+  sa.status = status;
   HipSelArgs ta;
   ta.NB = g.NB;
   ta.slab_stride = slab_rows;
@@ -314,10 +402,10 @@ cudaError_t launch_hip_index(const Geometry& g, const UnitMap& u, TensorView k, 
   ta.block_count = block_count;
   ta.block_ids = block_ids;
   ta.kb = kb;
-  const int score_smem = static_cast<int>(sizeof(ScoreSmem));
+  const int score_smem = static_cast<int>(sizeof(ScoreSmem)) + 1024;
   const int sel_smem = (g.NB + (g.NB + 31) / 32) * 4;
-  cudaError_t e = cudaFuncSetAttribute(hip_block_max_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, score_smem);
+  e = cudaFuncSetAttribute(hip_block_max_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           score_smem);
   if (e != cudaSuccess) return e;
   if (sel_smem > 48 * 1024) {
     e = cudaFuncSetAttribute(hip_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -331,8 +419,9 @@ cudaError_t launch_hip_index(const Geometry& g, const UnitMap& u, TensorView k, 
     sa.rows = rows;
     // key tiles past the slab's last query block hold no candidate
     const int kt_end = min(n_kt, (m0 + rows - 1) / 2 + 1);
-    hip_block_max_kernel<<<dim3(kt_end, (rows + kRT - 1) / kRT, g.n_units), kScoreThreads,
-                           score_smem, st>>>(sa);
+    const int chunks = (kt_end + kChunkTiles - 1) / kChunkTiles;
+    hip_block_max_kernel<<<dim3(chunks, (rows + kRT - 1) / kRT, g.n_units), kScoreThreads,
+                           score_smem, st>>>(sa, mqs, mk);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     ++*n_launch;
     ta.m0 = m0;

@@ -231,7 +231,7 @@ BSLayout bs_layout(const Geometry& g, int64_t topk) {
 // query blocks, the kept blocks (block-sparse format) and their item lists.
 struct HIPLayout {
   int kb, tile_cap, slab;
-  size_t vmax, qpool, rmax, block_count, block_ids, tiles, tile_count, v16, total;
+  size_t vmax, qpool, qsplit, rmax, block_count, block_ids, tiles, tile_count, v16, total;
 };
 
 HIPLayout hip_layout(const Geometry& g, int64_t keep_last) {
@@ -244,6 +244,7 @@ HIPLayout hip_layout(const Geometry& g, int64_t keep_last) {
   c.off = kStatusBytes;
   L.vmax = c.take<uint32_t>(vmax_count(g));
   L.qpool = c.take<float>(U * g.NB * kHeadDim);
+  L.qsplit = c.take<__nv_bfloat16>(3 * U * g.NB * kHeadDim);
   L.rmax = c.take<float>(U * L.slab * g.NB);
   L.block_count = c.take<int32_t>(U * g.NB);
   L.block_ids = c.take<int32_t>(U * g.NB * L.kb);
@@ -634,10 +635,13 @@ int msa_hierarchical(const msa_tensor* q, const msa_tensor* k, const msa_tensor*
   void* ws = opts->workspace;
   // the kept blocks feed the block-sparse attention kernel: K and the f16 copy
   // of v are read in 64-key boxes
-  CUtensorMap mq, mk64, mv64;
-  if ((s = make_map_4d(&mq, q)) ||
+  CUtensorMap mq, mk, mk64, mv64, mqs;
+  if ((s = make_map_4d(&mq, q)) || (s = make_map_4d(&mk, k)) ||
       (s = make_map_4d(&mk64, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 64)) ||
-      (s = make_map_f16(&mv64, at<void>(ws, L.v16), c.g, 64)))
+      (s = make_map_f16(&mv64, at<void>(ws, L.v16), c.g, 64)) ||
+      (s = make_map_rows(&mqs, at<void>(ws, L.qsplit),
+                         3 * static_cast<int64_t>(c.g.n_units) * c.g.NB,
+                         CU_TENSOR_MAP_DATA_TYPE_BFLOAT16)))
     return s;
   const StageTimer tm{opts->stage_events, c.st};
   int launches = 0;
@@ -648,9 +652,10 @@ int msa_hierarchical(const msa_tensor* q, const msa_tensor* k, const msa_tensor*
                       &launches);
   if (e == cudaSuccess) e = launch_pool_q(c.g, c.u, view(q), at<float>(ws, L.qpool), c.st, &launches);
   if (e == cudaSuccess)
-    e = launch_hip_index(c.g, c.u, view(k), at<float>(ws, L.qpool), sc, sk, n_stages,
-                         at<float>(ws, L.rmax), L.slab, at<int32_t>(ws, L.block_count),
-                         at<int32_t>(ws, L.block_ids), L.kb, c.st, &launches);
+    e = launch_hip_index(c.g, c.u, mk, at<float>(ws, L.qpool), at<__nv_bfloat16>(ws, L.qsplit), mqs,
+                         sc, sk, n_stages, at<float>(ws, L.rmax), L.slab,
+                         at<int32_t>(ws, L.block_count), at<int32_t>(ws, L.block_ids), L.kb,
+                         at<uint32_t>(ws, 0), c.st, &launches);
   if (e == cudaSuccess)
     e = launch_bs_tiles(c.g, L.kb, at<int32_t>(ws, L.block_count), at<int32_t>(ws, L.block_ids),
                         at<int32_t>(ws, L.tiles), at<int32_t>(ws, L.tile_count), L.tile_cap,

@@ -204,10 +204,14 @@ cudaError_t launch_bs_tiles(const Geometry& g, int kb, const int32_t* block_coun
 // slab by slab of slab_rows query blocks; writes kept blocks in the
 // block-sparse format.  hip_slab_rows gives the slab height for a call.
 int hip_slab_rows(int n_units, int NB);
-cudaError_t launch_hip_index(const Geometry& g, const UnitMap& u, TensorView k, const float* qpool,
-                             const int32_t* stage_c, const int32_t* stage_keep, int n_stages,
-                             float* rmax, int slab_rows, int32_t* block_count, int32_t* block_ids,
-                             int kb, cudaStream_t st, int* n_launch);
+// mk: TMA map of k in 128-key boxes; qsplit: [3][units * NB][128] bf16 scratch
+// for the split pooled queries, mqs its 2-D TMA map (128-row boxes).
+cudaError_t launch_hip_index(const Geometry& g, const UnitMap& u, const CUtensorMap& mk,
+                             const float* qpool, __nv_bfloat16* qsplit,
+                             const CUtensorMap& mqs, const int32_t* stage_c,
+                             const int32_t* stage_keep, int n_stages, float* rmax, int slab_rows,
+                             int32_t* block_count, int32_t* block_ids, int kb, uint32_t* status,
+                             cudaStream_t st, int* n_launch);
 // The f16 copy of v for the KV heads the call reads, with each head's largest
 // |v| in vmax ([B][Hkv] float bits, zeroed before the call) and heads beyond
 // the f16 range scaled by 2^-v_scale_exp(vmax).
