@@ -19,7 +19,9 @@
 // Four warps read the tile from TMEM, one query block per thread, and keep
 // the maximum of each 64-key half.
 //
-// Selection.  hip_select_kernel runs the stages for one query block per CTA:
+// Selection.  hip_select_warp_kernel (below) runs the stages for one query
+// block per warp over short candidate lists; hip_select_kernel, for stage
+// lists whose candidates would not fit, runs them for one query block per CTA:
 // a stage's chunk score is the maximum of r over the chunk's surviving
 // blocks; the own chunk (the one holding block m) is always kept; the best
 // keep - 1 others are found by an 8-bit radix select on an order-preserving
@@ -228,7 +230,8 @@ struct HipStages {
 };
 
 struct HipSelArgs {
-  int NB, m0, slab_stride;
+  int NB, m0, rows, slab_stride;
+  int cap, warps;  // warp-level selection: candidate capacity per warp, warps per CTA
   const float* rmax;
   HipStages st;
   int32_t* block_count;  // [units][NB]
@@ -354,6 +357,172 @@ __global__ void __launch_bounds__(kSelThreads) hip_select_kernel(const __grid_co
   if (tid == 0) a.block_count[static_cast<int64_t>(unit) * a.NB + m] = min(placed, a.kb);
 }
 
+// Warp-level form of the stages (the usual case): warp w of a CTA runs query
+// block m = m0 + 8 blockIdx.x + w alone.  Stage s only looks at the chunks
+// that survived stage s - 1: the candidates are the sub-chunks (of size c_s)
+// of the kept chunks (of size c_{s-1}), every one of whose blocks <= m is
+// still a candidate, because chunk sizes nest.  So a stage is a list of at
+// most `cap` candidate chunks, ascending: their scores (the maximum of r over
+// the chunk's blocks <= m), an 8-bit radix select of the best keep - 1 others
+// on one warp (histograms in shared memory), and an ascending compaction of
+// the kept ones (the own chunk always) into the other list.  The same rule as
+// hip_select_kernel: scores descending, ties to the lower chunk.
+__global__ void __launch_bounds__(kSelThreads) hip_select_warp_kernel(const __grid_constant__ HipSelArgs a) {
+  extern __shared__ __align__(16) float dyn_w[];
+  __shared__ int hist[kSelWarps][256];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int unit = blockIdx.y;
+  const int r_slab = blockIdx.x * a.warps + warp;  // slab row of this warp
+  if (warp >= a.warps || r_slab >= a.rows) return;  // no CTA-wide barrier follows
+  const int m = a.m0 + r_slab;
+  float* sc = dyn_w + warp * a.cap;                                        // [cap] scores
+  int* ids_a = reinterpret_cast<int*>(dyn_w + a.warps * a.cap) + warp * 2 * a.cap;  // [cap]
+  int* ids_b = ids_a + a.cap;                                              // [cap]
+  int* h = hist[warp];
+  const float* row = a.rmax + (static_cast<int64_t>(unit) * a.slab_stride + r_slab) * a.NB;
+  const uint32_t lt = (1u << lane) - 1u;
+  int* cur = ids_a;  // candidate chunks of this stage (ascending)
+  int* nxt = ids_b;  // kept chunks of this stage (ascending)
+  int n_c = 0, n_k = 0, c_prev = 1;
+  for (int s = 0; s < a.st.n; ++s) {
+    const int c = a.st.c[s], own = m / c;
+    // candidates: every chunk of [0, m] at the first stage, afterwards the
+    // sub-chunks of the previous stage's kept chunks that start at or before m
+    if (s == 0) {
+      n_c = min(own + 1, a.cap);
+      for (int x = lane; x < n_c; x += 32) cur[x] = x;
+    } else {
+      const int ratio = c_prev / c;
+      n_c = 0;
+      for (int base = 0; base < n_k * ratio; base += 32) {
+        const int i = base + lane;
+        int y = 0;
+        bool ok = false;
+        if (i < n_k * ratio) {
+          y = nxt[i / ratio] * ratio + i % ratio;
+          ok = y <= own;
+        }
+        const uint32_t bal = __ballot_sync(0xffffffffu, ok);
+        const int pos = n_c + __popc(bal & lt);
+        if (ok && pos < a.cap) cur[pos] = y;
+        n_c += __popc(bal);
+      }
+      n_c = min(n_c, a.cap);
+    }
+    __syncwarp();
+    // scores; the own chunk takes no part in the ranking (it is kept)
+    int own_pos = -1;
+    for (int base = 0; base < n_c; base += 32) {
+      const int i = base + lane;
+      bool is_own = false;
+      if (i < n_c) {
+        const int x = cur[i];
+        float best = -INFINITY;
+        if (x != own) {
+          const int n_end = min(x * c + c, m + 1);
+          for (int nb = x * c; nb < n_end; ++nb) best = fmaxf(best, row[nb]);
+        } else {
+          is_own = true;
+        }
+        sc[i] = best;
+      }
+      const uint32_t bal = __ballot_sync(0xffffffffu, is_own);
+      if (bal) own_pos = base + __ffs(static_cast<int>(bal)) - 1;
+    }
+    __syncwarp();
+    const int need = min(a.st.keep[s] - 1, n_c - (own_pos >= 0 ? 1 : 0));
+    uint32_t prefix = 0u, mask = 0u;
+    int take = need;
+    if (need > 0) {
+      for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        for (int i = lane; i < 256; i += 32) h[i] = 0;
+        __syncwarp();
+        for (int i = lane; i < n_c; i += 32) {
+          const uint32_t key = ordered_key(sc[i]);
+          if ((key & mask) == prefix) atomicAdd(&h[(key >> shift) & 255u], 1);
+        }
+        __syncwarp();
+        // lane l holds bins 255 - 8l down to 248 - 8l; the bucket is the one
+        // in which the count from the top reaches `take`
+        int cnt[8], tot = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          cnt[j] = h[255 - 8 * lane - j];
+          tot += cnt[j];
+        }
+        int incl = tot;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += v;
+        }
+        const int excl = incl - tot;
+        const bool mine = excl < take && incl >= take;
+        const int src = __ffs(static_cast<int>(__ballot_sync(0xffffffffu, mine))) - 1;
+        int bucket = 0, above = excl;
+        if (mine) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (above + cnt[j] >= take) {
+              bucket = 255 - 8 * lane - j;
+              break;
+            }
+            above += cnt[j];
+          }
+        }
+        bucket = __shfl_sync(0xffffffffu, bucket, src);
+        above = __shfl_sync(0xffffffffu, above, src);
+        take -= above;
+        prefix |= static_cast<uint32_t>(bucket) << shift;
+        mask |= 255u << shift;
+        __syncwarp();  // every lane has read the histogram before it is cleared
+      }
+    }
+    // kept chunks, ascending: the own chunk, keys above the threshold, and the
+    // first `take` keys equal to it (lower chunks first)
+    n_k = 0;
+    int eq_seen = 0;
+    for (int base = 0; base < n_c; base += 32) {
+      const int i = base + lane;
+      bool keep = false, eq = false;
+      if (i < n_c) {
+        if (i == own_pos) {
+          keep = true;
+        } else if (need > 0) {
+          const uint32_t key = ordered_key(sc[i]);
+          eq = key == prefix;
+          keep = key > prefix;
+        }
+      }
+      const uint32_t eqb = __ballot_sync(0xffffffffu, eq);
+      keep |= eq && eq_seen + __popc(eqb & lt) < take;
+      eq_seen += __popc(eqb);
+      const uint32_t kb = __ballot_sync(0xffffffffu, keep);
+      if (keep) nxt[n_k + __popc(kb & lt)] = cur[i];
+      n_k += __popc(kb);
+    }
+    __syncwarp();
+    c_prev = c;
+  }
+  // the last stage's chunks are single blocks
+  int32_t* ids = a.block_ids + (static_cast<int64_t>(unit) * a.NB + m) * a.kb;
+  const int cnt = min(n_k, a.kb);
+  for (int i = lane; i < cnt; i += 32) ids[i] = nxt[i];
+  if (lane == 0) a.block_count[static_cast<int64_t>(unit) * a.NB + m] = cnt;
+}
+
+// Candidate chunks a stage can hold at most (the first stage: every chunk of
+// [0, NB); later: the previous stage's kept chunks times the size ratio).
+int hip_stage_cap(int NB, const int32_t* c, const int32_t* keep, int n) {
+  int cap = NB / c[0] + 1;
+  for (int s = 1; s < n; ++s) {
+    const int64_t v = static_cast<int64_t>(keep[s - 1]) * (c[s - 1] / c[s]);
+    cap = static_cast<int>(v > cap ? (v < NB + 1 ? v : NB + 1) : cap);
+  }
+  return cap;
+}
+
 }  // namespace
 
 int hip_slab_rows(int n_units, int NB) {
@@ -403,13 +572,21 @@ cudaError_t launch_hip_index(const Geometry& g, const UnitMap& u, const CUtensor
   ta.block_ids = block_ids;
   ta.kb = kb;
   const int score_smem = static_cast<int>(sizeof(ScoreSmem)) + 1024;
-  const int sel_smem = (g.NB + (g.NB + 31) / 32) * 4;
+  // the warp-level selection while eight warps' candidate lists (a score and
+  // two ids per candidate) fit in 160 KB of shared memory, else a CTA per
+  // query block
+  ta.cap = hip_stage_cap(g.NB, stage_c, stage_keep, n_stages);
+  ta.warps = kSelWarps;
+  const bool warp_sel = static_cast<int64_t>(ta.cap) * 12 * kSelWarps <= 160 * 1024;
+  const int sel_smem = warp_sel ? ta.cap * 12 * kSelWarps : (g.NB + (g.NB + 31) / 32) * 4;
   e = cudaFuncSetAttribute(hip_block_max_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            score_smem);
   if (e != cudaSuccess) return e;
   if (sel_smem > 48 * 1024) {
-    e = cudaFuncSetAttribute(hip_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             sel_smem);
+    e = warp_sel ? cudaFuncSetAttribute(hip_select_warp_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, sel_smem)
+                 : cudaFuncSetAttribute(hip_select_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, sel_smem);
     if (e != cudaSuccess) return e;
   }
   const int n_kt = (g.N + kKT - 1) / kKT;
@@ -425,7 +602,12 @@ cudaError_t launch_hip_index(const Geometry& g, const UnitMap& u, const CUtensor
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     ++*n_launch;
     ta.m0 = m0;
-    hip_select_kernel<<<dim3(rows, g.n_units), kSelThreads, sel_smem, st>>>(ta);
+    ta.rows = rows;
+    if (warp_sel)
+      hip_select_warp_kernel<<<dim3((rows + kSelWarps - 1) / kSelWarps, g.n_units), kSelThreads,
+                               sel_smem, st>>>(ta);
+    else
+      hip_select_kernel<<<dim3(rows, g.n_units), kSelThreads, sel_smem, st>>>(ta);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     ++*n_launch;
   }

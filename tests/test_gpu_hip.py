@@ -138,3 +138,27 @@ def test_hierarchical_two_slabs():
         ref, _ = O.attend_rows(qn, kn, vn, rows, keys, SCALE)
         P.compare_out(P.to_np(out[0, h, rows]), ref, f"slab h{h}")
     assert near <= 2, f"{near} near-tie row blocks"
+
+
+def test_hierarchical_long_single_stage_cta_selection():
+    """One stage of single blocks over 2048 query blocks: the candidate lists
+    would not fit eight warps' shared memory, so the selection runs one CTA
+    per query block (the other path); kept blocks on sampled query blocks and
+    outputs on sampled rows against the oracle."""
+    N, stages = 131072, [(1, 20)]
+    q, k, v = qkv(1, 2, 1, N, 35)
+    out, ex = P.run_hip(q, k, v, stages)
+    NB = N // 64
+    rng = np.random.default_rng(35)
+    rows = sorted(set(rng.integers(0, N, 16).tolist()) | {0, N - 1})
+    blocks = sorted({0, 1, 19, 20, NB - 1} | {i // 64 for i in rows})
+    near = 0
+    for h in range(2):
+        qn, kn, vn = P.to_np(q[0, h]), P.to_np(k[0, 0]), P.to_np(v[0, 0])
+        sel, nt = P.check_hip_blocks(ex["block_count"][h], ex["block_ids"][h], qn, kn, stages,
+                                     blocks, f"single-stage h{h}")
+        near += nt
+        keys = lambda i: np.concatenate([np.arange(64 * n, 64 * n + 64) for n in sel[i // 64]])
+        ref, _ = O.attend_rows(qn, kn, vn, rows, keys, SCALE)
+        P.compare_out(P.to_np(out[0, h, rows]), ref, f"single-stage h{h}")
+    assert near <= 1, f"{near} near-tie row blocks"
