@@ -52,12 +52,12 @@ UNIT = "TFLOP/s"
 MEASURED_TRAFFIC = {
     "workload": "mixed_128k",
     "kind": "vs",
-    "bytes": 2.533e9 + 0.652e9,
+    "bytes": 2.529e9 + 0.654e9,
     "sources": ("dynamic_sparse_attention_slash_gb300/csrc/prefill.cu",
                 "dynamic_sparse_attention_slash_gb300/csrc/prefill_common.cuh",
                 "dynamic_sparse_attention_slash_gb300/csrc/sm103_ptx.cuh",
                 "dynamic_sparse_attention_slash_gb300/csrc/msa_internal.h"),
-    "sha256": "0470a4bcfb3e50c906c3fbd6322c63a223f55238e12645a583b32c622a4f24fa",
+    "sha256": "46005435e7e9387d8e1020ca1d0d4a08194d5357189647cf5da2b30ed9e56fc6",
 }
 
 
