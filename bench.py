@@ -67,6 +67,10 @@ MEASURED_TRAFFIC = {
 KV_WINDOW = 256
 KV_KEEP = 4096
 
+# Hierarchical pruning head measured beside the block-sparse heads of the step:
+# chunks of 16, 4 and 1 blocks keeping 16, 40 and the block-sparse top-k.
+HIER_STAGES = ((16, 16), (4, 40), (1, 100))
+
 # Kernel-aware pattern search on the benchmark's own example: four settings per
 # pattern around the workload's settings, at a budget of 10 % of the dense
 # causal attention FLOPs per head.
@@ -338,6 +342,8 @@ def main():
                     help="skip the kernel-aware pattern search measurement")
     ap.add_argument("--no-kv-select", action="store_true",
                     help="skip the KV-selection measurement (window score + keep set)")
+    ap.add_argument("--no-hier", action="store_true",
+                    help="skip the hierarchical-head measurement on the block-sparse heads")
     args = ap.parse_args()
     rank, local, world = dist_setup()
     if args.impl == "reference":
@@ -587,6 +593,38 @@ def main():
                  / (sum(kv_ms.values()) * 1e-3) / 1e12}
         del kvb
 
+    # ---- hierarchical pruning head (NEXT-3) on the step's block-sparse heads: the
+    # same inputs and attention work budget (the last stage keeps the block-sparse
+    # head's top-k), timed beside the block-sparse call (not part of the step)
+    hier = None
+    if not args.no_hier and rank == 0 and heads["bs"] and not heads["hip"]:
+        hstages = HIER_STAGES[:-1] + ((1, w.block_topk),)
+        hws = torch.empty(msa.workspace_bytes(msa.MSA_KIND_HIERARCHICAL, q, k, w.block_topk, 0,
+                                              len(heads["bs"])), dtype=torch.uint8, device=dev)
+        hcount = torch.empty(U_bs, (N + 63) // 64, dtype=torch.int32, device=dev)
+        hout = torch.zeros_like(q)
+        kw = dict(heads=heads["bs"], workspace=hws)
+        msa.msa_hierarchical(q, k, v, hstages, hout, export={"block_count": hcount}, **kw)
+        evh = new_events()
+        evb = new_events()
+        torch.cuda.synchronize()
+        msa.msa_hierarchical(q, k, v, hstages, hout, stage_events=evh, **kw)
+        msa.msa_block_sparse(q, k, v, w.block_topk, hout, heads=heads["bs"], workspace=ws["bs"],
+                             stage_events=evb)
+        torch.cuda.synchronize()
+        si, sp = msa.MSA_STAGE_INDEX, msa.MSA_STAGE_PREFILL
+        h_idx = evh[2 * si].elapsed_time(evh[2 * si + 1])
+        h_pf = evh[2 * sp].elapsed_time(evh[2 * sp + 1])
+        b_ms = evb[2 * si].elapsed_time(evb[2 * sp + 1])
+        h_flops = 4 * D * bs_pairs(hcount.cpu().numpy(), N)
+        hier = {"heads": len(heads["bs"]), "stages": [list(x) for x in hstages],
+                "index_ms": h_idx, "prefill_ms": h_pf, "ms": h_idx + h_pf,
+                "effective_tflops": h_flops / ((h_idx + h_pf) * 1e-3) / 1e12,
+                "prefill_tflops": h_flops / (h_pf * 1e-3) / 1e12,
+                "block_sparse_ms_same_heads": b_ms,
+                "device_status": msa.device_status(hws)}
+        del hws, hout
+
     # ---- kernel-aware pattern search (a separate measurement, not part of the step)
     psearch = None
     if not args.no_search and rank == 0:
@@ -638,6 +676,7 @@ def main():
             "dense_causal": dense,
             "device_status": status,
             "kv_select": kvsel,
+            "hierarchical": hier,
             "pattern_search": psearch,
         }
         print(json.dumps(line), flush=True)

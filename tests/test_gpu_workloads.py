@@ -39,6 +39,13 @@ def run_step(w, q, k, v, heads):
         msa.msa_block_sparse(q, k, v, w.block_topk, out, heads=heads["bs"], export=ex["bs"])
     if heads["st"]:
         msa.msa_streaming(q, k, v, w.init_num, w.local_window_num, out, heads=heads["st"])
+    if heads["hip"]:
+        U = B * len(heads["hip"])
+        NB = (N + 63) // 64
+        kb = min(w.hip_stages[-1][1], NB)
+        ex["hip"] = {"block_count": torch.empty(U, NB, dtype=torch.int32, device=q.device),
+                     "block_ids": torch.empty(U, NB, kb, dtype=torch.int32, device=q.device)}
+        msa.msa_hierarchical(q, k, v, w.hip_stages, out, heads=heads["hip"], export=ex["hip"])
     torch.cuda.synchronize()
     return out, {kind: {n: t.cpu().numpy() for n, t in d.items()} for kind, d in ex.items()}
 
@@ -49,17 +56,17 @@ def sample_rows(N, n, seed):
     return sorted(rows)
 
 
-ROWS = {"vs_32k": 48, "bs_64k": 48, "mixed_128k": 32, "vs_1m": 16}
+ROWS = {"vs_32k": 48, "bs_64k": 48, "mixed_128k": 32, "vs_1m": 16, "hip_64k": 32}
 
 
-@pytest.mark.parametrize("name", ["vs_32k", "bs_64k", "mixed_128k", "vs_1m"])
+@pytest.mark.parametrize("name", ["vs_32k", "bs_64k", "mixed_128k", "vs_1m", "hip_64k"])
 def test_workload_full_size(name):
     w, q, k, v, heads = inputs.make_workload(name, device="cuda")
     out, ex = run_step(w, q, k, v, heads)
     N, G = w.seq_len, w.n_q_heads // w.n_kv_heads
     scale = 1 / math.sqrt(D)
     rows = sample_rows(N, ROWS[name], w.seed)
-    kind_of = {h: kind for kind in ("vs", "bs", "st") for h in heads[kind]}
+    kind_of = {h: kind for kind in ("vs", "bs", "st", "hip") for h in heads[kind]}
     near_ties = 0
     for g in range(w.n_kv_heads):
         kn, vn = P.to_np(k[0, g]), P.to_np(v[0, g])
@@ -110,6 +117,17 @@ def test_workload_full_size(name):
                                                   f"{name} h{h} m{m}")
                     sel.append(got)
                 mask = O.block_mask_from_blocks(sel, N)
+            elif kind == "hip":
+                u = heads["hip"].index(h)
+                e = ex["hip"]
+                qn = P.to_np(q[0, h])  # pooled queries need every row of q
+                blocks = sorted({i // 64 for i in rows} | {0, (N + 63) // 64 - 1})
+                sel, nt = P.check_hip_blocks(e["block_count"][u], e["block_ids"][u], qn, kn,
+                                             w.hip_stages, blocks, f"{name} h{h}")
+                near_ties += nt
+                keys = lambda i, sel=sel: np.concatenate([np.arange(64 * n, min(N, 64 * n + 64))
+                                                          for n in sel[i // 64]])
+                mask = lambda m, keys=keys: np.isin(np.arange(N), keys(64 * m))
             else:
                 sel = [O.streaming_blocks(m, w.init_num, w.local_window_num) for m in range((N + 63) // 64)]
                 mask = O.block_mask_from_blocks(sel, N)
