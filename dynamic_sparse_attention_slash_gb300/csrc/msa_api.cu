@@ -150,8 +150,8 @@ constexpr size_t kStatusBytes = 256;
 
 struct VSLayout {
   int kv, ks, kv_pad, n_split, dist_words, chunk_words;
-  size_t vmax, partial, v_score, s_score, vertical, slash, tile_dist, qdelta, qdelta_count, col_chunks,
-      kc, vc, v16, total;
+  size_t vmax, partial, v_score, s_score, vertical, slash, tile_dist, qdelta, qdelta_count, e2,
+      e2_count, col_chunks, kc, vc, v16, total;
 };
 
 // Largest |v| per (batch, KV head), right after the status word; both are
@@ -195,6 +195,8 @@ VSLayout vs_layout(const Geometry& g, int64_t vertical_topk, int64_t slash) {
   L.tile_dist = c.take<uint32_t>(U * L.dist_words);
   L.qdelta = c.take<int32_t>(U * (g.NQ + 1));
   L.qdelta_count = c.take<int32_t>(U);
+  L.e2 = c.take<int32_t>(U * (g.NB + 2));
+  L.e2_count = c.take<int32_t>(U);
   L.col_chunks = c.take<uint32_t>(U * g.NQ * L.chunk_words);
   L.kc = c.take<__nv_bfloat16>(U * L.kv_pad * kHeadDim);
   L.vc = c.take<__half>(U * L.kv_pad * kHeadDim);
@@ -334,12 +336,13 @@ int make_map_f16(CUtensorMap* m, void* base, const Geometry& g, cuuint32_t box_r
   return make_map_4d(m, &t, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, box_rows);
 }
 
-int make_map_rows(CUtensorMap* m, void* base, int64_t rows, CUtensorMapDataType dtype) {
+int make_map_rows(CUtensorMap* m, void* base, int64_t rows, CUtensorMapDataType dtype,
+                  cuuint32_t box_rows = 128) {
   auto fn = encode_fn();
   if (!fn) return MSA_ERR_CUDA;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim * 2)};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t es[2] = {1, 1};
   const CUresult r = fn(m, dtype, 2, base, dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -403,6 +406,10 @@ cudaError_t run_kv_select(const Call& c, const msa_tensor* q, const msa_tensor* 
   tm.end(MSA_STAGE_KV_SELECT);
   return e;
 }
+
+// Whether a vertical-slash call runs on the one-tile kernel: when the chosen
+// offsets would cover under half of the 64-key bins on average (128 ks < N).
+bool vs_one_tile(int ks, int N) { return 128LL * ks < N; }
 
 // Every host-side check of a vertical-slash call that does not involve the
 // workspace; on MSA_OK, c and L describe the call.
@@ -480,12 +487,19 @@ int msa_vertical_slash(const msa_tensor* q, const msa_tensor* k, const msa_tenso
   if (s) return s;
   if ((s = check_workspace(c, L.total))) return s;
   void* ws = opts->workspace;
+  // Sparse tiles (slash lines cover under half the 64-key bins on average)
+  // run on the one-tile kernel, whose items pack 64-key blocks; denser ones
+  // on the two-tile kernel, which shares each 128-key tile between two query
+  // tiles.
+  const bool tile_kernel = vs_one_tile(L.ks, c.g.N);
   CUtensorMap mq, mk, mv, mkc, mvc;
   const int64_t crow = static_cast<int64_t>(c.g.n_units) * L.kv_pad;
-  if ((s = make_map_4d(&mq, q)) || (s = make_map_4d(&mk, k)) ||
-      (s = make_map_f16(&mv, at<void>(ws, L.v16), c.g)) ||
-      (s = make_map_rows(&mkc, at<void>(ws, L.kc), crow, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16)) ||
-      (s = make_map_rows(&mvc, at<void>(ws, L.vc), crow, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)))
+  const cuuint32_t box = tile_kernel ? 64 : 128;
+  if ((s = make_map_4d(&mq, q)) ||
+      (s = make_map_4d(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, box)) ||
+      (s = make_map_f16(&mv, at<void>(ws, L.v16), c.g, box)) ||
+      (s = make_map_rows(&mkc, at<void>(ws, L.kc), crow, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, box)) ||
+      (s = make_map_rows(&mvc, at<void>(ws, L.vc), crow, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, box)))
     return s;
   const StageTimer tm{opts->stage_events, c.st};
   int launches = 0;
@@ -513,6 +527,7 @@ int msa_vertical_slash(const msa_tensor* q, const msa_tensor* k, const msa_tenso
     e = launch_vs_index(c.g, c.u, view(k), at<__half>(ws, L.v16), at<int32_t>(ws, L.slash), L.ks,
                         at<int32_t>(ws, L.vertical), L.kv, at<uint32_t>(ws, L.tile_dist),
                         L.dist_words, at<int32_t>(ws, L.qdelta), at<int32_t>(ws, L.qdelta_count),
+                        at<int32_t>(ws, L.e2), at<int32_t>(ws, L.e2_count),
                         at<uint32_t>(ws, L.col_chunks), L.chunk_words,
                         at<__nv_bfloat16>(ws, L.kc), at<__half>(ws, L.vc), L.kv_pad,
                         at<uint32_t>(ws, 0), c.st, &launches);
@@ -529,8 +544,12 @@ int msa_vertical_slash(const msa_tensor* q, const msa_tensor* k, const msa_tenso
   p.vertical = at<int32_t>(ws, L.vertical);
   p.kv = L.kv;
   p.kv_pad = L.kv_pad;
+  p.vs_e2 = at<int32_t>(ws, L.e2);
+  p.vs_e2_count = at<int32_t>(ws, L.e2_count);
+  p.e2_stride = c.g.NB + 2;
   tm.begin(MSA_STAGE_PREFILL);
-  e = launch_prefill(p, mq, mk, mv, mkc, mvc, c.st, &launches);
+  e = tile_kernel ? launch_prefill_tile(p, mq, mk, mv, mkc, mvc, c.st, &launches)
+                  : launch_prefill(p, mq, mk, mv, mkc, mvc, c.st, &launches);
   tm.end(MSA_STAGE_PREFILL);
   if (e != cudaSuccess) return finish(e, launches);
   {
@@ -599,7 +618,7 @@ int msa_block_sparse(const msa_tensor* q, const msa_tensor* k, const msa_tensor*
   p.bs_tile_count = at<int32_t>(ws, L.tile_count);
   p.bs_tile_cap = L.tile_cap;
   tm.begin(MSA_STAGE_PREFILL);
-  e = launch_prefill_tile(p, mq, mk64, mv64, c.st, &launches);
+  e = launch_prefill_tile(p, mq, mk64, mv64, mk64, mv64, c.st, &launches);
   tm.end(MSA_STAGE_PREFILL);
   if (e != cudaSuccess) return finish(e, launches);
   {
@@ -668,7 +687,7 @@ int msa_hierarchical(const msa_tensor* q, const msa_tensor* k, const msa_tensor*
   p.bs_tile_count = at<int32_t>(ws, L.tile_count);
   p.bs_tile_cap = L.tile_cap;
   tm.begin(MSA_STAGE_PREFILL);
-  e = launch_prefill_tile(p, mq, mk64, mv64, c.st, &launches);
+  e = launch_prefill_tile(p, mq, mk64, mv64, mk64, mv64, c.st, &launches);
   tm.end(MSA_STAGE_PREFILL);
   if (e != cudaSuccess) return finish(e, launches);
   {

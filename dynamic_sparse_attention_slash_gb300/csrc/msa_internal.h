@@ -110,6 +110,12 @@ struct PrefillParams {
   int chunk_words;
   const int32_t* vertical;     // [units][kv] ascending chosen key columns
   int kv;                      // number of chosen columns
+  // vertical-slash on the one-tile kernel: per unit, the ascending distances
+  // d in [-1, NB] with d or d + 1 active, as (d + 1) << 2 | (bit 0: d active,
+  // bit 1: d + 1 active), and their count
+  const int32_t* vs_e2;        // [units][e2_stride]
+  const int32_t* vs_e2_count;  // [units]
+  int e2_stride;               // NB + 2
   int kv_pad;                  // rows per unit in the gathered K/V buffers (multiple of 128)
   // block-sparse plan
   const int32_t* bs_tiles;       // [units][NQ][bs_tile_cap][2] 64-key block | flags << 16
@@ -181,7 +187,8 @@ cudaError_t launch_kv_score(const Geometry& g, const UnitMap& u, TensorView q, T
 cudaError_t launch_vs_index(const Geometry& g, const UnitMap& u, TensorView k, const __half* v16,
                             const int32_t* slash, int ks, const int32_t* vertical, int kv,
                             uint32_t* tile_dist, int dist_words, int32_t* qdelta,
-                            int32_t* qdelta_count, uint32_t* col_chunks, int chunk_words,
+                            int32_t* qdelta_count, int32_t* e2, int32_t* e2_count,
+                            uint32_t* col_chunks, int chunk_words,
                             __nv_bfloat16* kc, __half* vc, int kv_pad, uint32_t* status,
                             cudaStream_t st, int* n_launch);
 // Export only: columns per row block of the vertical-slash format ([units][NB]).
@@ -220,11 +227,13 @@ cudaError_t launch_v_to_f16(TensorView v, const Geometry& g, const UnitMap& u, _
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                            const CUtensorMap& mv, const CUtensorMap& mkc, const CUtensorMap& mvc,
                            cudaStream_t st, int* n_launch);
-// One query tile per CTA, for block-sparse plans (launch_prefill routes them
-// here); any other kind returns cudaErrorInvalidValue.
-// Block-sparse heads: mk64 / mv64 map K and the f16 copy of v in 64-key boxes.
+// One query tile per CTA, for block-sparse plans and vertical-slash plans
+// (any other kind returns cudaErrorInvalidValue).  mk64 / mv64 map K and the
+// f16 copy of v in 64-key boxes; mkc64 / mvc64 the gathered column rows in
+// 64-row boxes (vertical-slash only; unused otherwise).
 cudaError_t launch_prefill_tile(const PrefillParams& p, const CUtensorMap& mq,
-                                const CUtensorMap& mk64, const CUtensorMap& mv64, cudaStream_t st,
-                                int* n_launch);
+                                const CUtensorMap& mk64, const CUtensorMap& mv64,
+                                const CUtensorMap& mkc64, const CUtensorMap& mvc64,
+                                cudaStream_t st, int* n_launch);
 
 }  // namespace msa

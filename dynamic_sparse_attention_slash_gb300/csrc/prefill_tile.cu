@@ -5,10 +5,14 @@
 // modification", Fig. 7: keep a running row max and row sum, rescale the output,
 // divide by the row sum at the end).
 //
-// This kernel serves the block-sparse heads: one CTA computes one 128-row
-// query tile p of one (batch, head) unit (row blocks 2p and 2p + 1).  It walks
-// the tile's item list that bs_index.cu builds: the blocks kept by either row
-// block, ascending, two 64-key blocks to an item.  The two blocks of an item
+// This kernel serves the block-sparse and hierarchical heads, and
+// vertical-slash heads whose tiles are sparse (few slash lines for the
+// length): one CTA computes one 128-row query tile p of one (batch, head)
+// unit (row blocks 2p and 2p + 1).  It walks the tile's items: for
+// block-sparse plans the list bs_index.cu builds (the blocks kept by either
+// row block, ascending, two 64-key blocks to an item); for vertical-slash
+// plans the tile's column chunks, then the blocks either row block admits,
+// derived from one per-unit list of active distances (see Tile).  The two blocks of an item
 // need not be adjacent, so an item wastes at most the quadrants of a block that
 // only one row block kept (on synthetic top-100 heads at 128K: 56 % of the
 // computed 64 x 64 quadrants are kept blocks, against 32 % with items of
@@ -70,61 +74,144 @@ struct __align__(1024) TileSmem {
 };
 
 struct Item {
+  bool cols;    // vertical-slash column chunk (gathered keys) instead of key blocks
+  int idx;      // the column chunk
   int blk[2];   // 64-key block of key half 0 and 1
   uint32_t qm;  // quadrant mask (bit a*2 + b: row half a sees key half b)
 };
 
-// The query tile of a CTA and its block-sparse item list: entry i is two
-// int32 slots, one per key half, each blk | flags << 16 (flag bit a: row
-// block 2p + a kept the block).
+// The query tile p of a CTA and its items.
+//  * block-sparse: the tile's item list; entry i is two int32 slots, one per
+//    key half, each blk | flags << 16 (flag bit a: row block 2p + a kept it).
+//  * vertical-slash (low tile density): the tile's column chunks (bit c of its
+//    col_chunks words: positions [128c, 128c + 128) of the vertical list),
+//    then the 64-key blocks of the unit's distance list e2, two to an item.
+//    An entry (d + 1) << 2 | flags stands for block n = 2p - d, with flag bit
+//    0 set iff tile distance d is active (row block 2p admits n) and bit 1 iff
+//    d + 1 is (row block 2p + 1 admits n); the entries with
+//    max(-1, 2p - NB + 1) <= d <= 2p belong to tile p, taken in descending d
+//    (ascending n).  Flags and the causal cut are those of block-sparse items.
 struct Tile {
   int n;  // items
-  const int32_t* list;
+  const int32_t* list;        // block-sparse
+  int n_chunks;               // vertical-slash
+  const uint32_t* chunks;
+  const int32_t* e2;
+  int j_hi, j_lo;             // e2 entries [j_lo, j_hi) belong to the tile
 };
 
+template <int kKind>
 __device__ __forceinline__ Tile make_tile(const PrefillParams& P, int unit, int p) {
   const int64_t t = static_cast<int64_t>(unit) * P.g.NQ + p;
   Tile T;
-  T.n = MSA_COUNT(P.bs_tile_count[t], P.bs_tile_cap, P.status);
-  T.list = P.bs_tiles + t * P.bs_tile_cap * 2;
+  if (kKind == kPrefillBS) {
+    T.n = MSA_COUNT(P.bs_tile_count[t], P.bs_tile_cap, P.status);
+    T.list = P.bs_tiles + t * P.bs_tile_cap * 2;
+    return T;
+  }
+  T.chunks = P.col_chunks + t * P.chunk_words;
+  T.n_chunks = 0;
+  for (int x = 0; x < P.chunk_words; ++x) T.n_chunks += __popc(T.chunks[x]);
+  T.e2 = P.vs_e2 + static_cast<int64_t>(unit) * P.e2_stride;
+  const int cnt = MSA_COUNT(P.vs_e2_count[unit], P.e2_stride, P.status);
+  // entries ascending by d: first with d >= d_lo, first with d > 2p
+  const int d_lo = max(-1, 2 * p - P.g.NB + 1);
+  auto first_above = [&](int d) {  // first entry with distance > d
+    int lo = 0, hi = cnt;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if ((T.e2[mid] >> 2) - 1 <= d) lo = mid + 1; else hi = mid;
+    }
+    return lo;
+  };
+  T.j_lo = first_above(d_lo - 1);
+  T.j_hi = first_above(2 * p);
+  T.n = T.n_chunks + (T.j_hi - T.j_lo + 1) / 2;
   return T;
 }
 
-__device__ __forceinline__ Item get_item(const PrefillParams& P, const Tile& T, int i) {
-  const int32_t s0 = T.list[2 * i], s1 = T.list[2 * i + 1];
-  const uint32_t f0 = static_cast<uint32_t>(s0 >> 16) & 3u, f1 = static_cast<uint32_t>(s1 >> 16) & 3u;
+template <int kKind>
+__device__ __forceinline__ Item get_item(const PrefillParams& P, const Tile& T, int i, int p) {
   Item it;
-  it.blk[0] = MSA_IDX(s0 & 0xffff, 0, P.g.NB, P.status);
-  it.blk[1] = MSA_IDX(s1 & 0xffff, 0, P.g.NB, P.status);
+  it.cols = false;
+  it.idx = 0;
+  if (kKind == kPrefillBS) {
+    const int32_t s0 = T.list[2 * i], s1 = T.list[2 * i + 1];
+    const uint32_t f0 = static_cast<uint32_t>(s0 >> 16) & 3u, f1 = static_cast<uint32_t>(s1 >> 16) & 3u;
+    it.blk[0] = MSA_IDX(s0 & 0xffff, 0, P.g.NB, P.status);
+    it.blk[1] = MSA_IDX(s1 & 0xffff, 0, P.g.NB, P.status);
+    it.qm = (f0 & 1u) | ((f1 & 1u) << 1) | ((f0 >> 1) << 2) | ((f1 >> 1) << 3);
+    return it;
+  }
+  if (i < T.n_chunks) {  // the (i+1)-th set chunk bit, ascending
+    int seen = 0;
+    for (int x = 0; x < P.chunk_words; ++x) {
+      uint32_t word = T.chunks[x];
+      const int cnt = __popc(word);
+      if (seen + cnt > i) {
+        for (int skip = i - seen; skip > 0; --skip) word &= word - 1;
+        it.cols = true;
+        it.idx = MSA_IDX(32 * x + (__ffs(word) - 1), 0, (P.kv + 127) / 128, P.status);
+        break;
+      }
+      seen += cnt;
+    }
+    it.blk[0] = it.blk[1] = 0;
+    it.qm = 0xFu;
+    return it;
+  }
+  const int t = i - T.n_chunks;
+  const int j0 = T.j_hi - 1 - 2 * t, j1 = j0 - 1;
+  const int32_t e0 = T.e2[MSA_IDX(j0, 0, P.e2_stride, P.status)];
+  const int32_t e1 = j1 >= T.j_lo ? T.e2[j1] : e0;
+  const bool second_row_block = 2 * p + 1 < P.g.NB;
+  uint32_t f0 = static_cast<uint32_t>(e0) & 3u, f1 = j1 >= T.j_lo ? static_cast<uint32_t>(e1) & 3u : 0u;
+  if (!second_row_block) {
+    f0 &= 1u;
+    f1 &= 1u;
+  }
+  it.blk[0] = MSA_IDX(2 * p - ((e0 >> 2) - 1), 0, P.g.NB, P.status);
+  it.blk[1] = MSA_IDX(2 * p - ((e1 >> 2) - 1), 0, P.g.NB, P.status);
   it.qm = (f0 & 1u) | ((f1 & 1u) << 1) | ((f0 >> 1) << 2) | ((f1 >> 1) << 3);
   return it;
 }
 
-// TMA of the item's K (or V) rows into dst, completion on bar: keys of block
-// blk[h] are rows [64h, 64h + 64) of the 128-row tile (both 64-column halves).
+// TMA of the item's K (or V) rows into dst, completion on bar: keys of key
+// half h are rows [64h, 64h + 64) of the 128-row tile (both 64-column
+// halves): block blk[h] of the KV head, or for a column chunk c the gathered
+// rows [128c + 64h, +64) of the unit.
 __device__ __forceinline__ void load_item(const Item& it, uint8_t* dst, const CUtensorMap* map64,
-                                          uint64_t* bar, int hkv, int b) {
+                                          const CUtensorMap* mapc64, uint64_t* bar, int hkv,
+                                          int b, int crow0) {
   mbar_arrive_expect_tx(bar, kTileBytes);
 #pragma unroll
   for (int hd = 0; hd < 2; ++hd)
 #pragma unroll
-    for (int kh = 0; kh < 2; ++kh)
-      tma_load_4d(dst + hd * kHalfBytes + kh * (kHalfBytes / 2), map64, bar, 64 * hd,
-                  64 * it.blk[kh], hkv, b);
+    for (int kh = 0; kh < 2; ++kh) {
+      uint8_t* d = dst + hd * kHalfBytes + kh * (kHalfBytes / 2);
+      if (it.cols)
+        tma_load_2d(d, mapc64, bar, 64 * hd, crow0 + 128 * it.idx + 64 * kh);
+      else
+        tma_load_4d(d, map64, bar, 64 * hd, 64 * it.blk[kh], hkv, b);
+    }
 }
 
+template <int kKind>
 __global__ void __launch_bounds__(kThreads, 1)
 sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ CUtensorMap mq,
                            const __grid_constant__ CUtensorMap mk64,
-                           const __grid_constant__ CUtensorMap mv64) {
+                           const __grid_constant__ CUtensorMap mv64,
+                           const __grid_constant__ CUtensorMap mkc64,
+                           const __grid_constant__ CUtensorMap mvc64) {
   extern __shared__ uint8_t smem_raw[];
   TileSmem& sm = *reinterpret_cast<TileSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int unit = blockIdx.y;
   const int p = P.g.NQ - 1 - static_cast<int>(blockIdx.x);  // heavy (late) tiles first
-  const Tile T = make_tile(P, unit, p);
+  const Tile T = make_tile<kKind>(P, unit, p);
   const int b = unit_batch(P, unit), h = unit_head(P, unit), hkv = h / P.g.G;
+  const int crow0 = unit * P.kv_pad;  // the unit's gathered column rows (vertical-slash)
   volatile int* abort = &sm.abort;
 
   if (tid == 0) {
@@ -159,6 +246,7 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
     if (lane == 0) {
       tma_prefetch_desc(&mq);
       tma_prefetch_desc(&mk64);
+      if (kKind == kPrefillVS) tma_prefetch_desc(&mkc64);
       mbar_arrive_expect_tx(&sm.q_full, kTileBytes);
       tma_load_4d(sm.q, &mq, &sm.q_full, 0, 128 * p, h, b);
       tma_load_4d(sm.q + kHalfBytes, &mq, &sm.q_full, 64, 128 * p, h, b);
@@ -166,7 +254,8 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
       for (int i = 0; i < T.n; ++i) {
         const int st = i % kStagesK;
         if (!mbar_wait(&sm.k_empty[st], ((i / kStagesK) & 1) ^ 1, abort)) break;
-        load_item(get_item(P, T, i), sm.k[st], &mk64, &sm.k_full[st], hkv, b);
+        load_item(get_item<kKind>(P, T, i, p), sm.k[st], &mk64, &mkc64, &sm.k_full[st], hkv, b,
+                  crow0);
         issued = i + 1;
       }
       // drain: the latest load of every stage, and Q, must land before exit
@@ -178,11 +267,13 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
     // ------------------------------------------------------------ V producer
     if (lane == 0) {
       tma_prefetch_desc(&mv64);
+      if (kKind == kPrefillVS) tma_prefetch_desc(&mvc64);
       int issued = 0;
       for (int i = 0; i < T.n; ++i) {
         const int st = i % kStagesV;
         if (!mbar_wait(&sm.v_empty[st], ((i / kStagesV) & 1) ^ 1, abort)) break;
-        load_item(get_item(P, T, i), sm.v[st], &mv64, &sm.v_full[st], hkv, b);
+        load_item(get_item<kKind>(P, T, i, p), sm.v[st], &mv64, &mvc64, &sm.v_full[st], hkv, b,
+                  crow0);
         issued = i + 1;
       }
       for (int i = max(0, issued - kStagesV); i < issued; ++i)
@@ -263,7 +354,7 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
     bool ok = true;
     int k = 0;  // items processed so far
     for (; k < T.n;) {
-      const Item it = get_item(P, T, k);
+      const Item it = get_item<kKind>(P, T, k, p);
       const uint32_t s_col = lane_base + kColS + 128 * (k & 1);
       // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
       const bool waited = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[k & 1], (k >> 1) & 1, abort));
@@ -282,7 +373,23 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
 #pragma unroll
           for (int e = 0; e < 64; ++e) x[e] = __uint_as_float(raw[e]);
         }
-        if (lim < 63) {
+        if (kKind == kPrefillVS && it.cols) {
+          // chosen key j of the gathered chunk: admitted iff j <= row and its
+          // 64x64 tile is not active for this row block (the tile covers it)
+          const int s0 = 128 * it.idx + 64 * g;
+          const int32_t* V = P.vertical + static_cast<int64_t>(unit) * P.kv + s0;
+          const uint32_t* dist = P.tile_dist + static_cast<int64_t>(unit) * P.dist_words;
+          const int mblk = 2 * p + half;
+#pragma unroll
+          for (int e = 0; e < 64; ++e) {
+            bool keep = false;
+            if (s0 + e < P.kv) {
+              const int j = MSA_IDX(V[e], 0, P.g.N, P.status);
+              keep = j <= row && !dist_bit_checked(P, dist, mblk - (j >> 6));
+            }
+            if (!keep) x[e] = -INFINITY;
+          }
+        } else if (lim < 63) {
 #pragma unroll
           for (int e = 0; e < 64; ++e)
             if (e > lim) x[e] = -INFINITY;
@@ -442,15 +549,17 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
 }  // namespace
 
 cudaError_t launch_prefill_tile(const PrefillParams& p, const CUtensorMap& mq,
-                                const CUtensorMap& mk64, const CUtensorMap& mv64, cudaStream_t st,
-                                int* n_launch) {
+                                const CUtensorMap& mk64, const CUtensorMap& mv64,
+                                const CUtensorMap& mkc64, const CUtensorMap& mvc64,
+                                cudaStream_t st, int* n_launch) {
   const int smem = static_cast<int>(sizeof(TileSmem)) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(sparse_prefill_tile_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (p.kind != kPrefillBS && p.kind != kPrefillVS) return cudaErrorInvalidValue;
+  auto kernel = p.kind == kPrefillBS ? sparse_prefill_tile_kernel<kPrefillBS>
+                                     : sparse_prefill_tile_kernel<kPrefillVS>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  if (p.kind != kPrefillBS) return cudaErrorInvalidValue;  // block-sparse tile lists only
   if (p.g.n_units == 0 || p.g.NQ == 0) return cudaSuccess;
-  sparse_prefill_tile_kernel<<<dim3(p.g.NQ, p.g.n_units), kThreads, smem, st>>>(p, mq, mk64, mv64);
+  kernel<<<dim3(p.g.NQ, p.g.n_units), kThreads, smem, st>>>(p, mq, mk64, mv64, mkc64, mvc64);
   e = cudaGetLastError();
   if (e == cudaSuccess) ++*n_launch;
   return e;

@@ -16,6 +16,9 @@
 //    and 2E+1; query tile pB sees key tile q at E = D and pA at E = D - 1.
 //    Entries are (D << 5) | bits 2D-3 .. 2D+1 of tile_dist, the bits that the
 //    quadrant masks of both query tiles read.
+//  * e2: for the one-tile kernel (used when the tiles are sparse), the
+//    ascending distances d in [-1, NB] with d or d + 1 active: query tile p
+//    (row blocks 2p, 2p + 1) sees 64-key block 2p - d at distances d and d + 1.
 //  * col_chunks: per 128-row query tile p, bit c is set iff some chosen key in
 //    positions [128c, 128c+128) of the ascending vertical list is needed as a
 //    column by row block 2p or 2p+1, i.e. lies at or before the block's last
@@ -34,7 +37,7 @@ constexpr int kTilesThreads = 512;
 __global__ void __launch_bounds__(kTilesThreads) vs_tile_dist_kernel(
     const int32_t* __restrict__ slash, int ks, int N, int NB, int NQ, uint32_t* __restrict__ tile_dist,
     int dist_words, int32_t* __restrict__ qdelta, int32_t* __restrict__ qdelta_count,
-    uint32_t* status) {
+    int32_t* __restrict__ e2, int32_t* __restrict__ e2_count, uint32_t* status) {
   extern __shared__ uint32_t bits[];
   __shared__ int warp_sums[kTilesThreads / 32 + 1];
   const int unit = blockIdx.x, tid = threadIdx.x;
@@ -65,6 +68,19 @@ __global__ void __launch_bounds__(kTilesThreads) vs_tile_dist_kernel(
     written += total;
   }
   if (tid == 0) qdelta_count[unit] = written;
+  // e2: distances d in [-1, NB] for the one-tile kernel's query tiles (row
+  // blocks 2p and 2p + 1 see block 2p - d at distances d and d + 1)
+  int32_t* ed = e2 + static_cast<int64_t>(unit) * (NB + 2);
+  written = 0;
+  for (int base = -1; base <= NB; base += kTilesThreads) {
+    const int d = base + tid;
+    const int flags = d <= NB ? (bit(d) ? 1 : 0) | (bit(d + 1) ? 2 : 0) : 0;
+    int total;
+    const int pos = block_exclusive_scan<kTilesThreads>(flags ? 1 : 0, warp_sums, &total);
+    if (flags) ed[MSA_IDX(written + pos, 0, NB + 2, status)] = ((d + 1) << 2) | flags;
+    written += total;
+  }
+  if (tid == 0) e2_count[unit] = written;
 }
 
 // One warp per (unit, query tile p, 32-chunk word).
@@ -187,7 +203,8 @@ cudaError_t launch_vs_col_count(const Geometry& g, const int32_t* vertical, int 
 cudaError_t launch_vs_index(const Geometry& g, const UnitMap& u, TensorView k, const __half* v16,
                             const int32_t* slash, int ks, const int32_t* vertical, int kv,
                             uint32_t* tile_dist, int dist_words, int32_t* qdelta,
-                            int32_t* qdelta_count, uint32_t* col_chunks, int chunk_words,
+                            int32_t* qdelta_count, int32_t* e2, int32_t* e2_count,
+                            uint32_t* col_chunks, int chunk_words,
                             __nv_bfloat16* kc, __half* vc, int kv_pad, uint32_t* status,
                             cudaStream_t st, int* n_launch) {
   cudaError_t e;
@@ -198,7 +215,7 @@ cudaError_t launch_vs_index(const Geometry& g, const UnitMap& u, TensorView k, c
   }
   vs_tile_dist_kernel<<<g.n_units, kTilesThreads, smem, st>>>(slash, ks, g.N, g.NB, g.NQ, tile_dist,
                                                              dist_words, qdelta, qdelta_count,
-                                                             status);
+                                                             e2, e2_count, status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   ++*n_launch;
   const int64_t warps = static_cast<int64_t>(g.n_units) * g.NQ * chunk_words;

@@ -246,6 +246,42 @@ def test_vertical_slash_batch_and_head_subset():
     check_vs_case(q, k, v, 100, 150, heads=[2, 1])
 
 
+@pytest.mark.parametrize("N,kv,ks", [(4096, 200, 20), (2112, 130, 10), (8192, 300, 50),
+                                     (1217, 50, 5), (4160, 1, 1)])
+def test_vertical_slash_sparse_tiles_one_tile_kernel(N, kv, ks):
+    """Few slash lines for the length (128 * slash < N): the call runs on the
+    one-query-tile kernel with packed 64-key block items and 64-key column
+    halves; scores, sets, the exact format and the outputs against the oracle,
+    including a ragged length and a single line of each kind."""
+    assert 128 * ks < N
+    q, k, v = qkv(1, 4, 2, N, 23)
+    check_vs_case(q, k, v, kv, ks)
+
+
+def test_vertical_slash_one_tile_kernel_batch_subset_and_normalisers():
+    """The one-tile vertical-slash path with a batch of two, a head subset and
+    the row normalisers (lse) against the oracle's over the GPU's own sets."""
+    N, kv, ks, heads = 2176, 90, 8, [3, 0]
+    q, k, v = qkv(2, 4, 2, N, 24)
+    check_vs_case(q, k, v, kv, ks, heads=heads)
+    kvb = msa.kv_select_buffers(q, 64, 16)
+    out, ex = P.run_vs(q, k, v, kv, ks, heads=heads)
+    msa.msa_vertical_slash(q, k, v, kv, ks, heads=heads, kv_select=kvb)
+    torch.cuda.synchronize()
+    qn, kn = np64(q), np64(k)
+    for b in range(2):
+        for t, h in enumerate(heads):
+            u = b * len(heads) + t
+            V, S = ex["vertical"][u].astype(np.int64), ex["slash"][u].astype(np.int64)
+            act = O.vs_active_tiles(S, N)
+            mask = O.vs_block_mask(act, O.vs_columns(V, act, N), N)
+            ref = O.row_lse(qn[b, h], kn[b, h // 2], np.arange(N), mask, 1 / math.sqrt(D))
+            got = kvb["lse"][b, h].double().cpu().numpy()
+            fin = np.isfinite(ref)
+            assert (np.isneginf(got) == ~fin).all()
+            assert np.abs(got[fin] - ref[fin]).max() <= 1e-4
+
+
 def test_vertical_topk_covering_all_keys_is_dense():
     q, k, v = qkv(1, 2, 1, 1152, 17)
     out, _ = P.run_vs(q, k, v, 5000, 2)
