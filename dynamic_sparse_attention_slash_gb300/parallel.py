@@ -7,7 +7,10 @@ groups so that each GPU holds only its own K/V heads, as tensor-parallel
 attention splits heads (the Novita vLLM article confines sparsity to each
 tensor-parallel rank for the same reason).  There is no communication inside
 the operation; an optional all-gather afterwards gives every rank the full
-output.
+output.  sharded_attention works on full-size tensors of which each rank reads
+and writes its heads only; sharded_attention_local works on rank-local
+tensors (each rank holds only its heads' q, k, v and out: the memory is
+sharded too).
 """
 from __future__ import annotations
 
@@ -53,20 +56,73 @@ def sharded_attention(call: Callable[..., object], q, k, v, out, *, gather: bool
     return heads
 
 
-def _gather_heads(out, Hq: int, Hkv: int, world: int, group: Optional[object]) -> None:
-    """All-gather of the head shards of out [B, Hq, N, D] (shards may differ in
-    size by one KV-head group: they are padded to the largest for the exchange)."""
+def local_head_range(n_q_heads: int, n_kv_heads: int, world: int, rank: int):
+    """(query-head range, KV-head range) of `rank` as (start, stop) pairs: the
+    slices of q/out and k/v a rank needs to hold (whole KV-head groups)."""
+    heads = shard_heads(n_q_heads, n_kv_heads, world, rank)
+    G = n_q_heads // n_kv_heads
+    if not heads:
+        return (0, 0), (0, 0)
+    return (heads[0], heads[-1] + 1), (heads[0] // G, heads[-1] // G + 1)
+
+
+def sharded_attention_local(call: Callable[..., object], q_loc, k_loc, v_loc, out_loc=None, *,
+                            gather: bool = False, n_q_heads: Optional[int] = None,
+                            n_kv_heads: Optional[int] = None, group=None):
+    """Runs call(q_loc, k_loc, v_loc, out=out_loc) on rank-local tensors.
+
+    Memory-sharded form: each rank holds only its own heads, q_loc / out_loc
+    [B, Hq_loc, N, D] and k_loc / v_loc [B, Hkv_loc, N, D] (the slices that
+    local_head_range names, e.g. loaded from the rank's part of a checkpoint),
+    and the call runs on all of the local heads.  With gather=True the shards
+    are all-gathered and the full output [B, n_q_heads, N, D] is returned
+    (n_q_heads and n_kv_heads are the totals over all ranks); otherwise the
+    local output.
+    """
+    if out_loc is None:
+        out_loc = torch.zeros_like(q_loc)
+    if q_loc.shape[1]:
+        call(q_loc, k_loc, v_loc, out=out_loc)
+    if not gather:
+        return out_loc
+    if n_q_heads is None or n_kv_heads is None:
+        raise ValueError("gather needs the total numbers of query and KV heads")
+    import torch.distributed as dist
+    world = dist.get_world_size(group) if dist.is_available() and dist.is_initialized() else 1
+    if world == 1:
+        return out_loc
+    B, _, N, D = out_loc.shape
+    full = torch.empty((B, n_q_heads, N, D), dtype=out_loc.dtype, device=out_loc.device)
+    _exchange(out_loc, full, n_q_heads, n_kv_heads, world, dist.get_rank(group), group)
+    return full
+
+
+def _exchange(mine_heads, full, Hq: int, Hkv: int, world: int, rank: int,
+              group: Optional[object]) -> None:
+    """All-gather of head shards into full [B, Hq, N, D].  Equal shards are
+    gathered as they are; unequal ones (Hkv not a multiple of world) are padded
+    to the largest for the exchange."""
     import torch.distributed as dist
     shards = [shard_heads(Hq, Hkv, world, r) for r in range(world)]
     width = max(len(s) for s in shards)
-    B, _, N, D = out.shape
-    rank = dist.get_rank(group)
-    mine = torch.zeros((B, width, N, D), dtype=out.dtype, device=out.device)
-    h = shards[rank]
-    if h:
-        mine[:, : len(h)] = out[:, h[0]: h[-1] + 1]
+    B, _, N, D = full.shape
+    if all(len(s) == width for s in shards):
+        mine = mine_heads.contiguous()
+    else:
+        mine = torch.zeros((B, width, N, D), dtype=full.dtype, device=full.device)
+        mine[:, : mine_heads.shape[1]] = mine_heads
     parts = [torch.empty_like(mine) for _ in range(world)]
     dist.all_gather(parts, mine, group=group)
     for r, s in enumerate(shards):
         if s:
-            out[:, s[0]: s[-1] + 1] = parts[r][:, : len(s)]
+            full[:, s[0]: s[-1] + 1] = parts[r][:, : len(s)]
+
+
+def _gather_heads(out, Hq: int, Hkv: int, world: int, group: Optional[object]) -> None:
+    """All-gather of the head shards of out [B, Hq, N, D] (shards may differ in
+    size by one KV-head group: they are padded to the largest for the exchange)."""
+    import torch.distributed as dist
+    rank = dist.get_rank(group)
+    h = shard_heads(Hq, Hkv, world, rank)
+    mine = out[:, h[0]: h[-1] + 1] if h else out[:, :0]
+    _exchange(mine, out, Hq, Hkv, world, rank, group)

@@ -1,9 +1,11 @@
 // Calling libmsa from C++ without Python: builds q [1, 4, N, 128] and k, v
 // [1, 2, N, 128] in device memory, runs vertical-slash attention on query
 // heads 0 and 1, block-sparse on head 2 and streaming on head 3 into one
-// output tensor, each call with its own workspace sized by the library, then
-// checks the host status codes, the device status words and that every
-// output value was written and is finite.  Exits 0 on success.
+// output tensor, each call with its own workspace sized by the library; then
+// the hierarchical pruning head on all four heads into a second output, and
+// the workspace-free vertical-slash call into a third.  It checks the host
+// status codes, the device status words and that every output value was
+// written and is finite.  Exits 0 on success.
 //
 //   nvcc -std=c++17 -I include include/msa_example.cu \
 //        -L dynamic_sparse_attention_slash_gb300 -l:libmsa.so \
@@ -54,14 +56,16 @@ int main() {
   for (auto& x : hk) x = __float2bfloat16(rnd());
   for (auto& x : hv) x = __float2bfloat16(rnd());
 
-  void *dq, *dk, *dv, *dout;
+  void *dq, *dk, *dv, *dout, *dout2, *dout3;
   if (cudaMalloc(&dq, nq * 2) || cudaMalloc(&dk, nk * 2) || cudaMalloc(&dv, nk * 2) ||
-      cudaMalloc(&dout, nq * 2))
+      cudaMalloc(&dout, nq * 2) || cudaMalloc(&dout2, nq * 2) || cudaMalloc(&dout3, nq * 2))
     return 1;
   cudaMemcpy(dq, hq.data(), nq * 2, cudaMemcpyHostToDevice);
   cudaMemcpy(dk, hk.data(), nk * 2, cudaMemcpyHostToDevice);
   cudaMemcpy(dv, hv.data(), nk * 2, cudaMemcpyHostToDevice);
   cudaMemset(dout, 0xff, nq * 2);  // NaN pattern: every value must be overwritten
+  cudaMemset(dout2, 0xff, nq * 2);
+  cudaMemset(dout3, 0xff, nq * 2);
 
   msa_tensor tq = view(dq, B, Hq, N), tk = view(dk, B, Hkv, N), tv = view(dv, B, Hkv, N),
              tout = view(dout, B, Hq, N);
@@ -92,14 +96,34 @@ int main() {
   o.workspace_bytes = need[2];
   if (!ok(msa_streaming(&tq, &tk, &tv, init_num, local, &tout, &o), "streaming")) return 1;
 
+  // hierarchical pruning on every head: chunks of 8, 2 and 1 blocks keeping 4, 6, 8
+  msa_tensor tout2 = view(dout2, B, Hq, N);
+  const msa_hip_stage stages[3] = {{8, 4}, {2, 6}, {1, 8}};
+  const size_t need_hip = msa_workspace_bytes(MSA_KIND_HIERARCHICAL, &tq, &tk, 8, 0, 0);
+  void* ws_hip;
+  if (need_hip == 0 || cudaMalloc(&ws_hip, need_hip)) return 1;
+  msa_opts oh = {};
+  oh.workspace = ws_hip;
+  oh.workspace_bytes = need_hip;
+  if (!ok(msa_hierarchical(&tq, &tk, &tv, stages, 3, &tout2, &oh), "hierarchical")) return 1;
+  // vertical-slash with the library's own scratch array (no workspace)
+  msa_tensor tout3 = view(dout3, B, Hq, N);
+  if (!ok(msa_vertical_slash_static(&tq, &tk, &tv, vertical_topk, slash, &tout3, nullptr),
+          "vertical-slash (static scratch)"))
+    return 1;
+
   for (int i = 0; i < 3; ++i)  // synchronises; a bounded wait that ran out would show here
     if (!ok(msa_device_status(ws[i], nullptr), "device status")) return 1;
-  cudaMemcpy(hout.data(), dout, nq * 2, cudaMemcpyDeviceToHost);
-  for (size_t i = 0; i < nq; ++i)
-    if (!std::isfinite(__bfloat162float(hout[i]))) {
-      std::fprintf(stderr, "output value %zu not written\n", i);
-      return 1;
-    }
+  if (!ok(msa_device_status(ws_hip, nullptr), "device status (hierarchical)")) return 1;
+  if (!ok(msa_vertical_slash_static_status(nullptr), "device status (static scratch)")) return 1;
+  for (void* d : {dout, dout2, dout3}) {
+    cudaMemcpy(hout.data(), d, nq * 2, cudaMemcpyDeviceToHost);
+    for (size_t i = 0; i < nq; ++i)
+      if (!std::isfinite(__bfloat162float(hout[i]))) {
+        std::fprintf(stderr, "output value %zu not written\n", i);
+        return 1;
+      }
+  }
   std::printf("msa_example ok: %lld kernel launches\n",
               static_cast<long long>(msa_kernel_launches()));
   return 0;

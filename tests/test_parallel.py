@@ -74,3 +74,52 @@ def test_gloo_ranks_gather_the_full_output(world):
         assert mine == seen
         all_heads += mine
     assert sorted(all_heads) == list(range(12))
+
+
+def _local_worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import torch.distributed as dist
+    from dynamic_sparse_attention_slash_gb300.parallel import (local_head_range,
+                                                               sharded_attention_local)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    B, Hq, Hkv, N, D = 2, 12, 3, 8, 4
+    (h0, h1), (g0, g1) = local_head_range(Hq, Hkv, world, rank)
+    # every rank builds only its own heads: q holds the head id, k the KV head id
+    q_loc = torch.arange(h0, h1).float().view(1, -1, 1, 1).expand(B, -1, N, D).contiguous()
+    k_loc = torch.arange(g0, g1).float().view(1, -1, 1, 1).expand(B, -1, N, D).contiguous()
+
+    def fake_call(q_, k_, v_, out):
+        G = q_.shape[1] // k_.shape[1]
+        kk = k_.repeat_interleave(G, dim=1)
+        out.copy_(100.0 * q_ + kk + torch.arange(B).view(B, 1, 1, 1).float())
+
+    full = sharded_attention_local(fake_call, q_loc, k_loc, k_loc, gather=True, n_q_heads=Hq,
+                                   n_kv_heads=Hkv)
+    want = (100.0 * torch.arange(Hq).view(1, Hq, 1, 1) + (torch.arange(Hq) // (Hq // Hkv)).view(
+        1, Hq, 1, 1) + torch.arange(B).view(B, 1, 1, 1)).float().expand(B, Hq, N, D)
+    ok = bool(torch.equal(full, want))
+    dist.destroy_process_group()
+    q.put((rank, h1 - h0, g1 - g0, ok))
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_gloo_ranks_with_local_shards_gather_the_full_output(world):
+    """Memory-sharded form: each rank holds only its heads' tensors (whole
+    KV-head groups); after the exchange every rank holds the full output,
+    with unequal shards (3 KV heads over 2 ranks) and equal ones (3 over 3)."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_local_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert sum(r[1] for r in res) == 12 and sum(r[2] for r in res) == 3
+    for rank, nq, nk, ok in res:
+        assert ok, f"rank {rank} does not hold the full output"
+        assert nq == 4 * nk
