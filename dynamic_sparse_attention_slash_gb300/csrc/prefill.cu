@@ -410,16 +410,22 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
           for (int e = 0; e < 128; ++e) x[e] = __uint_as_float(raw[e]);
         }
         if (it.cols) {
-          const int32_t* V = P.vertical + static_cast<int64_t>(unit) * P.kv + 128 * it.idx;
-          const int valid = min(128, P.kv - 128 * it.idx);
+          // the warp's admission bits for the chunk's 128 keys (column_bits);
+          // a key of the row's own block also needs j <= row
+          uint32_t adm[4], own[4];
+          int jv[4];
+          column_bits<4>(P, P.vertical + static_cast<int64_t>(unit) * P.kv, 128 * it.idx, dist,
+                         mblk, adm, own, jv);
 #pragma unroll
-          for (int e = 0; e < 128; ++e) {
-            bool keep = false;
-            if (e < valid) {
-              const int j = MSA_IDX(V[e], 0, P.g.N, P.status);
-              keep = j <= row && !dist_bit_checked(P, dist, mblk - (j >> 6));
+          for (int q = 0; q < 4; ++q) {
+            uint32_t keep = adm[q];
+            for (uint32_t ob = own[q]; ob; ob &= ob - 1) {  // warp-uniform: own[q] is a ballot
+              const int bit = __ffs(static_cast<int>(ob)) - 1;
+              if (__shfl_sync(0xffffffffu, jv[q], bit) <= row) keep |= 1u << bit;
             }
-            if (!keep) x[e] = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (!((keep >> e) & 1u)) x[32 * q + e] = -INFINITY;
           }
         } else {
           const uint32_t qm = t ? it.qmask[1] : it.qmask[0];

@@ -374,20 +374,25 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
           for (int e = 0; e < 64; ++e) x[e] = __uint_as_float(raw[e]);
         }
         if (kKind == kPrefillVS && it.cols) {
-          // chosen key j of the gathered chunk: admitted iff j <= row and its
-          // 64x64 tile is not active for this row block (the tile covers it)
-          const int s0 = 128 * it.idx + 64 * g;
-          const int32_t* V = P.vertical + static_cast<int64_t>(unit) * P.kv + s0;
-          const uint32_t* dist = P.tile_dist + static_cast<int64_t>(unit) * P.dist_words;
-          const int mblk = 2 * p + half;
+          // chosen key j of the gathered chunk's half g: admitted iff j <= row
+          // and its 64x64 tile is not active for this row block; the warp's
+          // bits from column_bits, the own block's keys checked per row
+          uint32_t adm[2], own[2];
+          int jv[2];
+          column_bits<2>(P, P.vertical + static_cast<int64_t>(unit) * P.kv,
+                         128 * it.idx + 64 * g,
+                         P.tile_dist + static_cast<int64_t>(unit) * P.dist_words, 2 * p + half,
+                         adm, own, jv);
 #pragma unroll
-          for (int e = 0; e < 64; ++e) {
-            bool keep = false;
-            if (s0 + e < P.kv) {
-              const int j = MSA_IDX(V[e], 0, P.g.N, P.status);
-              keep = j <= row && !dist_bit_checked(P, dist, mblk - (j >> 6));
+          for (int q = 0; q < 2; ++q) {
+            uint32_t keep = adm[q];
+            for (uint32_t ob = own[q]; ob; ob &= ob - 1) {  // warp-uniform: own[q] is a ballot
+              const int bit = __ffs(static_cast<int>(ob)) - 1;
+              if (__shfl_sync(0xffffffffu, jv[q], bit) <= row) keep |= 1u << bit;
             }
-            if (!keep) x[e] = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (!((keep >> e) & 1u)) x[32 * q + e] = -INFINITY;
           }
         } else if (lim < 63) {
 #pragma unroll
