@@ -52,12 +52,12 @@ UNIT = "TFLOP/s"
 MEASURED_TRAFFIC = {
     "workload": "mixed_128k",
     "kind": "vs",
-    "bytes": 2.529e9 + 0.654e9,
+    "bytes": 2.499e9 + 0.654e9,
     "sources": ("dynamic_sparse_attention_slash_gb300/csrc/prefill.cu",
                 "dynamic_sparse_attention_slash_gb300/csrc/prefill_common.cuh",
                 "dynamic_sparse_attention_slash_gb300/csrc/sm103_ptx.cuh",
                 "dynamic_sparse_attention_slash_gb300/csrc/msa_internal.h"),
-    "sha256": "46005435e7e9387d8e1020ca1d0d4a08194d5357189647cf5da2b30ed9e56fc6",
+    "sha256": "bde3bdca2f98084cc1347e361fb22760de9fc8c1a5c3633fec37e9ac6b40c0df",
 }
 
 
