@@ -55,8 +55,9 @@ constexpr int kStagesK = 3;
 constexpr int kStagesV = 2;
 // A sum of at most 2^15 over a half row bounds each of its p: P fits f16.
 constexpr float kSumLimit = 32768.f;
-// TMEM columns: S/P of item i at kColS + 128 (i & 1), O at kColO
-constexpr uint32_t kColS = 0, kColO = 256;
+// TMEM columns: S of item i at kColS + 128 (i & 1), O at kColO, P (f16 pairs)
+// of item i at kColP + 64 (i & 1)
+constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
 
 struct __align__(1024) TileSmem {
   uint8_t q[kTileBytes];
@@ -293,10 +294,13 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
       const uint64_t k_desc0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
       const uint64_t v_desc0 = sdesc_sw128(smem_u32(sm.v[0]), kHalfBytes, 1024);
       constexpr uint64_t kStageStep = kTileBytes >> 4;
-      // S(i) = Q K(i)^T into S buffer i & 1; its completion releases the K stage
+      // S(i) = Q K(i)^T into S buffer i & 1; its completion releases the K stage.
+      // K(0) and K(1) are waited for here; K(i) for i >= 2 has landed once P(i - 2)
+      // is complete (a softmax warp waits for it before that arrival), so the
+      // MMA thread waits only on P (a wait on this thread stalls its MMA stream).
       auto issue_s = [&](int i) -> bool {
         const int sk = i % kStagesK;
-        if (!mbar_wait(&sm.k_full[sk], (i / kStagesK) & 1, abort)) return false;
+        if (i < 2 && !mbar_wait(&sm.k_full[sk], (i / kStagesK) & 1, abort)) return false;
         tc_fence_after();
         const uint64_t kd = k_desc0 + sk * kStageStep;
         const uint32_t s_tm = tmem + kColS + 128 * (i & 1);
@@ -310,26 +314,34 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
         return true;
       };
       // O += P(i) V(i); its completion releases the V stage (and tells the
-      // softmax that O holds items 0..i)
-      auto issue_pv = [&](int i) -> bool {
+      // softmax that O holds items 0..i and that P buffer i & 1 is free)
+      auto issue_pv = [&](int i) {
         const int sv = i % kStagesV;
-        if (!mbar_wait(&sm.v_full[sv], (i / kStagesV) & 1, abort)) return false;
-        if (!mbar_wait(&sm.p_full[i & 1], (i >> 1) & 1, abort)) return false;
-        tc_fence_after();
         const uint64_t vd = v_desc0 + sv * kStageStep;
-        const uint32_t p_tm = tmem + kColS + 128 * (i & 1);
+        const uint32_t p_tm = tmem + kColP + 64 * (i & 1);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_ts(tmem + kColO, p_tm + kk * 8, vd + ((kk * 2048) >> 4), idO,
                  (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&sm.v_empty[sv]);
-        return true;
       };
-      // S(i + 1) is computed while the softmax works on S(i)
+      // P(i) complete means the softmax is done with S(i) and V(i) has
+      // landed: S(i + 2) goes into S(i)'s buffer ahead of P(i) V(i), so the
+      // softmax of item i + 1 (on S(i + 1), issued a step earlier) overlaps
+      // both products and S(i + 2) is ready before P(i) V(i) runs
       if (ok && n > 0) ok = issue_s(0);
+      if (ok && n > 1) ok = issue_s(1);
       for (int i = 0; ok && i < n; ++i) {
-        if (i + 1 < n && !issue_s(i + 1)) ok = false;
-        else if (!issue_pv(i)) ok = false;
+        if (!mbar_wait(&sm.p_full[i & 1], (i >> 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (i + 2 < n && !issue_s(i + 2)) {
+          ok = false;
+          break;
+        }
+        issue_pv(i);
       }
       // every MMA issued above must complete before TMEM is released
       mma_commit(&sm.final_bar);
@@ -351,13 +363,14 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t o_col = lane_base + kColO + 64 * g;
     float m_run = -INFINITY, l_run = 0.f;
-    bool ok = true;
+    bool ok = true, loads_ok = true;
     int k = 0;  // items processed so far
     for (; k < T.n;) {
       const Item it = get_item<kKind>(P, T, k, p);
       const uint32_t s_col = lane_base + kColS + 128 * (k & 1);
       // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
-      const bool waited = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[k & 1], (k >> 1) & 1, abort));
+      const bool waited =
+          __all_sync(0xffffffffu, mbar_wait(&sm.s_full[k & 1], (k >> 1) & 1, abort)) && loads_ok;
       tc_fence_after();
       // A key tile whose quadrant (row half, key half g) is not admitted leaves
       // this warp nothing to do: its half of P is zero, its maximum -inf.
@@ -470,7 +483,15 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
         if (!idle) rs = exps(x, m_run, pk);
       }
       l_run += rs;
-      tmem_st32(s_col + 32 * g, pk);  // f16 pairs of keys [64g, 64g + 64)
+      // P buffer k & 1 was last read by P(k - 2) V(k - 2): its completion
+      // released V stage (k - 2) % kStagesV
+      if (k >= 2) {
+        const int j = k - 2;
+        loads_ok = __all_sync(0xffffffffu, mbar_wait(&sm.v_empty[j % kStagesV],
+                                                     (j / kStagesV) & 1, abort)) && loads_ok;
+        tc_fence_after();
+      }
+      tmem_st32(lane_base + kColP + 64 * (k & 1) + 32 * g, pk);  // f16 pairs of keys [64g, 64g + 64)
       // both warps of these rows take this branch together (same maxima)
       if (__any_sync(0xffffffffu, correct)) {
         // O must hold P(k-1) V(k-1) before it is rescaled: that product's
@@ -495,13 +516,22 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
       }
       tmem_st_wait();
       tc_fence_before();
+      // for the MMA thread: V(k) (warp 4) and K(k + 2) (warp 5) have landed
+      // before P(k) is released; a failed wait ends both warps of these rows
+      // at the next item's barrier
+      if (warp == 4)
+        loads_ok = __all_sync(0xffffffffu, mbar_wait(&sm.v_full[k % kStagesV],
+                                                     (k / kStagesV) & 1, abort)) && loads_ok;
+      else if (warp == 5 && k + 2 < T.n)
+        loads_ok = __all_sync(0xffffffffu, mbar_wait(&sm.k_full[(k + 2) % kStagesK],
+                                                     ((k + 2) / kStagesK) & 1, abort)) && loads_ok;
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.p_full[k & 1]);
       ++k;
     }
     // ---- epilogue: add the two halves' row sums (both warps arrive here)
     sm.xsum[g][r] = l_run;
-    ok = bar_red_and(pair_bar, 64, ok);
+    ok = bar_red_and(pair_bar, 64, ok && loads_ok);
     const float l_row = l_run + sm.xsum[g ^ 1][r];
     uint4 outv[8];
     const bool have = ok && k > 0 && l_row > 0.f;
