@@ -131,13 +131,27 @@ __device__ __forceinline__ Tile make_tile(const PrefillParams& P, int unit, int 
   return T;
 }
 
+// The two list entries of item i (block-sparse: its two slots; vertical-slash
+// block items: its two e2 entries), read apart from their decoding so that a
+// loop can fetch them an item ahead.
 template <int kKind>
-__device__ __forceinline__ Item get_item(const PrefillParams& P, const Tile& T, int i, int p) {
+__device__ __forceinline__ int2 item_raw(const PrefillParams& P, const Tile& T, int i) {
+  if (kKind == kPrefillBS) return make_int2(T.list[2 * i], T.list[2 * i + 1]);
+  if (i < T.n_chunks) return make_int2(0, 0);
+  const int t = i - T.n_chunks;
+  const int j0 = T.j_hi - 1 - 2 * t, j1 = j0 - 1;
+  const int32_t e0 = T.e2[MSA_IDX(j0, 0, P.e2_stride, P.status)];
+  return make_int2(e0, j1 >= T.j_lo ? T.e2[j1] : (e0 & ~3));  // a missing second entry: no flags
+}
+
+template <int kKind>
+__device__ __forceinline__ Item decode_item(const PrefillParams& P, const Tile& T, int i, int p,
+                                            int2 raw) {
   Item it;
   it.cols = false;
   it.idx = 0;
   if (kKind == kPrefillBS) {
-    const int32_t s0 = T.list[2 * i], s1 = T.list[2 * i + 1];
+    const int32_t s0 = raw.x, s1 = raw.y;
     const uint32_t f0 = static_cast<uint32_t>(s0 >> 16) & 3u, f1 = static_cast<uint32_t>(s1 >> 16) & 3u;
     it.blk[0] = MSA_IDX(s0 & 0xffff, 0, P.g.NB, P.status);
     it.blk[1] = MSA_IDX(s1 & 0xffff, 0, P.g.NB, P.status);
@@ -161,13 +175,9 @@ __device__ __forceinline__ Item get_item(const PrefillParams& P, const Tile& T, 
     it.qm = 0xFu;
     return it;
   }
-  const int t = i - T.n_chunks;
-  const int j0 = T.j_hi - 1 - 2 * t, j1 = j0 - 1;
-  const int32_t e0 = T.e2[MSA_IDX(j0, 0, P.e2_stride, P.status)];
-  const int32_t e1 = j1 >= T.j_lo ? T.e2[j1] : e0;
-  const bool second_row_block = 2 * p + 1 < P.g.NB;
-  uint32_t f0 = static_cast<uint32_t>(e0) & 3u, f1 = j1 >= T.j_lo ? static_cast<uint32_t>(e1) & 3u : 0u;
-  if (!second_row_block) {
+  const int32_t e0 = raw.x, e1 = raw.y;
+  uint32_t f0 = static_cast<uint32_t>(e0) & 3u, f1 = static_cast<uint32_t>(e1) & 3u;
+  if (2 * p + 1 >= P.g.NB) {  // no second row block
     f0 &= 1u;
     f1 &= 1u;
   }
@@ -175,6 +185,11 @@ __device__ __forceinline__ Item get_item(const PrefillParams& P, const Tile& T, 
   it.blk[1] = MSA_IDX(2 * p - ((e1 >> 2) - 1), 0, P.g.NB, P.status);
   it.qm = (f0 & 1u) | ((f1 & 1u) << 1) | ((f0 >> 1) << 2) | ((f1 >> 1) << 3);
   return it;
+}
+
+template <int kKind>
+__device__ __forceinline__ Item get_item(const PrefillParams& P, const Tile& T, int i, int p) {
+  return decode_item<kKind>(P, T, i, p, item_raw<kKind>(P, T, i));
 }
 
 // TMA of the item's K (or V) rows into dst, completion on bar: keys of key
@@ -365,8 +380,18 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true, loads_ok = true;
     int k = 0;  // items processed so far
+    // block-sparse: the next item's list slots are read an item ahead, off the
+    // per-item path (vertical-slash reads its entries in place: the registers
+    // an early read holds cost that instantiation more than the read saves)
+    int2 raw = kKind == kPrefillBS && T.n > 0 ? item_raw<kKind>(P, T, 0) : make_int2(0, 0);
     for (; k < T.n;) {
-      const Item it = get_item<kKind>(P, T, k, p);
+      Item it;
+      if constexpr (kKind == kPrefillBS) {
+        it = decode_item<kKind>(P, T, k, p, raw);
+        if (k + 1 < T.n) raw = item_raw<kKind>(P, T, k + 1);
+      } else {
+        it = get_item<kKind>(P, T, k, p);
+      }
       const uint32_t s_col = lane_base + kColS + 128 * (k & 1);
       // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
       const bool waited =
