@@ -321,20 +321,13 @@ struct TileArgs {
 };
 
 // One warp per (unit, 128-row query tile p): the union U of the blocks kept by
-// row blocks 2p and 2p + 1, packed two blocks to an item, as blk | flags << 16
-// with flag bit a set when row block 2p + a kept it.  The softmax of an item
-// runs on the SM sub-partitions that own the admitting row halves (rows
-// 0-63 on two of them, 64-127 on the other two), so the pairing balances
-// them: blocks kept by both row blocks are paired with each other, and a block
-// kept by 2p only with one kept by 2p + 1 only (row half 0 then computes key
-// half 0 and row half 1 key half 1, one half each, instead of one row half
-// computing both while the other idles).  Items: the both-kept pairs, then the
-// complementary pairs, then the rest (an odd both-kept block, then the
-// one-sided blocks left over), each class ascending.  The kept blocks set bits
-// of two bitmaps in shared memory (one per row block); scans over their words
-// give each block its rank within its class.  An odd |U| leaves the last
-// item's second half a copy of the block before it with no flags (a valid load
-// that the softmax masks out).
+// row blocks 2p and 2p + 1, ascending, packed two blocks to an item.  The kept
+// blocks set bits of two bitmaps in shared memory (one per row block); a scan
+// over the words of their OR gives each block of U its rank r, and the block
+// goes to item r >> 1, key half r & 1, as blk | flags << 16 with flag bit a
+// set when row block 2p + a kept it.  An odd |U| leaves the last item's second
+// half a copy of its first block with no flags (a valid load that the softmax
+// masks out).
 __global__ void __launch_bounds__(32 * kTilesWarps) bs_tiles_kernel(TileArgs a) {
   extern __shared__ uint32_t tile_bits[];  // [kTilesWarps][2][words_per_warp / 2]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -358,63 +351,40 @@ __global__ void __launch_bounds__(32 * kTilesWarps) bs_tiles_kernel(TileArgs a) 
     }
   }
   __syncwarp();
-  // class sizes: kept by both (B), by row block 2p only (A0), by 2p + 1 only (A1)
-  int nB = 0, nA0 = 0, nA1 = 0;
-  for (int i = lane; i < words; i += 32) {
-    const uint32_t b0 = w0[i], b1 = w1[i];
-    nB += __popc(b0 & b1);
-    nA0 += __popc(b0 & ~b1);
-    nA1 += __popc(b1 & ~b0);
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    nB += __shfl_xor_sync(0xffffffffu, nB, off);
-    nA0 += __shfl_xor_sync(0xffffffffu, nA0, off);
-    nA1 += __shfl_xor_sync(0xffffffffu, nA1, off);
-  }
-  const int hB = nB >> 1;          // items of two both-kept blocks
-  const int m = min(nA0, nA1);     // complementary items
-  const int rest = 2 * (hB + m);   // first slot of the rest
-  const int oddB = nB & 1;
   int32_t* out = a.tiles + gid * a.tile_cap * 2;
-  auto put = [&](int slot, int blk, int flags) {
-    out[MSA_IDX(slot, 0, 2 * a.tile_cap, a.status)] = blk | (flags << 16);
-  };
-  int rB = 0, r0 = 0, r1 = 0;  // class ranks reached before this group of 32 words
+  int n = 0, last = 0;  // blocks of U placed so far; the largest of them
   for (int base = 0; base < words; base += 32) {
     const int i = base + lane;
     const uint32_t b0 = i < words ? w0[i] : 0u, b1 = i < words ? w1[i] : 0u;
-    uint32_t cB = b0 & b1, c0 = b0 & ~b1, c1 = b1 & ~b0;
-    // inclusive scans of the three counts over the lanes
-    int sB = __popc(cB), s0 = __popc(c0), s1 = __popc(c1);
-    const int oB = sB, o0 = s0, o1 = s1;
+    uint32_t u = b0 | b1;
+    const int cw = __popc(u);
+    int incl = cw;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      const int vB = __shfl_up_sync(0xffffffffu, sB, off);
-      const int v0 = __shfl_up_sync(0xffffffffu, s0, off);
-      const int v1 = __shfl_up_sync(0xffffffffu, s1, off);
-      if (lane >= off) {
-        sB += vB;
-        s0 += v0;
-        s1 += v1;
-      }
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
     }
-    int xB = rB + sB - oB, x0 = r0 + s0 - o0, x1 = r1 + s1 - o1;
-    for (; cB; cB &= cB - 1, ++xB)  // both-kept: pairs, an odd last one opens the rest
-      put(xB < 2 * hB ? xB : rest, 32 * i + __ffs(cB) - 1, 3);
-    for (; c0; c0 &= c0 - 1, ++x0)  // 2p only: key half 0 of a complementary item, or the rest
-      put(x0 < m ? 2 * (hB + x0) : rest + oddB + (x0 - m), 32 * i + __ffs(c0) - 1, 1);
-    for (; c1; c1 &= c1 - 1, ++x1)  // 2p + 1 only: key half 1, or the rest
-      put(x1 < m ? 2 * (hB + x1) + 1 : rest + oddB + (x1 - m), 32 * i + __ffs(c1) - 1, 2);
-    rB += __shfl_sync(0xffffffffu, sB, 31);
-    r0 += __shfl_sync(0xffffffffu, s0, 31);
-    r1 += __shfl_sync(0xffffffffu, s1, 31);
+    int r = n + incl - cw;
+    while (u) {
+      const int bit = __ffs(u) - 1;
+      u &= u - 1;
+      const int flags = static_cast<int>(((b0 >> bit) & 1u) | (((b1 >> bit) & 1u) << 1));
+      out[MSA_IDX(r, 0, 2 * a.tile_cap, a.status)] = (32 * i + bit) | (flags << 16);
+      ++r;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (total > 0) {  // the highest lane with a block holds the largest so far
+      const uint32_t has = __ballot_sync(0xffffffffu, cw > 0);
+      const int src = 31 - __clz(static_cast<int>(has));
+      const int top = cw > 0 ? 32 * i + 31 - __clz(static_cast<int>(b0 | b1)) : 0;
+      last = __shfl_sync(0xffffffffu, top, src);
+    }
+    n += total;
   }
-  const int total = rest + oddB + (nA0 - m) + (nA1 - m);
-  __syncwarp();  // every lane's slots are written and visible to lane 0
   if (lane == 0) {
-    if (total & 1) put(total, out[MSA_IDX(total - 1, 0, 2 * a.tile_cap, a.status)] & 0xffff, 0);
-    a.tile_count[gid] = (total + 1) >> 1;
+    if (n & 1) out[MSA_IDX(n, 0, 2 * a.tile_cap, a.status)] = last;  // second half of the last
+                                                                    // item: same block, no flags
+    a.tile_count[gid] = (n + 1) >> 1;
   }
 }
 

@@ -31,18 +31,24 @@
 //              into the scale) against the row's running max, decide together
 //              once per item (one named barrier) whether a row needs its max
 //              and only then exchange half-row maxima through shared memory,
-//              write P as f16 back over S, rescale their half of O in TMEM when
-//              the running max moves, and write their half of the output row.
+//              write P as f16 into the item's P buffer, rescale their half of
+//              O in TMEM when the running max moves, and write their half of
+//              the output row.  Before P(i) is released, warp 4 waits for V(i)
+//              and warp 5 for K(i + 2) to land, so the MMA thread waits on P
+//              alone (a wait on that thread stalls its MMA stream).
 //
-// TMEM (512 columns allocated): two S/P buffers at [0,128) and [128,256) for
-// even and odd items, the output accumulator O at [256,384).  S = Q K^T reads Q
-// and K from 128B-swizzled shared memory (K-major); O += P V reads P from TMEM
-// and V from shared memory (MN-major).  The MMA issue order is S(0), S(1),
-// PV(0), S(2), PV(1), ...: the tensor core computes S(i+1) while the softmax
-// works on S(i).  Every mbarrier wait is bounded (see sm103_ptx.cuh); a timeout
-// sets the status word and the CTA drains its copies and MMAs and exits.  The
-// named barriers between the two warps of a row group are reached by both on
-// every path (every wait before them is bounded and both leave together).
+// TMEM (512 columns allocated): two S buffers at [0,128) and [128,256) for even
+// and odd items, the output accumulator O at [256,384), two P buffers (f16
+// pairs) at [384,448) and [448,512).  S = Q K^T reads Q and K from
+// 128B-swizzled shared memory (K-major); O += P V reads P from TMEM and V from
+// shared memory (MN-major).  The MMA issue order is S(0), S(1), then per item
+// i, once P(i) is complete: S(i + 2) into S(i)'s buffer, then PV(i).  The
+// softmax of item i + 1 runs on S(i + 1) while the tensor core computes S(i + 2)
+// and PV(i); P(i + 2) is written once PV(i) has read its buffer.  Every
+// mbarrier wait is bounded (see sm103_ptx.cuh); a timeout sets the status word
+// and the CTA drains its copies and MMAs and exits.  The named barriers
+// between the two warps of a row group are reached by both on every path
+// (every wait before them is bounded and both leave together).
 #include "prefill_common.cuh"
 
 namespace msa {
