@@ -59,6 +59,7 @@ using namespace prefill;
 constexpr int kThreads = 384;
 constexpr int kStagesK = 3;
 constexpr int kStagesV = 2;
+constexpr int kRing = 8;  // decoded-item slots (more than kStagesK + 2)
 // A sum of at most 2^15 over a half row bounds each of its p: P fits f16.
 constexpr float kSumLimit = 32768.f;
 // TMEM columns: S of item i at kColS + 128 (i & 1), O at kColO, P (f16 pairs)
@@ -74,6 +75,7 @@ struct __align__(1024) TileSmem {
   uint64_t v_full[kStagesV], v_empty[kStagesV];
   uint64_t s_full[2], p_full[2];
   uint64_t final_bar;
+  int4 ring[kRing];       // decoded items, K producer -> softmax
   float xmax[2][2][128];  // half-row maxima [item parity][column half][row]
   float xsum[2][128];     // half-row sums at the end
   uint32_t tmem_base;
@@ -137,27 +139,13 @@ __device__ __forceinline__ Tile make_tile(const PrefillParams& P, int unit, int 
   return T;
 }
 
-// The two list entries of item i (block-sparse: its two slots; vertical-slash
-// block items: its two e2 entries), read apart from their decoding so that a
-// loop can fetch them an item ahead.
 template <int kKind>
-__device__ __forceinline__ int2 item_raw(const PrefillParams& P, const Tile& T, int i) {
-  if (kKind == kPrefillBS) return make_int2(T.list[2 * i], T.list[2 * i + 1]);
-  if (i < T.n_chunks) return make_int2(0, 0);
-  const int t = i - T.n_chunks;
-  const int j0 = T.j_hi - 1 - 2 * t, j1 = j0 - 1;
-  const int32_t e0 = T.e2[MSA_IDX(j0, 0, P.e2_stride, P.status)];
-  return make_int2(e0, j1 >= T.j_lo ? T.e2[j1] : (e0 & ~3));  // a missing second entry: no flags
-}
-
-template <int kKind>
-__device__ __forceinline__ Item decode_item(const PrefillParams& P, const Tile& T, int i, int p,
-                                            int2 raw) {
+__device__ __forceinline__ Item get_item(const PrefillParams& P, const Tile& T, int i, int p) {
   Item it;
   it.cols = false;
   it.idx = 0;
   if (kKind == kPrefillBS) {
-    const int32_t s0 = raw.x, s1 = raw.y;
+    const int32_t s0 = T.list[2 * i], s1 = T.list[2 * i + 1];
     const uint32_t f0 = static_cast<uint32_t>(s0 >> 16) & 3u, f1 = static_cast<uint32_t>(s1 >> 16) & 3u;
     it.blk[0] = MSA_IDX(s0 & 0xffff, 0, P.g.NB, P.status);
     it.blk[1] = MSA_IDX(s1 & 0xffff, 0, P.g.NB, P.status);
@@ -181,9 +169,13 @@ __device__ __forceinline__ Item decode_item(const PrefillParams& P, const Tile& 
     it.qm = 0xFu;
     return it;
   }
-  const int32_t e0 = raw.x, e1 = raw.y;
-  uint32_t f0 = static_cast<uint32_t>(e0) & 3u, f1 = static_cast<uint32_t>(e1) & 3u;
-  if (2 * p + 1 >= P.g.NB) {  // no second row block
+  const int t = i - T.n_chunks;
+  const int j0 = T.j_hi - 1 - 2 * t, j1 = j0 - 1;
+  const int32_t e0 = T.e2[MSA_IDX(j0, 0, P.e2_stride, P.status)];
+  const int32_t e1 = j1 >= T.j_lo ? T.e2[j1] : e0;
+  const bool second_row_block = 2 * p + 1 < P.g.NB;
+  uint32_t f0 = static_cast<uint32_t>(e0) & 3u, f1 = j1 >= T.j_lo ? static_cast<uint32_t>(e1) & 3u : 0u;
+  if (!second_row_block) {
     f0 &= 1u;
     f1 &= 1u;
   }
@@ -193,9 +185,44 @@ __device__ __forceinline__ Item decode_item(const PrefillParams& P, const Tile& 
   return it;
 }
 
-template <int kKind>
-__device__ __forceinline__ Item get_item(const PrefillParams& P, const Tile& T, int i, int p) {
-  return decode_item<kKind>(P, T, i, p, item_raw<kKind>(P, T, i));
+// Decoded items pass from the K producer to the softmax warps through a ring
+// in shared memory (an L2 read of the list entry per item sat on the softmax's
+// per-item path): slot i % kRing holds item i as {i, blk0 | blk1 << 16,
+// qm | cols << 4, idx}, its tag written last.  The producer writes item i
+// before loading K(i) and may only reach item i + kRing once P(i + kRing - 5)
+// is complete (K stage reuse), long after every softmax warp has read slot i.
+__device__ __forceinline__ void post_item(int4* ring, int i, const Item& it) {
+  volatile int* s = reinterpret_cast<volatile int*>(ring + (i % kRing));
+  s[1] = it.blk[0] | (it.blk[1] << 16);
+  s[2] = static_cast<int>(it.qm) | (it.cols ? 16 : 0);
+  s[3] = it.idx;
+  __threadfence_block();
+  s[0] = i;
+}
+// Item i from the ring; false (and a fully masked item) if its tag does not
+// appear within the wait limit or the CTA has aborted.
+__device__ __forceinline__ bool take_item(int4* ring, int i, volatile int* abort, Item& it) {
+  volatile int* s = reinterpret_cast<volatile int*>(ring + (i % kRing));
+  bool got = true;
+  if (s[0] != i) {
+    const uint64_t t0 = global_timer_ns();
+    while (s[0] != i) {
+      if (*abort || global_timer_ns() - t0 > MSA_WAIT_LIMIT_NS) {
+        *abort = 1;
+        got = false;
+        break;
+      }
+    }
+  }
+  got = __all_sync(0xffffffffu, got);
+  __threadfence_block();
+  const int y = s[1], z = s[2];
+  it.blk[0] = got ? (y & 0xffff) : 0;
+  it.blk[1] = got ? ((y >> 16) & 0xffff) : 0;
+  it.qm = got ? static_cast<uint32_t>(z) & 0xFu : 0u;
+  it.cols = got && (z & 16);
+  it.idx = got ? s[3] : 0;
+  return got;
 }
 
 // TMA of the item's K (or V) rows into dst, completion on bar: keys of key
@@ -251,6 +278,7 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
       mbar_init(&sm.p_full[t], 8);  // one arrival per softmax warp
     }
     mbar_init(&sm.final_bar, 1);
+    for (int s = 0; s < kRing; ++s) sm.ring[s].x = -1;
     sm.abort = 0;
     fence_mbar_init();
   }
@@ -276,8 +304,9 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
       for (int i = 0; i < T.n; ++i) {
         const int st = i % kStagesK;
         if (!mbar_wait(&sm.k_empty[st], ((i / kStagesK) & 1) ^ 1, abort)) break;
-        load_item(get_item<kKind>(P, T, i, p), sm.k[st], &mk64, &mkc64, &sm.k_full[st], hkv, b,
-                  crow0);
+        const Item it = get_item<kKind>(P, T, i, p);
+        post_item(sm.ring, i, it);
+        load_item(it, sm.k[st], &mk64, &mkc64, &sm.k_full[st], hkv, b, crow0);
         issued = i + 1;
       }
       // drain: the latest load of every stage, and Q, must land before exit
@@ -386,22 +415,30 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true, loads_ok = true;
     int k = 0;  // items processed so far
-    // block-sparse: the next item's list slots are read an item ahead, off the
-    // per-item path (vertical-slash reads its entries in place: the registers
-    // an early read holds cost that instantiation more than the read saves)
-    int2 raw = kKind == kPrefillBS && T.n > 0 ? item_raw<kKind>(P, T, 0) : make_int2(0, 0);
+    // Block-sparse items come from the ring one item ahead: the producer posts
+    // item k + 1 as soon as K(k + 1)'s stage is free, which the completion of
+    // S(k - 2) (before this warp starts item k) guarantees.  Vertical-slash
+    // items are taken in place (holding the next one costs that
+    // instantiation's registers more than the read saves).
+    Item nxt;
+    bool nxt_got = true;
+    if constexpr (kKind == kPrefillBS)
+      if (T.n > 0) nxt_got = take_item(sm.ring, 0, abort, nxt);
     for (; k < T.n;) {
       Item it;
+      bool got;
       if constexpr (kKind == kPrefillBS) {
-        it = decode_item<kKind>(P, T, k, p, raw);
-        if (k + 1 < T.n) raw = item_raw<kKind>(P, T, k + 1);
+        it = nxt;
+        got = nxt_got;
+        if (k + 1 < T.n) nxt_got = take_item(sm.ring, k + 1, abort, nxt);
       } else {
-        it = get_item<kKind>(P, T, k, p);
+        got = take_item(sm.ring, k, abort, it);
       }
       const uint32_t s_col = lane_base + kColS + 128 * (k & 1);
       // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
       const bool waited =
-          __all_sync(0xffffffffu, mbar_wait(&sm.s_full[k & 1], (k >> 1) & 1, abort)) && loads_ok;
+          __all_sync(0xffffffffu, mbar_wait(&sm.s_full[k & 1], (k >> 1) & 1, abort)) && loads_ok &&
+          got;
       tc_fence_after();
       // A key tile whose quadrant (row half, key half g) is not admitted leaves
       // this warp nothing to do: its half of P is zero, its maximum -inf.
