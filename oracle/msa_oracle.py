@@ -312,17 +312,23 @@ def block_scores(q, k, scale: float):
     return (mean_pool(q, N) @ mean_pool(k, N).T) * scale
 
 
-def block_sparse_blocks(q, k, topk: int, scale: float | None = None):
+def block_sparse_blocks(q, k, topk: int, scale: float | None = None, row_blocks=None):
     """Selected key blocks per row block [MInf-2.2]: the diagonal block plus the
     top-(topk-1) earlier blocks by pooled score (ties to the lower block);
-    min(topk, m+1) blocks, ascending."""
+    min(topk, m+1) blocks, ascending.  With row_blocks given, only those row
+    blocks are scored and selected: the lists and the score rows follow
+    row_blocks' order (each score row is that row of the full score matrix)."""
     N, d = q.shape
     scale = default_scale(d) if scale is None else scale
-    S = block_scores(q, k, scale)
-    NB = S.shape[0]
+    if row_blocks is None:
+        S = block_scores(q, k, scale)
+        rows = range(S.shape[0])
+    else:
+        rows = [int(m) for m in row_blocks]
+        S = (mean_pool(q, N)[rows] @ mean_pool(k, N).T) * scale
     sel = []
-    for m in range(NB):
-        earlier = topk_indices(S[m, :m], max(topk - 1, 0)) if m > 0 else np.zeros(0, np.int64)
+    for r, m in enumerate(rows):
+        earlier = topk_indices(S[r, :m], max(topk - 1, 0)) if m > 0 else np.zeros(0, np.int64)
         sel.append(np.sort(np.concatenate([earlier, [m]]).astype(np.int64)))
     return sel, S
 

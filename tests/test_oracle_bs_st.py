@@ -57,6 +57,24 @@ def test_block_selection_brute_force(topk):
         assert len(s) == min(topk, m + 1) and m in s.tolist()
 
 
+def test_row_restricted_selection_brute_force():
+    """Selecting for a few row blocks scores exactly those rows: brute force on
+    the pooled means, in the order the rows are given (ragged last block)."""
+    N, topk = 700, 4
+    rng = np.random.default_rng(6)
+    q, k = rng.standard_normal((N, D)), rng.standard_normal((N, D))
+    rows = [10, 0, 3, 7]
+    sel, S = O.block_sparse_blocks(q, k, topk, row_blocks=rows)
+    NB = (N + 63) // 64
+    kp = np.stack([k[64 * n:min(N, 64 * n + 64)].mean(0) for n in range(NB)])
+    for r, m in enumerate(rows):
+        qm = q[64 * m:min(N, 64 * m + 64)].mean(0)
+        want = (kp @ qm) / np.sqrt(D)
+        np.testing.assert_allclose(S[r], want, rtol=1e-12, atol=1e-12)
+        order = sorted(range(m), key=lambda n: (-want[n], n))[:topk - 1]
+        assert sel[r].tolist() == sorted(order + [m])
+
+
 def test_diagonal_block_kept_even_when_it_scores_lowest():
     N = 256
     rng = np.random.default_rng(4)
