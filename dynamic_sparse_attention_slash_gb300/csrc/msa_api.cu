@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <utility>
 
 #include <cudaTypedefs.h>
 
@@ -38,9 +39,24 @@ int check_tensor(const msa_tensor* t) {
   if (t->D != kHeadDim) return MSA_ERR_UNSUPPORTED;
   if (t->N > (int64_t{1} << 21)) return MSA_ERR_UNSUPPORTED;
   if (!aligned(t->data, 16)) return MSA_ERR_INVALID;
-  if (t->sn < t->D || t->sn % 8 || t->sh % 8 || t->sb % 8 || t->sh < 0 || t->sb < 0)
+  if (t->sn % 8 || t->sh % 8 || t->sb % 8 || t->sn < 0 || t->sh < 0 || t->sb < 0)
     return MSA_ERR_INVALID;
-  if (t->H > 1 && t->sh < t->sn) return MSA_ERR_INVALID;
+  // Distinct indices must address distinct elements, in any dimension order
+  // ([B, H, N, D] or the [B, N, H, D] storage of a projection, seen as a view):
+  // with the dimensions of extent > 1 taken by increasing stride, each stride
+  // must pass the largest offset the smaller ones reach.
+  int64_t st[4] = {1, t->sn, t->sh, t->sb}, ex[4] = {t->D, t->N, t->H, t->B};
+  for (int i = 1; i < 4; ++i)  // insertion sort by stride
+    for (int j = i; j > 0 && st[j] < st[j - 1]; --j) {
+      std::swap(st[j], st[j - 1]);
+      std::swap(ex[j], ex[j - 1]);
+    }
+  int64_t reach = 0;  // largest element offset of the dimensions taken so far
+  for (int i = 0; i < 4; ++i) {
+    if (ex[i] == 1) continue;
+    if (st[i] <= reach) return MSA_ERR_INVALID;
+    reach += st[i] * (ex[i] - 1);
+  }
   return MSA_OK;
 }
 

@@ -20,7 +20,10 @@
  * Tensors   q and out are [B, Hq, N, D]; k and v are [B, Hkv, N, D]; all bf16 in
  *           device memory, innermost dimension contiguous, other strides given
  *           in elements and multiples of 8 (16 bytes), base addresses 16-byte
- *           aligned.  Query head h reads KV head h / (Hq / Hkv).
+ *           aligned.  The strides may order the dimensions in any way (a
+ *           [B, N, H, D] buffer passes as sb = N H D, sh = D, sn = H D) as
+ *           long as distinct indices address distinct elements; anything else
+ *           is MSA_ERR_INVALID.  Query head h reads KV head h / (Hq / Hkv).
  * Supported D = 128, 1 <= N <= 2^21, Hq a multiple of Hkv.  Other shapes return
  *           MSA_ERR_UNSUPPORTED before anything is enqueued.  When N is not a
  *           multiple of 64 the block formats treat the last block as a padded

@@ -88,6 +88,7 @@ def test_workspace_bytes(lib):
     ("flags", 1), ("lastq", 1), ("head_range", 1), ("head_dup", 1), ("no_ws", 3),
     ("small_ws", 3), ("ws_align", 3), ("odd_stride", 1), ("n_mismatch", 1),
     ("out_is_q", 1), ("out_overlaps_v", 1), ("ws_overlaps_k", 3),
+    ("rows_overlap", 1), ("heads_alias", 1), ("bnhd_layout", 3), ("bnhd_rows_overlap", 1),
 ])
 def test_vertical_slash_rejects(lib, case, expect):
     q, k, v, out = T(), T(H=2), T(H=2), T()
@@ -130,6 +131,15 @@ def test_vertical_slash_rejects(lib, case, expect):
         out = T(ptr=v.data + (2 * 1024 * 128 - 64) * 2)
     elif case == "ws_overlaps_k":
         o.workspace = k.data + 0x1000
+    elif case == "rows_overlap":  # row i + 1 starts inside row i
+        q = T(sn=64)
+    elif case == "heads_alias":  # every head on the same memory
+        q = T(sh=0)
+    elif case == "bnhd_layout":  # [B, N, H, D] storage seen as [B, H, N, D]: valid,
+        q = T(sn=4 * 128, sh=128, sb=1024 * 4 * 128)  # stops at the missing workspace
+        o = None
+    elif case == "bnhd_rows_overlap":  # heads interleaved with too small a row stride
+        q = T(sn=2 * 128, sh=128, sb=1024 * 4 * 128)
     assert call_vs(lib, q, k, v, out, kv=kv, o=o) == expect
 
 
