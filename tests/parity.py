@@ -29,7 +29,7 @@ def to_np(t):
     return t.detach().to("cpu", torch.float64).numpy()
 
 
-def run_vs(q, k, v, vertical_topk, slash, last_q=64, heads=None):
+def run_vs(q, k, v, vertical_topk, slash, last_q=64, heads=None, scale=None):
     """CUDA vertical-slash call with index export; returns (out, export dict of numpy)."""
     B, Hq, N, _ = q.shape
     heads_l = list(range(Hq)) if heads is None else list(heads)
@@ -38,7 +38,7 @@ def run_vs(q, k, v, vertical_topk, slash, last_q=64, heads=None):
     dev = q.device
     ex = vs_export_buffers(U, N, kv, ks, dev)
     out = msa.msa_vertical_slash(q, k, v, vertical_topk, slash, last_q=last_q, heads=heads,
-                                 export=ex)
+                                 export=ex, scale=scale)
     torch.cuda.synchronize()
     return out, {name: t.cpu().numpy() for name, t in ex.items()}
 

@@ -199,13 +199,13 @@ def test_block_sparse_selection_at_long_lengths(NB):
 
 
 # ----------------------------------------------------------------------------- vertical-slash
-def check_vs_case(q, k, v, vertical_topk, slash, last_q=64, heads=None):
-    out, ex = P.run_vs(q, k, v, vertical_topk, slash, last_q=last_q, heads=heads)
+def check_vs_case(q, k, v, vertical_topk, slash, last_q=64, heads=None, scale=None):
+    out, ex = P.run_vs(q, k, v, vertical_topk, slash, last_q=last_q, heads=heads, scale=scale)
     B, Hq, N, _ = q.shape
     G = Hq // k.shape[1]
     heads_l = list(range(Hq)) if heads is None else list(heads)
     qn, kn, vn = np64(q), np64(k), np64(v)
-    scale = 1 / math.sqrt(D)
+    scale = 1 / math.sqrt(D) if scale is None else scale
     NB = (N + 63) // 64
     for b in range(B):
         for t, h in enumerate(heads_l):
@@ -235,10 +235,29 @@ def test_vertical_slash_tiny_workload():
 
 @pytest.mark.parametrize("N,kv,ks,last_q", [(2368, 300, 200, 64), (1088, 130, 40, 64),
                                             (2048, 64, 2048, 32), (960, 960, 1, 64),
-                                            (64, 5, 3, 64)])
+                                            (64, 5, 3, 64), (1536, 100, 30, 1),
+                                            (4160, 200, 16, 8)])
 def test_vertical_slash_ragged(N, kv, ks, last_q):
     q, k, v = qkv(1, 4, 2, N, 15)
     check_vs_case(q, k, v, kv, ks, last_q=last_q)
+
+
+@pytest.mark.parametrize("N,ks,scale", [(2368, 200, 0.03), (4160, 16, 0.2)])
+def test_vertical_slash_custom_scale(N, ks, scale):
+    """A softmax scale other than 1/sqrt(d) on both prefill kernels (128 * 16 <
+    4160: the one-query-tile kernel), estimate included."""
+    q, k, v = qkv(1, 4, 2, N, 21)
+    check_vs_case(q, k, v, 150, ks, scale=scale)
+
+
+def test_streaming_custom_scale():
+    q, k, v = qkv(2, 4, 2, 2500, 22)
+    out = msa.msa_streaming(q, k, v, 2, 5, scale=0.25)
+    torch.cuda.synchronize()
+    ref, _ = O.streaming_forward(np64(q), np64(k), np64(v), 2, 5, scale=0.25)
+    for b in range(2):
+        for h in range(4):
+            P.compare_out(np64(out[b, h]), ref[b, h], f"streaming scale b{b} h{h}")
 
 
 def test_vertical_slash_batch_and_head_subset():
