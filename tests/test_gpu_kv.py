@@ -87,11 +87,13 @@ def oracle_kv(qn, kn, mask, window, lse_rows):
     return lse, S
 
 
-@pytest.mark.parametrize("N,window,keep_k", [(2048, 64, 256), (1088, 100, 64), (1024, 1, 16)])
-def test_vertical_slash_kv_select(N, window, keep_k):
+# slash 16 at N = 4160: 128 * 16 < N, the one-query-tile kernel writes the lse
+@pytest.mark.parametrize("N,window,keep_k,slash", [(2048, 64, 256, 300), (1088, 100, 64, 300),
+                                                   (1024, 1, 16, 300), (4160, 64, 256, 16)])
+def test_vertical_slash_kv_select(N, window, keep_k, slash):
     q, k, v = qkv(1, 2, 1, N, 21)
     kv = msa.kv_select_buffers(q, window, keep_k)
-    _, ex = run_vs_kv(q, k, v, 200, 300, kv)
+    _, ex = run_vs_kv(q, k, v, 200, slash, kv)
     qn, kn = P.to_np(q[0]), P.to_np(k[0, 0])
     for h in range(2):
         mask = vs_mask_from_export(ex, h, N)
