@@ -70,8 +70,9 @@ def test_static_entry_rejects_on_host():
 
 
 # (seed, N, vertical_topk, slash): the second call is shorter, so its buffers
-# lie on the first call's leftovers in the array
-CALLS = [(41, 4096, 300, 500), (42, 2112, 130, 260)]
+# lie on the first call's leftovers in the array; the third runs the
+# one-query-tile kernel (128 * 16 < N) over both
+CALLS = [(41, 4096, 300, 500), (42, 2112, 130, 260), (43, 4160, 200, 16)]
 
 
 @pytest.mark.gpu
