@@ -16,7 +16,7 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 SUITES = ["tests/test_gpu_parity.py", "tests/test_gpu_edge_cases.py", "tests/test_gpu_hip.py",
-          "tests/test_gpu_ragged.py", "tests/test_gpu_kv.py"]
+          "tests/test_gpu_ragged.py", "tests/test_gpu_kv.py", "tests/test_gpu_layouts.py"]
 
 
 @pytest.mark.gpu
