@@ -260,6 +260,37 @@ def test_streaming_custom_scale():
             P.compare_out(np64(out[b, h]), ref[b, h], f"streaming scale b{b} h{h}")
 
 
+def test_eight_query_heads_per_kv_head():
+    """GQA with eight query heads on one KV head (the ratio of Llama-3-70B's
+    layers): vertical-slash on both prefill kernels, block-sparse and
+    streaming heads, each against the oracle."""
+    N = 2240
+    q, k, v = qkv(1, 8, 1, N, 25, bs=True)
+    check_vs_case(q, k, v, 150, 300, heads=[0, 5])   # 128 * 300 >= N: two query tiles
+    check_vs_case(q, k, v, 150, 12, heads=[7, 2])    # 128 * 12 < N: one query tile
+    out, ex = P.run_bs(q, k, v, 7, heads=[3, 6])
+    qn, kn, vn = np64(q), np64(k), np64(v)
+    NB = (N + 63) // 64
+    for u, h in enumerate([3, 6]):
+        sel, S = O.block_sparse_blocks(qn[0, h], kn[0, 0], 7)
+        gpu_sel = []
+        for m in range(NB):
+            cnt = int(ex["block_count"][u, m])
+            assert cnt == min(7, m + 1)
+            got = ex["block_ids"][u, m, :cnt]
+            if m > 0:
+                P.check_topk(got[:-1], S[m, :m], 6, f"bs h{h} m{m}")
+            gpu_sel.append(got.astype(np.int64))
+        ref, _ = O.attend_blocks(qn[0, h], kn[0, 0], vn[0, 0], O.block_mask_from_blocks(gpu_sel, N),
+                                 1 / math.sqrt(D))
+        P.compare_out(np64(out[0, h]), ref, f"bs h{h}")
+    out = msa.msa_streaming(q, k, v, 1, 3, heads=[1, 4])
+    torch.cuda.synchronize()
+    ref, _ = O.streaming_forward(qn, kn, vn, 1, 3, heads=[1, 4])
+    P.compare_out(np64(out[0, 1]), ref[0, 0], "streaming h1")
+    P.compare_out(np64(out[0, 4]), ref[0, 1], "streaming h4")
+
+
 def test_vertical_slash_batch_and_head_subset():
     q, k, v = qkv(2, 4, 1, 1024, 16)
     check_vs_case(q, k, v, 100, 150, heads=[2, 1])
