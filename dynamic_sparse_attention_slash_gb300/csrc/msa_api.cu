@@ -402,6 +402,10 @@ PrefillParams base_prefill(const Call& c, msa_tensor* out, uint32_t* status,
   p.status = status;
   p.vmax = vmax;
   p.units = c.u;
+  // K and the f16 copy of v of the KV heads the call reads, against L2 (128 MiB)
+  const int64_t kv_bytes = static_cast<int64_t>(kv_heads_of(c.g.Hkv, c.g.G, c.u).n) * c.g.B *
+                           c.g.N * kHeadDim * 4;
+  p.units_fast = kv_bytes <= (int64_t{128} << 20) ? 1 : 0;
   return p;
 }
 

@@ -130,6 +130,11 @@ struct PrefillParams {
   const uint32_t* vmax;
   uint32_t* status;
   UnitMap units;
+  // grid order: 0 — x enumerates a unit's query tiles (heavy first), y the
+  // units, so the CTAs resident at a time read nearby K/V of one KV head; 1 —
+  // x enumerates the units, y the tiles (heavy first over every unit), when
+  // the K/V the call reads fit L2 and only the balance of the last waves counts
+  int units_fast;
 };
 
 // Key set J_i of the call's attention, for the KV-selection score: which 64-key

@@ -208,8 +208,8 @@ sparse_prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_cons
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int unit = blockIdx.y;
-  const int c = P.npair - 1 - static_cast<int>(blockIdx.x);  // heavy (late) pairs first
+  const int unit = P.units_fast ? blockIdx.x : blockIdx.y;
+  const int c = P.npair - 1 - static_cast<int>(P.units_fast ? blockIdx.y : blockIdx.x);  // heavy first
   const int pA = 2 * c;
   const int b = unit_batch(P, unit), h = unit_head(P, unit), hkv = h / P.g.G;
   volatile int* abort = &sm.abort;
@@ -596,7 +596,8 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& mq, const 
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (p.g.n_units == 0 || p.npair == 0) return cudaSuccess;
-  sparse_prefill_kernel<<<dim3(p.npair, p.g.n_units), kThreads, smem, st>>>(p, mq, mk, mv, mkc, mvc);
+  const dim3 grid = p.units_fast ? dim3(p.g.n_units, p.npair) : dim3(p.npair, p.g.n_units);
+  sparse_prefill_kernel<<<grid, kThreads, smem, st>>>(p, mq, mk, mv, mkc, mvc);
   e = cudaGetLastError();
   if (e == cudaSuccess) ++*n_launch;
   return e;

@@ -256,8 +256,8 @@ sparse_prefill_tile_kernel(const __grid_constant__ PrefillParams P, const __grid
   TileSmem& sm = *reinterpret_cast<TileSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int unit = blockIdx.y;
-  const int p = P.g.NQ - 1 - static_cast<int>(blockIdx.x);  // heavy (late) tiles first
+  const int unit = P.units_fast ? blockIdx.x : blockIdx.y;
+  const int p = P.g.NQ - 1 - static_cast<int>(P.units_fast ? blockIdx.y : blockIdx.x);  // heavy first
   const Tile T = make_tile<kKind>(P, unit, p);
   const int b = unit_batch(P, unit), h = unit_head(P, unit), hkv = h / P.g.G;
   const int crow0 = unit * P.kv_pad;  // the unit's gathered column rows (vertical-slash)
@@ -662,7 +662,8 @@ cudaError_t launch_prefill_tile(const PrefillParams& p, const CUtensorMap& mq,
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (p.g.n_units == 0 || p.g.NQ == 0) return cudaSuccess;
-  kernel<<<dim3(p.g.NQ, p.g.n_units), kThreads, smem, st>>>(p, mq, mk64, mv64, mkc64, mvc64);
+  const dim3 grid = p.units_fast ? dim3(p.g.n_units, p.g.NQ) : dim3(p.g.NQ, p.g.n_units);
+  kernel<<<grid, kThreads, smem, st>>>(p, mq, mk64, mv64, mkc64, mvc64);
   e = cudaGetLastError();
   if (e == cudaSuccess) ++*n_launch;
   return e;
