@@ -52,12 +52,12 @@ UNIT = "TFLOP/s"
 MEASURED_TRAFFIC = {
     "workload": "mixed_128k",
     "kind": "vs",
-    "bytes": 2.499e9 + 0.654e9,
+    "bytes": 2.500e9 + 0.654e9,
     "sources": ("dynamic_sparse_attention_slash_gb300/csrc/prefill.cu",
                 "dynamic_sparse_attention_slash_gb300/csrc/prefill_common.cuh",
                 "dynamic_sparse_attention_slash_gb300/csrc/sm103_ptx.cuh",
                 "dynamic_sparse_attention_slash_gb300/csrc/msa_internal.h"),
-    "sha256": "bde3bdca2f98084cc1347e361fb22760de9fc8c1a5c3633fec37e9ac6b40c0df",
+    "sha256": "dfaef1d9e422347163dddd5b709e13ce86816d072b1a65a4aa4aca3365612a4c",
 }
 
 
